@@ -1,0 +1,145 @@
+"""Seeded synthetic inputs for the gated delta-rule state update.
+
+This module is shared by the CUDA path's tests and benchmark and by the CPU
+oracle's tests. It holds no arithmetic of the method itself: it only draws
+random tensors with the shapes and value distributions of the decode and
+prefill workloads and returns them as contiguous fp32 NumPy arrays in the
+library's canonical layouts.
+
+Layouts (row-major, fp32):
+  S        [B][vh][kd][vd]     one state per (sequence, value head)
+  q, k     [B][T][kh][kd]      T tokens per call (T = 1 for a single step)
+  v        [B][T][vh][vd]
+  g, beta  [B][T][vh]
+
+Distributions (drawn in fp64 with NumPy's PCG64, transformed in fp64, cast to
+fp32 once):
+  S     ~ N(0, 0.02^2)  (std 0.02), or zeros for prefill
+  q, k  ~ N(0, 1) per element, then each (b, t, key-head) row scaled to unit
+          L2 norm
+  v     ~ N(0, 1)
+  g     = -softplus(x) * g_scale,  x ~ N(0, 1)   (log-domain decay, < 0)
+  beta  = sigmoid(x),              x ~ N(0, 1)
+
+Draw order from a single generator: S, q, k, v, g-source, beta-source.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+
+# Seeds of the named workloads: workload i uses SEED_BASE + i.
+SEED_BASE = 20261202
+
+
+@dataclasses.dataclass
+class GDNInputs:
+    S: np.ndarray
+    q: np.ndarray
+    k: np.ndarray
+    v: np.ndarray
+    g: np.ndarray
+    beta: np.ndarray
+    B: int
+    T: int
+    kh: int
+    vh: int
+    kd: int
+    vd: int
+    seed: int
+
+    def step(self, t: int) -> "GDNInputs":
+        """The inputs of token t alone (T = 1), as contiguous arrays."""
+        sl = slice(t, t + 1)
+        return GDNInputs(
+            S=self.S, q=np.ascontiguousarray(self.q[:, sl]),
+            k=np.ascontiguousarray(self.k[:, sl]),
+            v=np.ascontiguousarray(self.v[:, sl]),
+            g=np.ascontiguousarray(self.g[:, sl]),
+            beta=np.ascontiguousarray(self.beta[:, sl]),
+            B=self.B, T=1, kh=self.kh, vh=self.vh, kd=self.kd, vd=self.vd,
+            seed=self.seed)
+
+    def tokens(self, t0: int, t1: int) -> "GDNInputs":
+        """Tokens t0..t1-1 as contiguous arrays (T = t1 - t0)."""
+        sl = slice(t0, t1)
+        return GDNInputs(
+            S=self.S, q=np.ascontiguousarray(self.q[:, sl]),
+            k=np.ascontiguousarray(self.k[:, sl]),
+            v=np.ascontiguousarray(self.v[:, sl]),
+            g=np.ascontiguousarray(self.g[:, sl]),
+            beta=np.ascontiguousarray(self.beta[:, sl]),
+            B=self.B, T=t1 - t0, kh=self.kh, vh=self.vh, kd=self.kd,
+            vd=self.vd, seed=self.seed)
+
+    def heads(self, b_idx, vi_idx) -> "GDNInputs":
+        """Restrict to sequences b_idx and value heads vi_idx.
+
+        vi_idx must be whole groups of value heads that share a key head
+        (contiguous runs of rep = vh // kh heads starting at a multiple of
+        rep), so the head mapping stays valid; the key heads kept are those
+        groups' key heads in the same order.
+        """
+        b_idx = np.asarray(b_idx, dtype=np.int64)
+        vi_idx = np.asarray(vi_idx, dtype=np.int64)
+        rep = self.vh // self.kh
+        if len(vi_idx) % rep or np.any(vi_idx.reshape(-1, rep)[:, 0] % rep) or \
+           np.any(np.diff(vi_idx.reshape(-1, rep), axis=1) != 1):
+            raise ValueError("vi_idx must be whole key-head groups")
+        kh_idx = vi_idx.reshape(-1, rep)[:, 0] // rep
+        return GDNInputs(
+            S=np.ascontiguousarray(self.S[b_idx][:, vi_idx]),
+            q=np.ascontiguousarray(self.q[b_idx][:, :, kh_idx]),
+            k=np.ascontiguousarray(self.k[b_idx][:, :, kh_idx]),
+            v=np.ascontiguousarray(self.v[b_idx][:, :, vi_idx]),
+            g=np.ascontiguousarray(self.g[b_idx][:, :, vi_idx]),
+            beta=np.ascontiguousarray(self.beta[b_idx][:, :, vi_idx]),
+            B=len(b_idx), T=self.T, kh=len(kh_idx), vh=len(vi_idx),
+            kd=self.kd, vd=self.vd, seed=self.seed)
+
+
+def _unit_rows(x: np.ndarray) -> np.ndarray:
+    n = np.sqrt(np.sum(x * x, axis=-1, keepdims=True))
+    return x / n
+
+
+def make_inputs(seed: int, B: int, T: int, kh: int = 16, vh: int = 48,
+                kd: int = 128, vd: int = 128, s_std: float = 0.02,
+                zero_state: bool = False, g_scale: float = 1.0) -> GDNInputs:
+    """Draw one workload's inputs (see the module docstring)."""
+    if vh % kh:
+        raise ValueError("vh must be a multiple of kh")
+    rng = np.random.Generator(np.random.PCG64(seed))
+    if zero_state:
+        S = np.zeros((B, vh, kd, vd), dtype=np.float32)
+    else:
+        S = (rng.standard_normal((B, vh, kd, vd)) * s_std).astype(np.float32)
+    q = _unit_rows(rng.standard_normal((B, T, kh, kd))).astype(np.float32)
+    k = _unit_rows(rng.standard_normal((B, T, kh, kd))).astype(np.float32)
+    v = rng.standard_normal((B, T, vh, vd)).astype(np.float32)
+    xg = rng.standard_normal((B, T, vh))
+    g = (-np.logaddexp(0.0, xg) * g_scale).astype(np.float32)
+    xb = rng.standard_normal((B, T, vh))
+    beta = (1.0 / (1.0 + np.exp(-xb))).astype(np.float32)
+    return GDNInputs(S=S, q=q, k=k, v=v, g=g, beta=beta, B=B, T=T, kh=kh,
+                     vh=vh, kd=kd, vd=vd, seed=seed)
+
+
+# The named workloads (sizes from the decode / verify / prefill scenarios).
+WORKLOADS = {
+    "decode_b1": dict(B=1, T=1),                 # one decode step, one sequence
+    "decode_b1_t64": dict(B=1, T=64),            # 64 chained decode steps
+    "decode_b64": dict(B=64, T=1),               # batched decode, HBM-bound
+    "verify_b32": dict(B=32, T=8),               # M-step verify, M in {2,4,8}
+    "prefill_b8_t4096": dict(B=8, T=4096, zero_state=True, g_scale=0.1),
+}
+
+WORKLOAD_SEED = {name: SEED_BASE + i for i, name in enumerate(WORKLOADS)}
+
+
+def make_workload(name: str, **overrides) -> GDNInputs:
+    kw = dict(WORKLOADS[name])
+    kw.update(overrides)
+    return make_inputs(WORKLOAD_SEED[name], **kw)
