@@ -1,0 +1,465 @@
+"""Benchmark of the gated delta-rule state update on GB300.
+
+Headline workload (one "step"): the batched decode step, 64 sequences x 48
+value heads (16 key heads), kd = vd = 128, fp32 state -- one launch of the
+token-serial kernel over 3072 heads, 406.9 MB of algorithmic HBM traffic.
+Three state sets (3 x 201 MB, larger than the 129 MB L2) rotate between
+steps, so every step reads its state from HBM.
+
+Also timed (the "parts" object): the M-token verify launch (32 x 48 heads,
+M = 2, 4, 8, with and without per-token checkpoints) and the prefill of
+8 x 4096 tokens x 48 heads.
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle on a
+bounded sample of the same workload instead.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdn|reference]
+Multi-GPU: launched by torchrun, one rank per GPU; each rank runs its own
+independent batch (weak scaling, no collective on the data path).
+"""
+
+from __future__ import annotations
+
+import argparse
+import datetime
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import gdn_inputs  # noqa: E402
+
+METRIC = "GDN head-steps/sec and achieved HBM GB/s (% of 8 TB/s) at 1 GB300"
+UNIT = "head-steps/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+NSETS = 3
+D = 128
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# --------------------------------------------------------------- bytes
+
+def decode_bytes(B, kh, vh, M=1, ckpt=False):
+    """Algorithmic HBM bytes of one launch over M tokens: the state read
+    once and written once (plus M checkpoints), the token inputs read and o
+    written once."""
+    state = B * vh * D * D * 4
+    qk = 2 * B * M * kh * D * 4
+    vo = 2 * B * M * vh * D * 4
+    gb = 2 * B * M * vh * 4
+    return 2 * state + (M * state if ckpt else 0) + qk + vo + gb
+
+
+# ------------------------------------------------------------- clocks
+
+CLOCK_FIELDS = ("timestamp,uuid,clocks.sm,clocks.max.sm,power.draw,"
+                "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+                "clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,"
+                "clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms in the background."""
+
+    def __init__(self):
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + CLOCK_FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(
+                    parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                continue
+            self.rows.append((ts, parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1, uuid=None):
+        rows = [p for ts, p in self.rows]
+        if uuid:
+            mine = [p for p in rows if uuid.lower() in p[1].lower()]
+            rows = mine or rows
+        inwin = [p for (ts, p) in self.rows if t0 <= ts <= t1 and p in rows]
+        use = inwin or rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "samples": 0, "note": "nvidia-smi unavailable"}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[2]) for p in use if num(p[2]) is not None]
+        mx = [num(p[3]) for p in use if num(p[3]) is not None]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap")
+        reasons = sorted({n for p in use for n, v in zip(names, p[6:10])
+                          if v.strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(use), "samples_in_timed_window": len(inwin),
+                "window": "timed" if inwin else "whole run (timed region "
+                          "shorter than the sampling period)"}
+
+
+# --------------------------------------------------------------- timing
+
+def time_launches(torch, fn, n, stream):
+    """Average device time of fn() over n launches, CUDA events on stream."""
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for i in range(n):
+        fn(i)
+    ev1.record(stream)
+    ev1.synchronize()
+    return ev0.elapsed_time(ev1) / n
+
+
+def kernel_traffic(kernel_src_files, name):
+    """Per-launch DRAM bytes from the committed ncu summary, or None when the
+    kernel source changed after the counters were taken."""
+    path = os.path.join(ROOT, "profiles", name)
+    try:
+        fields = dict(tok.split("=", 1) for tok in open(path).read().split()
+                      if "=" in tok)
+    except OSError:
+        return None
+    h = hashlib.sha256()
+    for f in kernel_src_files:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    if fields.get("source_sha256", "")[:16] != h.hexdigest()[:16]:
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# --------------------------------------------------------- CPU baseline
+
+def cpu_baseline(inp, seconds=10.0):
+    """The oracle, as it is, on the host cores: sequences of the headline
+    workload, one token each, repeated for about `seconds`."""
+    import oracle
+    oracle.build()
+    nseq = min(8, inp.B)
+    sub = inp.heads(range(nseq), range(inp.vh))
+    heads = sub.B * sub.vh
+    calls, t0 = 0, time.perf_counter()
+    while True:
+        oracle.run_inputs(sub)
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": heads * calls / el, "unit": UNIT,
+            "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"decode_b64 sequences 0-{nseq - 1} x {sub.vh} heads "
+                      f"({heads} head-steps per call), {calls} calls in "
+                      f"{el:.1f} s",
+            "gbs": decode_bytes(sub.B, sub.kh, sub.vh) * calls / el / 1e9}
+
+
+# ------------------------------------------------------------ reference
+
+def run_reference(args, rank, world):
+    """--impl reference: the CPU oracle timed as the reference arm."""
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    inp = gdn_inputs.make_workload("decode_b64")
+    one = inp.heads([0], range(inp.vh))
+    t0 = time.perf_counter()
+    oracle.run_inputs(one)
+    t1 = time.perf_counter() - t0
+    budget = 90.0 / max(1, args.steps + args.warmup)
+    nseq = int(max(1, min(inp.B, budget // max(t1, 1e-6))))
+    sub = inp.heads(range(nseq), range(inp.vh))
+    for _ in range(args.warmup):
+        oracle.run_inputs(sub)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.run_inputs(sub)
+    el = time.perf_counter() - t0
+    heads = sub.B * sub.vh
+    value = heads * args.steps / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": "decode_b64 (sampled: %d of 64 sequences x 48 "
+                   "heads per step)" % nseq, "B": 64, "kh": 16, "vh": 48,
+                   "kd": 128, "vd": 128, "seed": inp.seed},
+        "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle",
+                         "cores": oracle.threads(),
+                         "sample": f"{nseq} sequences x 48 heads per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------- main arm
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
+    ap.add_argument("--no-parts", action="store_true",
+                    help="skip the verify / prefill sub-measurements")
+    ap.add_argument("--no-cpu", action="store_true",
+                    help="skip the CPU-baseline leg")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    import gated_deltanet_linear_gb300 as gdn
+    from gated_deltanet_linear_gb300 import _build
+    _build.build()
+    gdn.load()
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream()
+    peaks, peak_kind = load_peaks()
+    hbm_peak = float(peaks["hbm_gbs"])
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x):
+        if dist is None:
+            return x
+        t = torch.tensor([x], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---- headline workload: batched decode step
+    inp = gdn_inputs.make_workload("decode_b64")
+    B, kh, vh = inp.B, inp.kh, inp.vh
+    tens = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    S0 = tens(inp.S)
+    states = [S0.clone() for _ in range(NSETS)]
+    del S0
+    q, k, v, g, beta = (tens(x) for x in (inp.q, inp.k, inp.v, inp.g, inp.beta))
+    o = torch.empty(B, 1, vh, D, device=dev)
+
+    def step(i):
+        gdn.gdn_step(states[i % NSETS], q, k, v, g, beta, o, stream=stream)
+
+    sampler = ClockSampler()
+    sampler.start()
+    time.sleep(0.3)
+    for i in range(args.warmup):
+        step(i)
+    barrier()
+    t_wall0 = time.time()
+    ms = time_launches(torch, step, args.steps, stream)
+    t_wall1 = time.time()
+    barrier()
+    ms = max_over_ranks(ms)
+    bytes_step = decode_bytes(B, kh, vh)
+    heads_per_step = B * vh
+    value = heads_per_step * world / (ms * 1e-3)
+    achieved_gbs = bytes_step / (ms * 1e-3) / 1e9
+
+    # ---- end to end through the public API with host buffers
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    h_in = [pin(x) for x in (inp.q, inp.k, inp.v, inp.g, inp.beta)]
+    d_in = [torch.empty_like(x, device=dev) for x in h_in]
+    h_o = torch.empty(tuple(o.shape), dtype=torch.float32).pin_memory()
+    h2d = sum(x.numel() * 4 for x in h_in)
+    d2h = h_o.numel() * 4
+
+    def e2e_step(i):
+        for hx, dx in zip(h_in, d_in):
+            dx.copy_(hx, non_blocking=True)
+        gdn.gdn_step(states[i % NSETS], *d_in, o, stream=stream)
+        h_o.copy_(o, non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    barrier()
+    ms_e2e = max_over_ranks(time_launches(torch, e2e_step, args.steps, stream))
+    e2e = {"value": heads_per_step * world / (ms_e2e * 1e-3), "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "ms_per_step": ms_e2e,
+           "note": "q, k, v, g, beta copied from pinned host memory and o "
+                   "copied back every step; the recurrent state stays "
+                   "resident on the device"}
+
+    # ---- parts: verify launches and prefill (rank 0 only, N = 1 shapes)
+    parts = {}
+    launches = args.steps  # headline timed region: one kernel per step
+    if not args.no_parts and rank == 0:
+        del states
+        torch.cuda.empty_cache()
+        vin = gdn_inputs.make_workload("verify_b32")
+        Sv = [tens(vin.S) for _ in range(NSETS)]
+        ck = torch.empty((8,) + tuple(vin.S.shape), device=dev)
+        for M in (2, 4, 8):
+            sub = vin.tokens(0, M)
+            vq, vk, vv, vg, vb = (tens(x) for x in
+                                  (sub.q, sub.k, sub.v, sub.g, sub.beta))
+            vo = torch.empty(sub.B, M, sub.vh, D, device=dev)
+            for use_ck in (False, True):
+                def vstep(i, M=M, use_ck=use_ck):
+                    s = Sv[i % NSETS]
+                    gdn.gdn_step_m(s, s, ck[:M] if use_ck else None, vq, vk,
+                                   vv, vg, vb, vo, M=M, stream=stream)
+                n = max(20, min(200, args.steps))
+                for i in range(5):
+                    vstep(i)
+                vms = time_launches(torch, vstep, n, stream)
+                nb = decode_bytes(sub.B, sub.kh, sub.vh, M, use_ck)
+                parts[f"verify_b32_m{M}{'_ckpt' if use_ck else ''}"] = {
+                    "ms": vms, "head_steps_per_s": sub.B * sub.vh * M / (vms * 1e-3),
+                    "gbs": nb / (vms * 1e-3) / 1e9,
+                    "frac_of_measured_hbm": nb / (vms * 1e-3) / 1e9 / hbm_peak,
+                    "bytes_per_launch": nb}
+        del Sv, ck
+        torch.cuda.empty_cache()
+        pin_ = gdn_inputs.make_workload("prefill_b8_t4096")
+        pq, pk, pv, pg, pb = (tens(x) for x in
+                              (pin_.q, pin_.k, pin_.v, pin_.g, pin_.beta))
+        Sp = tens(pin_.S)
+        po = torch.empty(pin_.B, pin_.T, pin_.vh, D, device=dev)
+
+        def pstep(i):
+            Sp.zero_()
+            gdn.gdn_prefill(Sp, pq, pk, pv, pg, pb, po,
+                            precision=gdn.GDN_PREC_FP32, stream=stream)
+        pstep(0)
+        pms = time_launches(torch, pstep, 3, stream)
+        toks = pin_.B * pin_.T
+        flops = 7 * D * D * toks * pin_.vh
+        parts["prefill_b8_t4096_fp32"] = {
+            "ms": pms, "tokens_per_s": toks / (pms * 1e-3),
+            "head_steps_per_s": toks * pin_.vh / (pms * 1e-3),
+            "tflops_fp32_equiv": flops / (pms * 1e-3) / 1e12,
+            "note": "token-serial fp32 path (includes a state memset)"}
+        del pq, pk, pv, pg, pb, Sp, po
+
+    sampler.stop()
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = None
+    clocks = sampler.summary(t_wall0, t_wall1, uuid)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    cpu = None
+    if world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(inp)
+
+    traffic = kernel_traffic(["gated_deltanet_linear_gb300/csrc/gdn_decode.cu"],
+                             "gdn_steps_decode_b64.traffic.txt")
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "decode_b64: batched decode step, B=64 "
+                   "sequences x vh=48 value heads (kh=16), kd=vd=128, fp32 "
+                   "state", "B": B, "kh": kh, "vh": vh, "kd": D, "vd": D,
+                   "seed": inp.seed,
+                   "l2": f"{NSETS} rotating state sets of "
+                         f"{B * vh * D * D * 4 / 1e6:.0f} MB (> 129 MB L2)",
+                   "bytes_per_step": bytes_step},
+        "hbm_gbs": achieved_gbs,
+        "hbm_frac_of_8tbs": achieved_gbs / NOMINAL_HBM_GBS,
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs,
+                     "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved_gbs / hbm_peak,
+                     "traffic": traffic, "peak_kind": peak_kind,
+                     "kernel": "gdn_steps_kernel<false>"},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "parts": parts,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

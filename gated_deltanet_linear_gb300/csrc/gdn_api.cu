@@ -1,0 +1,225 @@
+// C ABI of libgdn_gb300.so: argument validation on the host, then one
+// asynchronous launch on the caller's stream.  Declarations and the contract
+// of every entry point are in include/gdn.h.
+//
+// Conventions follow the articles' device library: device pointers plus a
+// stream, no implicit synchronisation ("24 · GDN linear attention to GPU",
+// section 11, the device-pointer layer step), an int status where a
+// refusal is an error code rather than a silent fallback (same article,
+// section 8; "34 · batched M rows", section 3.5), and no truncation of a
+// request that does not fit (article 24, section 10).
+
+#include <stdint.h>
+#include <string.h>
+
+#include "gdn.h"
+#include "gdn_internal.cuh"
+
+namespace {
+
+struct Buf {
+  const void *p;
+  size_t bytes;
+};
+
+bool overlaps(const Buf &a, const Buf &b) {
+  if (!a.p || !b.p || a.bytes == 0 || b.bytes == 0) return false;
+  const uintptr_t a0 = (uintptr_t)a.p, b0 = (uintptr_t)b.p;
+  return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Device (or managed) memory of the current device.
+int check_device_ptr(const void *p) {
+  cudaPointerAttributes attr;
+  memset(&attr, 0, sizeof(attr));
+  cudaError_t e = cudaPointerGetAttributes(&attr, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return GDN_EPTR;
+  }
+  if (attr.type == cudaMemoryTypeManaged) return GDN_OK;
+  if (attr.type != cudaMemoryTypeDevice) return GDN_EPTR;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return GDN_ECUDA;
+  }
+  return attr.device == dev ? GDN_OK : GDN_EPTR;
+}
+
+int check_shape(const gdn_shape *s) {
+  if (!s) return GDN_EINVAL;
+  if (s->B < 0 || s->kh <= 0 || s->vh <= 0) return GDN_ESHAPE;
+  if (s->kd != gdn::kDim || s->vd != gdn::kDim) return GDN_ESHAPE;
+  if (s->vh % s->kh) return GDN_ESHAPE;
+  return GDN_OK;
+}
+
+// Every buffer: non-null, 16-byte aligned, device memory.
+int check_bufs(const Buf *b, int n) {
+  for (int i = 0; i < n; ++i) {
+    if (!b[i].p) return GDN_EINVAL;
+    if (!aligned16(b[i].p)) return GDN_EALIGN;
+  }
+  for (int i = 0; i < n; ++i) {
+    const int r = check_device_ptr(b[i].p);
+    if (r != GDN_OK) return r;
+  }
+  return GDN_OK;
+}
+
+int status_of(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ECUDA; }
+
+size_t state_floats(const gdn_shape *s) {
+  return (size_t)s->B * s->vh * s->kd * s->vd;
+}
+
+// Validate and launch M serial tokens (shared by gdn_step, gdn_step_m and
+// the fp32 prefill path).
+int steps_common(const gdn_shape *s, int M, const float *S_in, float *S_out,
+                 float *ckpt, const float *q, const float *k, const float *v,
+                 const float *g, const float *beta, float *o,
+                 cudaStream_t stream) {
+  int r = check_shape(s);
+  if (r) return r;
+  if (M < 1 || M > GDN_MAX_TOKENS) return GDN_ERANGE;
+  if (s->B == 0) return GDN_OK;
+  const size_t sb = state_floats(s) * 4;
+  const size_t qkb = (size_t)s->B * M * s->kh * s->kd * 4;
+  const size_t vb = (size_t)s->B * M * s->vh * s->vd * 4;
+  const size_t gb = (size_t)s->B * M * s->vh * 4;
+  Buf in[] = {{S_in, sb}, {q, qkb}, {k, qkb}, {v, vb}, {g, gb}, {beta, gb}};
+  Buf out[] = {{S_out, sb}, {o, vb}, {ckpt, sb * (size_t)M}};
+  const int nout = ckpt ? 3 : 2;
+  r = check_bufs(in, 6);
+  if (r) return r;
+  r = check_bufs(out, nout);
+  if (r) return r;
+  // Outputs never overlap inputs or each other; the one exception is an
+  // in-place state (S_out == S_in exactly).
+  for (int i = 0; i < nout; ++i) {
+    for (int j = 0; j < 6; ++j) {
+      if (i == 0 && j == 0 && out[0].p == in[0].p) continue;
+      if (overlaps(out[i], in[j])) return GDN_EALIAS;
+    }
+    for (int j = i + 1; j < nout; ++j)
+      if (overlaps(out[i], out[j])) return GDN_EALIAS;
+  }
+  cudaGetLastError();  // start from a clean per-thread error state
+  return status_of(gdn::launch_steps(S_in, S_out, ckpt, q, k, v, g, beta, o,
+                                     s->B, s->kh, s->vh, M, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdn_step(const gdn_shape *shape, float *S, const float *q, const float *k,
+             const float *v, const float *g, const float *beta, float *o,
+             gdn_stream_t stream) {
+  return steps_common(shape, 1, S, S, nullptr, q, k, v, g, beta, o,
+                      (cudaStream_t)stream);
+}
+
+int gdn_step_m(const gdn_shape *shape, int M, const float *S_in, float *S_out,
+               float *ckpt, const float *q, const float *k, const float *v,
+               const float *g, const float *beta, float *o,
+               gdn_stream_t stream) {
+  return steps_common(shape, M, S_in, S_out, ckpt, q, k, v, g, beta, o,
+                      (cudaStream_t)stream);
+}
+
+int gdn_mark(const gdn_shape *shape, const float *S, float *snap,
+             gdn_stream_t stream) {
+  int r = check_shape(shape);
+  if (r) return r;
+  if (shape->B == 0) return GDN_OK;
+  const size_t n = state_floats(shape);
+  Buf b[] = {{S, n * 4}, {snap, n * 4}};
+  r = check_bufs(b, 2);
+  if (r) return r;
+  if (overlaps(b[0], b[1])) return GDN_EALIAS;
+  cudaGetLastError();
+  return status_of(gdn::launch_copy(snap, S, n, (cudaStream_t)stream));
+}
+
+int gdn_rollback(const gdn_shape *shape, int M, int m, const float *snap,
+                 const float *ckpt, float *S, gdn_stream_t stream) {
+  int r = check_shape(shape);
+  if (r) return r;
+  if (M < 1 || M > GDN_MAX_TOKENS || m < 0 || m > M) return GDN_ERANGE;
+  if (shape->B == 0) return GDN_OK;
+  const size_t n = state_floats(shape);
+  const float *src = m == 0 ? snap : (ckpt ? ckpt + (size_t)(m - 1) * n : nullptr);
+  Buf b[] = {{src, n * 4}, {S, n * 4}};
+  r = check_bufs(b, 2);
+  if (r) return r;
+  if (overlaps(b[0], b[1])) return GDN_EALIAS;
+  cudaGetLastError();
+  return status_of(gdn::launch_copy(S, src, n, (cudaStream_t)stream));
+}
+
+int gdn_rollback_seq(const gdn_shape *shape, int M, const int *m_dev,
+                     const float *snap, const float *ckpt, float *S,
+                     int *err_dev, gdn_stream_t stream) {
+  int r = check_shape(shape);
+  if (r) return r;
+  if (M < 1 || M > GDN_MAX_TOKENS) return GDN_ERANGE;
+  if (shape->B == 0) return GDN_OK;
+  const size_t n = state_floats(shape);
+  Buf b[] = {{snap, n * 4}, {ckpt, n * 4 * (size_t)M}, {S, n * 4},
+             {m_dev, (size_t)shape->B * 4}};
+  r = check_bufs(b, 4);
+  if (r) return r;
+  if (err_dev) {
+    if (((uintptr_t)err_dev & 3u) != 0) return GDN_EALIGN;
+    r = check_device_ptr(err_dev);
+    if (r) return r;
+  }
+  for (int j = 0; j < 4; ++j)
+    if (j != 2 && overlaps(b[2], b[j])) return GDN_EALIAS;
+  cudaGetLastError();
+  return status_of(gdn::launch_rollback_seq(S, snap, ckpt, m_dev, err_dev,
+                                            shape->B, shape->vh, M,
+                                            (cudaStream_t)stream));
+}
+
+size_t gdn_prefill_workspace(const gdn_shape *shape, int T, int chunk,
+                             int precision) {
+  if (check_shape(shape) || T < 1 || T > GDN_MAX_TOKENS) return 0;
+  (void)chunk;
+  (void)precision;
+  return 0;
+}
+
+int gdn_prefill(const gdn_shape *shape, int T, float *S, const float *q,
+                const float *k, const float *v, const float *g,
+                const float *beta, float *o, int chunk, int precision,
+                void *workspace, size_t ws_bytes, gdn_stream_t stream) {
+  (void)chunk;
+  (void)workspace;
+  (void)ws_bytes;
+  if (precision != GDN_PREC_FP32) return GDN_ERANGE;
+  return steps_common(shape, T, S, S, nullptr, q, k, v, g, beta, o,
+                      (cudaStream_t)stream);
+}
+
+const char *gdn_strerror(int status) {
+  switch (status) {
+    case GDN_OK: return "success";
+    case GDN_EINVAL: return "invalid argument (NULL pointer or bad value)";
+    case GDN_ESHAPE: return "unsupported shape (kd == vd == 128, vh % kh == 0, B >= 0)";
+    case GDN_EALIGN: return "pointer not 16-byte aligned";
+    case GDN_ECUDA: return "CUDA runtime error or kernel launch failure";
+    case GDN_ERANGE: return "count out of range (M, m, T, chunk, precision or workspace)";
+    case GDN_EPTR: return "pointer is not device memory of the current device";
+    case GDN_EALIAS: return "buffers overlap where they must not";
+    default: return "unknown status";
+  }
+}
+
+int gdn_version(void) { return 100; }
+
+}  // extern "C"

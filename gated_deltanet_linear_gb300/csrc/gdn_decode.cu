@@ -1,0 +1,321 @@
+// Token-serial gated delta-rule update for sm_103a (decode, M-token verify,
+// fp32 prefill).
+//
+// What it computes (per sequence b, value head vi, key head hh = vi / rep,
+// token m), "Kestrel_VLLM - 24 · GDN linear attention to GPU", section 4:
+//     alpha = exp(g);  S = alpha S;  kv = S^T k;  tmp = (v - kv) beta;
+//     S = S + k tmp^T;  o = S^T q.
+// The output is taken in the algebraically equal form
+//     o = alpha (S_old^T q) + (q . k) tmp,
+// so that S^T k, S^T q and q . k come out of one pass over the state and
+// the rank-1 update follows; the state after the update is the same
+// expression as in the definition.
+//
+// Work split.  A head's 128 x 128 state is 64 KB.  Warp w of a head owns
+// value columns [8w, 8w+8) over all 128 key rows, so every reduction over
+// the key dimension stays inside one warp (no shared memory, no barriers):
+//   lane = 16 * h + p,  p in 0..15 -> key rows 8p .. 8p+7,
+//                       h in 0..1  -> value columns 8w + 4h .. 8w + 4h + 3.
+// Each lane keeps its 8 x 4 block of S in registers for all M tokens, so
+// the state is read from HBM once and written once per launch however many
+// tokens it covers (the register-resident idea of "27 · register-resident &
+// fused launch", section 3, split over 16 warps instead of one thread per
+// column).  Loads and stores are 128-bit; one warp instruction touches 16
+// full 32-byte sectors.  A CTA is 4 warps = a quarter head, so a batch of
+// B*vh heads launches 4*B*vh CTAs.
+//
+// Determinism.  Every product and sum is an explicit round-to-nearest
+// intrinsic and the reduction tree is fixed, so a token gives the same bits
+// whether it is the only token of a launch or one of M: gdn_step_m(M) is
+// bit-identical to M gdn_step calls.
+
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kWarpsPerCta = 4;
+constexpr int kWarpsPerHead = kDim / 8;  // 16
+constexpr int kCtasPerHead = kWarpsPerHead / kWarpsPerCta;
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ float4 ld_stream(const float *p) {
+  float4 r;
+  asm("ld.global.cs.v4.f32 {%0, %1, %2, %3}, [%4];"
+      : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+      : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ void st_stream(float *p, float4 v) {
+  asm volatile("st.global.cs.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p),
+               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ float comp(const float4 &a, int i) {
+  return i == 0 ? a.x : (i == 1 ? a.y : (i == 2 ? a.z : a.w));
+}
+
+// The per-token inputs a lane needs: k and q for its 8 key rows, v for its 4
+// value columns, and the head's two scalars.
+struct TokenIn {
+  float4 k0, k1, q0, q1, v;
+  float g, beta;
+};
+
+__device__ __forceinline__ TokenIn load_token(const float *__restrict__ q,
+                                              const float *__restrict__ k,
+                                              const float *__restrict__ v,
+                                              const float *__restrict__ g,
+                                              const float *__restrict__ beta,
+                                              size_t qk_row, size_t v_row,
+                                              size_t gi) {
+  TokenIn t;
+  const float4 *kp = reinterpret_cast<const float4 *>(k + qk_row);
+  const float4 *qp = reinterpret_cast<const float4 *>(q + qk_row);
+  t.k0 = __ldg(kp);
+  t.k1 = __ldg(kp + 1);
+  t.q0 = __ldg(qp);
+  t.q1 = __ldg(qp + 1);
+  t.v = __ldg(reinterpret_cast<const float4 *>(v + v_row));
+  t.g = __ldg(g + gi);
+  t.beta = __ldg(beta + gi);
+  return t;
+}
+
+__device__ __forceinline__ float row_of(const TokenIn &t, bool isq, int j) {
+  const float4 &a = isq ? (j < 4 ? t.q0 : t.q1) : (j < 4 ? t.k0 : t.k1);
+  return comp(a, j & 3);
+}
+
+// Partial dot products of the lane's 8 rows with x (k or q), per column.
+__device__ __forceinline__ float4 partial_dot(const float4 (&s)[8],
+                                              const TokenIn &t, bool isq) {
+  float x0 = row_of(t, isq, 0);
+  float4 a = make_float4(__fmul_rn(s[0].x, x0), __fmul_rn(s[0].y, x0),
+                         __fmul_rn(s[0].z, x0), __fmul_rn(s[0].w, x0));
+#pragma unroll
+  for (int j = 1; j < 8; ++j) {
+    const float xj = row_of(t, isq, j);
+    a.x = __fmaf_rn(s[j].x, xj, a.x);
+    a.y = __fmaf_rn(s[j].y, xj, a.y);
+    a.z = __fmaf_rn(s[j].z, xj, a.z);
+    a.w = __fmaf_rn(s[j].w, xj, a.w);
+  }
+  return a;
+}
+
+// One token for the lane's 8 x 4 block.  Updates s in place and, on the
+// lanes that own an output element, writes it to o_col[c] (c = 0..3 is the
+// column within the lane's half-group).
+__device__ __forceinline__ void token_update(float4 (&s)[8], const TokenIn &t,
+                                             int lane, float *o_half) {
+  const int p = lane & 15;
+  const int half_base = lane & 16;
+
+  // 1. Partials over this lane's rows: S^T k and S^T q for 4 columns, q.k.
+  const float4 kv = partial_dot(s, t, false);
+  const float4 qs = partial_dot(s, t, true);
+  float qk = __fmul_rn(t.q0.x, t.k0.x);
+  qk = __fmaf_rn(t.q0.y, t.k0.y, qk);
+  qk = __fmaf_rn(t.q0.z, t.k0.z, qk);
+  qk = __fmaf_rn(t.q0.w, t.k0.w, qk);
+  qk = __fmaf_rn(t.q1.x, t.k1.x, qk);
+  qk = __fmaf_rn(t.q1.y, t.k1.y, qk);
+  qk = __fmaf_rn(t.q1.z, t.k1.z, qk);
+  qk = __fmaf_rn(t.q1.w, t.k1.w, qk);
+
+  // 2. Reduce-scatter the 8 column partials over the 16 lanes of the half
+  // (xor 8, 4, 2, 1).  Afterwards the lane holds the full sum of value
+  // index idx = 4*[p&8] + 2*[p&4] + [p&2]: idx < 4 is kv of column idx,
+  // idx >= 4 is S^T q of column idx - 4.
+  const bool b8 = p & 8, b4 = p & 4, b2 = p & 2;
+  float r4[4];
+  {
+    const float keep[4] = {b8 ? qs.x : kv.x, b8 ? qs.y : kv.y,
+                           b8 ? qs.z : kv.z, b8 ? qs.w : kv.w};
+    const float send[4] = {b8 ? kv.x : qs.x, b8 ? kv.y : qs.y,
+                           b8 ? kv.z : qs.z, b8 ? kv.w : qs.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      r4[i] = __fadd_rn(keep[i], __shfl_xor_sync(kFull, send[i], 8));
+  }
+  float r2[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float keep = b4 ? r4[i + 2] : r4[i];
+    const float send = b4 ? r4[i] : r4[i + 2];
+    r2[i] = __fadd_rn(keep, __shfl_xor_sync(kFull, send, 4));
+  }
+  float r1;
+  {
+    const float keep = b2 ? r2[1] : r2[0];
+    const float send = b2 ? r2[0] : r2[1];
+    r1 = __fadd_rn(keep, __shfl_xor_sync(kFull, send, 2));
+  }
+  const float red = __fadd_rn(r1, __shfl_xor_sync(kFull, r1, 1));
+  const int idx = (b8 ? 4 : 0) + (b4 ? 2 : 0) + (b2 ? 1 : 0);
+
+  // q . k over all 128 rows (each half holds every row once).
+  qk = __fadd_rn(qk, __shfl_xor_sync(kFull, qk, 8));
+  qk = __fadd_rn(qk, __shfl_xor_sync(kFull, qk, 4));
+  qk = __fadd_rn(qk, __shfl_xor_sync(kFull, qk, 2));
+  qk = __fadd_rn(qk, __shfl_xor_sync(kFull, qk, 1));
+
+  // 3. tmp = (v - alpha kv) beta on the kv lanes, then broadcast the four
+  // columns' tmp to the whole half.  Column c's kv lives on p = 4*(c>>1) +
+  // 2*(c&1).
+  const float alpha = expf(t.g);
+  const int col = idx & 3;
+  const float tmp_mine =
+      __fmul_rn(__fsub_rn(comp(t.v, col), __fmul_rn(alpha, red)), t.beta);
+  float tmp[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    tmp[c] = __shfl_sync(kFull, tmp_mine, half_base | (4 * (c >> 1) + 2 * (c & 1)));
+
+  // 4. o = alpha (S^T q) + (q . k) tmp on the S^T q lanes (even p only).
+  if (idx >= 4 && !(p & 1)) {
+    float tc = tmp[0];
+#pragma unroll
+    for (int c = 1; c < 4; ++c)
+      if (col == c) tc = tmp[c];
+    o_half[col] = __fmaf_rn(qk, tc, __fmul_rn(alpha, red));
+  }
+
+  // 5. Rank-1 update of the decayed state: S = alpha S + k tmp^T.
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float kj = row_of(t, false, j);
+    s[j].x = __fmaf_rn(kj, tmp[0], __fmul_rn(alpha, s[j].x));
+    s[j].y = __fmaf_rn(kj, tmp[1], __fmul_rn(alpha, s[j].y));
+    s[j].z = __fmaf_rn(kj, tmp[2], __fmul_rn(alpha, s[j].z));
+    s[j].w = __fmaf_rn(kj, tmp[3], __fmul_rn(alpha, s[j].w));
+  }
+}
+
+template <bool kCkpt>
+__global__ void __launch_bounds__(kWarpsPerCta * 32)
+    gdn_steps_kernel(const float *S_in, float *S_out,
+                     float *__restrict__ ckpt, const float *__restrict__ q,
+                     const float *__restrict__ k, const float *__restrict__ v,
+                     const float *__restrict__ g,
+                     const float *__restrict__ beta, float *__restrict__ o,
+                     int vh, int kh, int rep, int M, size_t nheads) {
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const size_t head = blockIdx.x / kCtasPerHead;
+  const int cg = (blockIdx.x % kCtasPerHead) * kWarpsPerCta + warp;
+  const int b = static_cast<int>(head / vh);
+  const int vi = static_cast<int>(head % vh);
+  const int hh = vi / rep;
+  const int p = lane & 15;
+  const int row0 = 8 * p;
+  const int col0 = 8 * cg + 4 * (lane >> 4);
+
+  const size_t hoff = head * (size_t)(kDim * kDim);
+  const size_t eoff = (size_t)row0 * kDim + col0;
+  float4 s[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) s[j] = ld_stream(S_in + hoff + eoff + j * kDim);
+
+  auto qk_row = [&](int m) {
+    return (((size_t)b * M + m) * kh + hh) * kDim + row0;
+  };
+  auto v_row = [&](int m) {
+    return (((size_t)b * M + m) * vh + vi) * kDim + col0;
+  };
+  auto g_idx = [&](int m) { return ((size_t)b * M + m) * vh + vi; };
+
+  TokenIn cur = load_token(q, k, v, g, beta, qk_row(0), v_row(0), g_idx(0));
+  for (int m = 0; m < M; ++m) {
+    TokenIn nxt = cur;
+    if (m + 1 < M)
+      nxt = load_token(q, k, v, g, beta, qk_row(m + 1), v_row(m + 1),
+                       g_idx(m + 1));
+    token_update(s, cur, lane, o + v_row(m));
+    if (kCkpt) {
+      float *cp = ckpt + (size_t)m * nheads * (kDim * kDim) + hoff + eoff;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) st_stream(cp + j * kDim, s[j]);
+    }
+    cur = nxt;
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) st_stream(S_out + hoff + eoff + j * kDim, s[j]);
+}
+
+__global__ void copy_kernel(float4 *__restrict__ dst,
+                            const float4 *__restrict__ src, size_t n4) {
+  size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (; i < n4; i += stride) dst[i] = __ldg(src + i);
+}
+
+// One CTA per (b, vi) head: copies the source the sequence's count selects.
+__global__ void rollback_seq_kernel(float4 *__restrict__ S,
+                                    const float4 *__restrict__ snap,
+                                    const float4 *__restrict__ ckpt,
+                                    const int *__restrict__ m_dev,
+                                    int *__restrict__ err, int vh, int M,
+                                    size_t nheads) {
+  const size_t head = blockIdx.x;
+  const int b = static_cast<int>(head / vh);
+  const int m = __ldg(m_dev + b);
+  constexpr size_t n4 = kDim * kDim / 4;
+  if (m < 0 || m > M) {
+    if (err && threadIdx.x == 0) *err = 1;
+    return;
+  }
+  const float4 *src = m == 0 ? snap + head * n4
+                             : ckpt + ((size_t)(m - 1) * nheads + head) * n4;
+  float4 *dst = S + head * n4;
+  for (size_t i = threadIdx.x; i < n4; i += blockDim.x) dst[i] = __ldg(src + i);
+}
+
+}  // namespace
+
+cudaError_t launch_steps(const float *S_in, float *S_out, float *ckpt,
+                         const float *q, const float *k, const float *v,
+                         const float *g, const float *beta, float *o, int B,
+                         int kh, int vh, int M, cudaStream_t stream) {
+  const size_t nheads = (size_t)B * vh;
+  const size_t nblocks = nheads * kCtasPerHead;
+  if (nblocks == 0) return cudaSuccess;
+  if (nblocks > 0x7fffffffull) return cudaErrorInvalidConfiguration;
+  const dim3 grid((unsigned)nblocks), block(kWarpsPerCta * 32);
+  if (ckpt)
+    gdn_steps_kernel<true><<<grid, block, 0, stream>>>(
+        S_in, S_out, ckpt, q, k, v, g, beta, o, vh, kh, vh / kh, M, nheads);
+  else
+    gdn_steps_kernel<false><<<grid, block, 0, stream>>>(
+        S_in, S_out, nullptr, q, k, v, g, beta, o, vh, kh, vh / kh, M, nheads);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy(float *dst, const float *src, size_t n,
+                        cudaStream_t stream) {
+  const size_t n4 = n / 4;
+  if (n4 == 0) return cudaSuccess;
+  size_t blocks = (n4 + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  copy_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+      reinterpret_cast<float4 *>(dst), reinterpret_cast<const float4 *>(src),
+      n4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rollback_seq(float *S, const float *snap, const float *ckpt,
+                                const int *m_dev, int *err_dev, int B, int vh,
+                                int M, cudaStream_t stream) {
+  const size_t nheads = (size_t)B * vh;
+  if (nheads == 0) return cudaSuccess;
+  if (nheads > 0x7fffffffull) return cudaErrorInvalidConfiguration;
+  rollback_seq_kernel<<<(unsigned)nheads, 256, 0, stream>>>(
+      reinterpret_cast<float4 *>(S), reinterpret_cast<const float4 *>(snap),
+      reinterpret_cast<const float4 *>(ckpt), m_dev, err_dev, vh, M, nheads);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

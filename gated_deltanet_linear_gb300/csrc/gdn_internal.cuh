@@ -1,0 +1,38 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gdn {
+
+constexpr int kDim = 128;  // kd == vd: the only head size the kernels serve
+
+// Token-serial update of every head over M tokens (gdn_step, gdn_step_m and
+// the fp32 prefill path).  Pointers and layouts as in gdn.h; S_out may equal
+// S_in.  ckpt may be nullptr.
+cudaError_t launch_steps(const float *S_in, float *S_out, float *ckpt,
+                         const float *q, const float *k, const float *v,
+                         const float *g, const float *beta, float *o, int B,
+                         int kh, int vh, int M, cudaStream_t stream);
+
+// dst[i] = src[i] for n floats (n % 4 == 0, both 16-byte aligned).
+cudaError_t launch_copy(float *dst, const float *src, size_t n,
+                        cudaStream_t stream);
+
+// Per-sequence rollback copy (see gdn_rollback_seq).
+cudaError_t launch_rollback_seq(float *S, const float *snap, const float *ckpt,
+                                const int *m_dev, int *err_dev, int B, int vh,
+                                int M, cudaStream_t stream);
+
+// Chunked tensor-core prefill (defined in gdn_prefill.cu).
+size_t prefill_workspace_bytes(int B, int kh, int vh, int T, int chunk,
+                               int precision);
+cudaError_t launch_prefill_chunked(float *S, const float *q, const float *k,
+                                   const float *v, const float *g,
+                                   const float *beta, float *o, int B, int kh,
+                                   int vh, int T, int precision,
+                                   void *workspace, cudaStream_t stream);
+
+}  // namespace gdn

@@ -1,0 +1,186 @@
+/*
+ * gdn.h - C ABI of the GB300 (sm_103a) gated delta-rule state update library
+ * (libgdn_gb300.so).
+ *
+ * The operation.  For every sequence b and value head vi, with key head
+ * hh = vi / (vh / kh) and a row-major [kd][vd] fp32 state S, one token does
+ *     alpha = exp(g);  S = alpha * S;
+ *     kv = S^T k;  tmp = (v - kv) * beta;  S = S + k tmp^T;
+ *     o = S^T q                                  (with the updated S)
+ * as defined in "Kestrel_VLLM - 24 · GDN linear attention to GPU"
+ * (wsisp.com/helps/119760.html), section 4 (the delta-recurrence kernel) and
+ * figure 1 step 5; the register-resident kernel of "Kestrel_VLLM - 27 ·
+ * register-resident & fused launch" (juejin.cn/post/7703369445846777871),
+ * section 3.1, computes the same thing.  M tokens are M serial updates
+ * ("Kestrel_VLLM - 34 · batched M rows", juejin.cn/post/7704936491831377954,
+ * section 3.6), and mark / rollback snapshot and restore the state
+ * (same article, section 3.7).
+ *
+ * Conventions shared by every call
+ *   - Shapes: kd == vd == 128, vh % kh == 0, B >= 0 (B == 0 is a no-op that
+ *     returns GDN_OK).  Anything else returns GDN_ESHAPE.
+ *   - Layouts: contiguous row-major fp32 DEVICE arrays
+ *         S          [B][vh][kd][vd]
+ *         q, k       [B][T][kh][kd]     (T = 1 for gdn_step, M, or T)
+ *         v, o       [B][T][vh][vd]
+ *         g, beta    [B][T][vh]         (g is the log-domain decay, alpha = exp(g))
+ *         ckpt       [M][B][vh][kd][vd]
+ *     Every array pointer must be 16-byte aligned (GDN_EALIGN otherwise) and
+ *     point to device (or managed) memory of the current device (GDN_EPTR
+ *     otherwise).  NULL where a buffer is required gives GDN_EINVAL.
+ *   - Ownership: the caller allocates and frees everything.  The library
+ *     never allocates device memory and never synchronises; every call only
+ *     enqueues work on `stream` and returns.
+ *   - Aliasing: outputs must not overlap inputs or each other, except where
+ *     a call states otherwise (GDN_EALIAS).
+ *   - Errors: arguments are validated on the host before anything is
+ *     enqueued; on any error nothing is launched.  A failed kernel launch
+ *     returns GDN_ECUDA.  Asynchronous faults surface on the stream as
+ *     usual CUDA errors.
+ *   - Precision: fp32 throughout (expf from CUDA's math library, fused
+ *     multiply-adds, fixed reduction trees).  Results are deterministic: the
+ *     same inputs and shape give the same bits on every call.
+ */
+#ifndef GDN_GB300_H
+#define GDN_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream.  NULL is the legacy default
+ * stream. */
+typedef struct CUstream_st *gdn_stream_t;
+
+typedef struct gdn_shape {
+    int B;   /* sequences, each with its own vh states                    */
+    int kh;  /* key heads (q and k are per key head)                      */
+    int vh;  /* value heads; value head vi reads key head vi / (vh / kh)  */
+    int kd;  /* key dimension: must be 128                                */
+    int vd;  /* value dimension: must be 128                              */
+} gdn_shape;
+
+enum {
+    GDN_OK = 0,
+    GDN_EINVAL = -1, /* NULL pointer or meaningless argument               */
+    GDN_ESHAPE = -2, /* shape not supported (kd, vd, vh % kh, negative)    */
+    GDN_EALIGN = -3, /* a pointer is not 16-byte aligned                   */
+    GDN_ECUDA = -4,  /* a CUDA runtime call or kernel launch failed        */
+    GDN_ERANGE = -5, /* M, m, T, chunk or workspace size out of range      */
+    GDN_EPTR = -6,   /* a pointer is not device memory of this device      */
+    GDN_EALIAS = -7  /* buffers overlap where they must not                */
+};
+
+/* Largest M / T accepted by one call. */
+#define GDN_MAX_TOKENS (1 << 20)
+
+/* Prefill precisions. */
+enum {
+    GDN_PREC_FP32 = 0,   /* token-serial fp32: bit-identical to T gdn_step  */
+    GDN_PREC_3XTF32 = 1, /* chunked, tensor cores, split-tf32 operands      */
+    GDN_PREC_TF32 = 2    /* chunked, tensor cores, plain tf32 operands      */
+};
+
+/*
+ * gdn_step - one token for all B * vh heads, state updated in place.
+ *   S     [B][vh][kd][vd]  in/out
+ *   q, k  [B][kh][kd]      in
+ *   v     [B][vh][vd]      in
+ *   g     [B][vh]          in, log-domain decay (alpha = exp(g))
+ *   beta  [B][vh]          in
+ *   o     [B][vh][vd]      out
+ * Bit-identical to gdn_step_m with M = 1 and S_out == S_in (it is that
+ * call).  Algorithmic HBM traffic: 2 * B*vh*kd*vd*4 bytes of state plus the
+ * token inputs and o.
+ */
+int gdn_step(const gdn_shape *shape, float *S, const float *q, const float *k,
+             const float *v, const float *g, const float *beta, float *o,
+             gdn_stream_t stream);
+
+/*
+ * gdn_step_m - M tokens in one launch; the state is read once, kept on chip
+ * across the M serial updates, and written once.
+ *   S_in   [B][vh][kd][vd]      in  (state before token 0)
+ *   S_out  [B][vh][kd][vd]      out (state after token M-1); may equal S_in
+ *                               exactly (in place), no other overlap
+ *   ckpt   [M][B][vh][kd][vd]   out, or NULL: ckpt[m] = state after token m
+ *   q, k   [B][M][kh][kd]       in
+ *   v      [B][M][vh][vd]       in
+ *   g,beta [B][M][vh]           in
+ *   o      [B][M][vh][vd]       out
+ * 1 <= M <= GDN_MAX_TOKENS (GDN_ERANGE otherwise).  Output m is
+ * bit-identical to the m-th of M successive gdn_step calls on the same
+ * inputs, and ckpt[m] to the state after it.
+ */
+int gdn_step_m(const gdn_shape *shape, int M, const float *S_in, float *S_out,
+               float *ckpt, const float *q, const float *k, const float *v,
+               const float *g, const float *beta, float *o,
+               gdn_stream_t stream);
+
+/*
+ * gdn_mark - snapshot the state: snap = S (B*vh*kd*vd floats, device to
+ * device, on `stream`).  snap must not overlap S.
+ */
+int gdn_mark(const gdn_shape *shape, const float *S, float *snap,
+             gdn_stream_t stream);
+
+/*
+ * gdn_rollback - restore the state after m of the M tokens of a gdn_step_m
+ * call:  m == 0 copies snap (the state before the call, from gdn_mark or the
+ * S_in of an out-of-place call) into S;  1 <= m <= M copies ckpt[m-1].
+ * snap may be NULL when m > 0; ckpt may be NULL when m == 0.  0 <= m <= M
+ * (GDN_ERANGE otherwise).  The copy is bit-exact.  Sources must not overlap
+ * S.
+ */
+int gdn_rollback(const gdn_shape *shape, int M, int m, const float *snap,
+                 const float *ckpt, float *S, gdn_stream_t stream);
+
+/*
+ * gdn_rollback_seq - per-sequence rollback: sequence b restores the state
+ * after m_dev[b] tokens (same rule as gdn_rollback), where m_dev is an int
+ * array [B] in DEVICE memory, so a count produced on the device needs no
+ * host round trip.  A value outside 0..M leaves that sequence's S
+ * untouched and sets *err_dev (device int, may be NULL) to 1; the host call
+ * itself cannot see device values.  Both snap and ckpt are required.
+ */
+int gdn_rollback_seq(const gdn_shape *shape, int M, const int *m_dev,
+                     const float *snap, const float *ckpt, float *S,
+                     int *err_dev, gdn_stream_t stream);
+
+/*
+ * gdn_prefill_workspace - bytes of device workspace gdn_prefill needs for
+ * this shape, T, chunk and precision (0 for GDN_PREC_FP32).  Returns 0 and
+ * sets nothing on invalid arguments; gdn_prefill validates again.
+ */
+size_t gdn_prefill_workspace(const gdn_shape *shape, int T, int chunk,
+                             int precision);
+
+/*
+ * gdn_prefill - T tokens for all heads, state in place (in: S_0, out: S_T).
+ *   q, k [B][T][kh][kd];  v, o [B][T][vh][vd];  g, beta [B][T][vh].
+ * precision GDN_PREC_FP32: the token-serial path, bit-identical to T
+ *   successive gdn_step calls; chunk and workspace are ignored (pass 0 /
+ *   NULL).
+ * GDN_PREC_3XTF32 / GDN_PREC_TF32: the chunk-parallel form with chunk == 64,
+ *   its dense products on tcgen05 tensor cores; workspace of at least
+ *   gdn_prefill_workspace() bytes (GDN_ERANGE if smaller).
+ * 1 <= T <= GDN_MAX_TOKENS.
+ */
+int gdn_prefill(const gdn_shape *shape, int T, float *S, const float *q,
+                const float *k, const float *v, const float *g,
+                const float *beta, float *o, int chunk, int precision,
+                void *workspace, size_t ws_bytes, gdn_stream_t stream);
+
+/* Static description of a status code (never NULL). */
+const char *gdn_strerror(int status);
+
+/* Library ABI version: major * 10000 + minor * 100 + patch. */
+int gdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_GB300_H */

@@ -1,0 +1,92 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol the
+header declares, and refuses bad arguments on the host before any CUDA call.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import gated_deltanet_linear_gb300 as gdn
+from gated_deltanet_linear_gb300 import _build
+
+HEADER = os.path.join(_build.INCLUDE, "gdn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return gdn.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(gdn.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    raw = ctypes.CDLL(_build.LIB)
+    for name in declared_functions():
+        assert ctypes.cast(getattr(raw, name), ctypes.c_void_p).value
+
+
+def test_version_and_strerror(lib):
+    assert gdn.gdn_version() == 100
+    for code in range(-7, 1):
+        assert gdn.gdn_strerror(code) != "unknown status"
+    assert gdn.gdn_strerror(-99) == "unknown status"
+
+
+def _call_step(lib, shape):
+    null = None
+    return lib.gdn_step(shape, *([null] * 7), None)
+
+
+def test_host_side_refusals(lib):
+    """Refusals decided from the shape and counts alone (no CUDA call)."""
+    assert _call_step(lib, None) == gdn.GDN_EINVAL
+    for bad in [gdn.Shape(1, 16, 48, 64, 128), gdn.Shape(1, 16, 48, 128, 64),
+                gdn.Shape(1, 16, 40, 128, 128), gdn.Shape(-1, 16, 48, 128, 128),
+                gdn.Shape(1, 0, 48, 128, 128)]:
+        assert _call_step(lib, ctypes.byref(bad)) == gdn.GDN_ESHAPE
+    ok = gdn.Shape(1, 16, 48, 128, 128)
+    # NULL buffers with a valid shape
+    assert _call_step(lib, ctypes.byref(ok)) == gdn.GDN_EINVAL
+    # M out of range
+    for M in (0, -3, gdn.GDN_MAX_TOKENS + 1):
+        assert lib.gdn_step_m(ctypes.byref(ok), M, *([None] * 9),
+                              None) == gdn.GDN_ERANGE
+    # rollback m out of range
+    assert lib.gdn_rollback(ctypes.byref(ok), 4, 5, None, None, None,
+                            None) == gdn.GDN_ERANGE
+    assert lib.gdn_rollback(ctypes.byref(ok), 4, -1, None, None, None,
+                            None) == gdn.GDN_ERANGE
+    # B == 0 is a no-op
+    zero = gdn.Shape(0, 16, 48, 128, 128)
+    assert _call_step(lib, ctypes.byref(zero)) == gdn.GDN_OK
+    # misaligned pointers are refused before any device query
+    fake = ctypes.c_void_p(0x1004)
+    args = [fake] * 7
+    assert lib.gdn_step(ctypes.byref(ok), *args, None) == gdn.GDN_EALIGN
+    # prefill: T range and unknown precision
+    assert lib.gdn_prefill(ctypes.byref(ok), 0, *([None] * 7), 64, 0, None,
+                           0, None) == gdn.GDN_ERANGE
+    assert lib.gdn_prefill(ctypes.byref(ok), 8, *([None] * 7), 64, 7, None,
+                           0, None) == gdn.GDN_ERANGE
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    S = torch.zeros(1, 3, 128, 128)
+    q = torch.zeros(1, 1, 1, 128)
+    with pytest.raises(ValueError):
+        gdn.gdn_step(S, q, q, torch.zeros(1, 1, 3, 128), torch.zeros(1, 1, 3),
+                     torch.zeros(1, 1, 3), torch.zeros(1, 1, 3, 128))

@@ -1,0 +1,362 @@
+"""CUDA path against the CPU oracle, and the CUDA path's exactness
+guarantees (M-token launch vs single tokens, rollback vs checkpoints).
+
+Tolerances: the normwise relative error max|x - ref| / max|ref| of "24 · GDN
+linear attention to GPU", section 6, where it is taken over one token's
+whole output vector.  Here: for o per (sequence, token) over all value
+heads, for the state per (sequence, value head).  A single token must be
+within 1e-5, runs of several tokens within 1e-4, on both o and the state.
+The GPU sums in a different order than the oracle and uses fused
+multiply-adds, so bitwise agreement with the oracle is not expected.
+
+A single head's output at one token can be ill-conditioned (q nearly
+orthogonal to everything in S makes |o| tiny next to sum |S q|); there the
+fp32 oracle itself is off by ~1e-4 relative to exact.  Such slices are
+checked element by element against the fp64 matrix form, within the fp32
+rounding bound of the sum (test_output_elementwise_rounding_bound).
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import gated_deltanet_linear_gb300 as gdn
+import gdn_inputs
+from oracle.ref64 import max_rel
+from gpu_util import dev, empty, host, run_single_steps, run_step, run_step_m
+
+pytestmark = pytest.mark.gpu
+
+TOL_STEP = 1e-5
+TOL_MULTI = 1e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def err_state(S, ref):       # [B][vh][kd][vd]
+    return max_rel(S, ref, axes=(-2, -1))
+
+
+def err_out(o, ref):         # [B][T][vh][vd]: per (sequence, token)
+    return max_rel(o, ref, axes=(-2, -1))
+
+
+# ---------------------------------------------------------------- decode
+
+def test_decode_b1_single_step(oracle_mod):
+    """One token, one sequence x 48 value heads (16 key heads)."""
+    inp = gdn_inputs.make_workload("decode_b1")
+    S, o = run_step(inp)
+    S_ref, o_ref = oracle_mod.run_inputs(inp)
+    es, eo = err_state(host(S), S_ref), err_out(host(o), o_ref)
+    print(f"decode_b1: state {es:.3e} o {eo:.3e}")
+    assert es < TOL_STEP and eo < TOL_STEP
+
+
+def test_decode_b1_chained_64(oracle_mod):
+    """64 chained gdn_step calls with fresh inputs each token."""
+    inp = gdn_inputs.make_workload("decode_b1_t64")
+    S, o, _ = run_single_steps(inp)
+    S_ref, o_ref = oracle_mod.run_inputs(inp)
+    es, eo = err_state(host(S), S_ref), err_out(host(o), o_ref)
+    print(f"decode_b1_t64: state {es:.3e} o(all tokens) {eo:.3e}")
+    assert es < TOL_MULTI and eo < TOL_MULTI
+
+
+def test_decode_b64_full_size(oracle_mod):
+    """Batched decode at full size: 64 sequences x 48 heads, every head."""
+    inp = gdn_inputs.make_workload("decode_b64")
+    S, o = run_step(inp)
+    S_ref, o_ref = oracle_mod.run_inputs(inp)
+    es, eo = err_state(host(S), S_ref), err_out(host(o), o_ref)
+    print(f"decode_b64: state {es:.3e} o {eo:.3e}")
+    assert es < TOL_STEP and eo < TOL_STEP
+
+
+@pytest.mark.parametrize("B,kh,vh,T", [(1, 1, 1, 1), (3, 1, 1, 2),
+                                       (2, 4, 4, 3), (1, 1, 3, 5),
+                                       (5, 2, 6, 3), (7, 16, 48, 1)])
+def test_odd_shapes(oracle_mod, B, kh, vh, T):
+    """Other head counts, group sizes and batch sizes (ragged grids)."""
+    inp = gdn_inputs.make_inputs(1000 + 7 * B + vh, B=B, T=T, kh=kh, vh=vh)
+    _, S, _, o = run_step_m(inp, ckpt=False)
+    S_ref, o_ref = oracle_mod.run_inputs(inp)
+    tol = TOL_STEP if T == 1 else TOL_MULTI
+    assert err_state(host(S), S_ref) < tol
+    assert err_out(host(o), o_ref) < tol
+
+
+def test_empty_batch():
+    """B = 0 is a no-op that succeeds."""
+    S = empty(0, 48, 128, 128)
+    q = empty(0, 1, 16, 128)
+    gdn.gdn_step(S, q, q, empty(0, 1, 48, 128), empty(0, 1, 48),
+                 empty(0, 1, 48), empty(0, 1, 48, 128))
+
+
+def test_no_writes_outside_outputs():
+    """Guard bands around every output stay untouched."""
+    inp = gdn_inputs.make_inputs(77, B=3, T=4, kh=2, vh=6)
+    G = 4096
+    n_s = inp.S.size
+    n_o = inp.v.size
+
+    def guarded(n, init=None):
+        buf = torch.full((n + 2 * G,), float("nan"), device="cuda")
+        if init is not None:
+            buf[G:G + n] = dev(init).reshape(-1)
+        return buf
+
+    S_buf = guarded(n_s, inp.S)
+    o_buf = guarded(n_o)
+    ck_buf = guarded(inp.T * n_s)
+    sh = gdn.Shape(inp.B, inp.kh, inp.vh, 128, 128)
+    ins = [dev(x) for x in (inp.q, inp.k, inp.v, inp.g, inp.beta)]
+    lib = gdn.load()
+    st = lib.gdn_step_m(ctypes.byref(sh), inp.T, S_buf[G:].data_ptr(),
+                        S_buf[G:].data_ptr(), ck_buf[G:].data_ptr(),
+                        *[x.data_ptr() for x in ins], o_buf[G:].data_ptr(),
+                        torch.cuda.current_stream().cuda_stream)
+    assert st == gdn.GDN_OK
+    torch.cuda.synchronize()
+    for buf, n in ((S_buf, n_s), (o_buf, n_o), (ck_buf, inp.T * n_s)):
+        assert torch.isnan(buf[:G]).all() and torch.isnan(buf[G + n:]).all()
+        assert not torch.isnan(buf[G:G + n]).any()
+
+
+def test_batch_slice_and_determinism():
+    """The same head at sequence 0 and at sequence B-1 gives the same bits
+    (offset addressing), and a repeated launch gives the same bits."""
+    inp = gdn_inputs.make_inputs(31, B=9, T=3, kh=16, vh=48)
+    for x in (inp.S, inp.q, inp.k, inp.v, inp.g, inp.beta):
+        x[-1] = x[0]
+    _, S1, ck1, o1 = run_step_m(inp)
+    _, S2, ck2, o2 = run_step_m(inp)
+    assert torch.equal(S1, S2) and torch.equal(o1, o2) and torch.equal(ck1, ck2)
+    assert torch.equal(S1[0], S1[-1]) and torch.equal(o1[0], o1[-1])
+
+
+# ------------------------------------------------------ M-token verify path
+
+@pytest.mark.parametrize("M", [2, 4, 8])
+def test_verify_m_bit_exact_vs_single_steps(oracle_mod, M):
+    """32 sequences x 48 heads, M tokens in one launch: o, every checkpoint
+    and the final state are bit-identical to M single-token launches, and
+    within tolerance of the oracle."""
+    inp = gdn_inputs.make_workload("verify_b32").tokens(0, M)
+    S_in, S_out, ck, o = run_step_m(inp)
+    S_ss, o_ss, states = run_single_steps(inp)
+    assert torch.equal(o, o_ss)
+    assert torch.equal(S_out, S_ss)
+    for m in range(M):
+        assert torch.equal(ck[m], states[m]), m
+    # S_in untouched by an out-of-place launch
+    assert torch.equal(S_in, dev(inp.S))
+    S_ref, o_ref, ck_ref = oracle_mod.run_inputs(inp, ckpt=True)
+    es = err_state(host(S_out), S_ref)
+    eo = err_out(host(o), o_ref)
+    ec = max_rel(host(ck), ck_ref, axes=(-2, -1))
+    print(f"verify_b32 M={M}: state {es:.3e} o {eo:.3e} ckpt {ec:.3e}")
+    assert es < TOL_MULTI and eo < TOL_MULTI and ec < TOL_MULTI
+
+
+def test_verify_variants_identical():
+    """In place vs out of place, with vs without checkpoints: same bits."""
+    inp = gdn_inputs.make_workload("verify_b32").tokens(0, 4).heads(
+        range(8), range(48))
+    _, S_a, ck_a, o_a = run_step_m(inp, ckpt=True, inplace=False)
+    _, S_b, _, o_b = run_step_m(inp, ckpt=False, inplace=False)
+    _, S_c, ck_c, o_c = run_step_m(inp, ckpt=True, inplace=True)
+    assert torch.equal(S_a, S_b) and torch.equal(S_a, S_c)
+    assert torch.equal(o_a, o_b) and torch.equal(o_a, o_c)
+    assert torch.equal(ck_a, ck_c)
+    assert torch.equal(ck_a[-1], S_a)
+
+
+@pytest.mark.parametrize("M", [2, 4, 8])
+def test_rollback_discriminates(M):
+    """A: reset -> M single tokens.  B: reset -> mark -> M-token launch in
+    place (the state moves on) -> rollback to 0 -> the same M single tokens.
+    B must equal A bit for bit; without a working rollback B would start
+    from the advanced state and differ ("34 · batched M rows", section 3.7,
+    the --rb check)."""
+    inp = gdn_inputs.make_workload("verify_b32").tokens(0, M).heads(
+        range(16), range(48))
+    S_a, o_a, _ = run_single_steps(inp)
+
+    S = dev(inp.S)
+    snap = torch.empty_like(S)
+    gdn.gdn_mark(S, snap, inp.kh)
+    ck = empty(M, *inp.S.shape)
+    o = empty(inp.B, M, inp.vh, inp.vd)
+    gdn.gdn_step_m(S, S, ck, dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.g),
+                   dev(inp.beta), o)
+    assert not torch.equal(S, snap)
+    gdn.gdn_rollback(S, M, 0, snap, ck, inp.kh)
+    assert torch.equal(S, dev(inp.S))
+    q, k, v, g, beta = (dev(x) for x in (inp.q, inp.k, inp.v, inp.g, inp.beta))
+    o_b = empty(inp.B, M, inp.vh, inp.vd)
+    for t in range(M):
+        ot = empty(inp.B, 1, inp.vh, inp.vd)
+        gdn.gdn_step(S, q[:, t].contiguous(), k[:, t].contiguous(),
+                     v[:, t].contiguous(), g[:, t].contiguous(),
+                     beta[:, t].contiguous(), ot)
+        o_b[:, t] = ot[:, 0]
+    assert torch.equal(S, S_a) and torch.equal(o_b, o_a)
+
+
+def test_rollback_to_every_m():
+    """rollback(m) restores exactly the state after m single tokens."""
+    M = 8
+    inp = gdn_inputs.make_workload("verify_b32").tokens(0, M).heads(
+        range(4), range(48))
+    _, _, states = run_single_steps(inp)
+    S_in, S_out, ck, _ = run_step_m(inp)
+    for m in range(M + 1):
+        S = torch.zeros_like(S_in)
+        gdn.gdn_rollback(S, M, m, S_in, ck, inp.kh)
+        want = dev(inp.S) if m == 0 else states[m - 1]
+        assert torch.equal(S, want), m
+
+
+def test_rollback_per_sequence():
+    """Each sequence restores the state after its own accepted count; an
+    out-of-range count leaves its state alone and raises the error flag."""
+    M = 4
+    inp = gdn_inputs.make_workload("verify_b32").tokens(0, M).heads(
+        range(6), range(48))
+    _, _, states = run_single_steps(inp)
+    S_in, S_out, ck, _ = run_step_m(inp)
+    counts = [0, 1, 2, 3, 4, 9]
+    m_dev = torch.tensor(counts, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    S = S_out.clone()
+    gdn.gdn_rollback_seq(S, M, m_dev, S_in, ck, inp.kh, err_dev=err)
+    torch.cuda.synchronize()
+    for b, m in enumerate(counts):
+        if m > M:
+            want = S_out[b]
+        elif m == 0:
+            want = dev(inp.S)[b]
+        else:
+            want = states[m - 1][b]
+        assert torch.equal(S[b], want), b
+    assert int(err.item()) == 1
+
+
+# ----------------------------------------------------------- fp32 prefill
+
+def test_prefill_fp32_short_bit_exact(oracle_mod):
+    """The token-serial prefill over 100 tokens (not a multiple of any tile)
+    is bit-identical to 100 gdn_step calls and within tolerance of the
+    oracle."""
+    inp = gdn_inputs.make_inputs(4242, B=2, T=100, kh=16, vh=48,
+                                 zero_state=True, g_scale=0.1)
+    S = dev(inp.S)
+    o = empty(inp.B, inp.T, inp.vh, inp.vd)
+    gdn.gdn_prefill(S, dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.g),
+                    dev(inp.beta), o, precision=gdn.GDN_PREC_FP32)
+    S_ss, o_ss, _ = run_single_steps(inp)
+    assert torch.equal(S, S_ss) and torch.equal(o, o_ss)
+    S_ref, o_ref = oracle_mod.run_inputs(inp)
+    es, eo = err_state(host(S), S_ref), err_out(host(o), o_ref)
+    print(f"prefill fp32 T=100: state {es:.3e} o {eo:.3e}")
+    assert es < TOL_MULTI and eo < TOL_MULTI
+
+
+def test_output_elementwise_rounding_bound():
+    """Every output element against the fp64 matrix form, within the fp32
+    rounding bound of the sum that produces it: |o - o64| <= 1e-5 max|o_t|
+    + 2 (kd + 8) u sum_dk |S_t[dk][dv] q[dk]|, u = 2^-24, S_t the fp64 state
+    after the token.  Holds for ill-conditioned heads too."""
+    from oracle import ref64
+    inp = gdn_inputs.make_inputs(4242, B=2, T=100, kh=16, vh=48,
+                                 zero_state=True, g_scale=0.1)
+    S = dev(inp.S)
+    o = empty(inp.B, inp.T, inp.vh, inp.vd)
+    gdn.gdn_prefill(S, dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.g),
+                    dev(inp.beta), o, precision=gdn.GDN_PREC_FP32)
+    o_h = host(o).astype(np.float64)
+    _, o64, ck64 = ref64.run_matrix(inp.S, inp.q, inp.k, inp.v, inp.g,
+                                    inp.beta, ckpt=True)
+    u = 2.0 ** -24
+    rep = inp.vh // inp.kh
+    worst = 0.0
+    for b in range(inp.B):
+        for t in range(inp.T):
+            scale = np.max(np.abs(o64[b, t]))
+            for vi in range(inp.vh):
+                qv = np.abs(inp.q[b, t, vi // rep].astype(np.float64))
+                mag = np.abs(ck64[t, b, vi]).T @ qv
+                bound = 1e-5 * scale + 2 * (inp.kd + 8) * u * mag
+                excess = np.abs(o_h[b, t, vi] - o64[b, t, vi]) / bound
+                worst = max(worst, float(np.max(excess)))
+    print(f"worst |o - o64| / bound = {worst:.3f}")
+    assert worst <= 1.0
+
+
+def test_prefill_fp32_full_size_sampled(oracle_mod):
+    """8 sequences x 4096 tokens x 48 heads (the long-sequence workload) in
+    one launch; the oracle recomputes two whole key-head groups (6 value
+    heads) in two sequences over all 4096 tokens."""
+    inp = gdn_inputs.make_workload("prefill_b8_t4096")
+    S = dev(inp.S)
+    o = empty(inp.B, inp.T, inp.vh, inp.vd)
+    gdn.gdn_prefill(S, dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.g),
+                    dev(inp.beta), o, precision=gdn.GDN_PREC_FP32)
+    torch.cuda.synchronize()
+    bs, vis = [0, 7], [0, 1, 2, 45, 46, 47]
+    sub = inp.heads(bs, vis)
+    S_ref, o_ref = oracle_mod.run_inputs(sub)
+    S_h = host(S)[np.ix_(bs, vis)]
+    o_h = host(o)[bs][:, :, vis]
+    es, eo = err_state(S_h, S_ref), err_out(o_h, o_ref)
+    print(f"prefill fp32 B=8 T=4096 (sampled heads): state {es:.3e} o {eo:.3e}")
+    assert es < TOL_MULTI and eo < TOL_MULTI
+    assert torch.isfinite(o).all() and torch.isfinite(S).all()
+
+
+# ------------------------------------------------ refusals with real memory
+
+def test_refusals_with_device_memory():
+    lib = gdn.load()
+    sh = gdn.Shape(1, 16, 48, 128, 128)
+    S = empty(1, 48, 128, 128)
+    q = empty(1, 16, 128)
+    v = empty(1, 48, 128)
+    g = empty(1, 48)
+    o = empty(1, 48, 128)
+    st = torch.cuda.current_stream().cuda_stream
+    p = lambda t: t.data_ptr()
+
+    def step(*ptrs):
+        return lib.gdn_step(ctypes.byref(sh), *ptrs, st)
+
+    base = [p(S), p(q), p(q), p(v), p(g), p(g), p(o)]
+    assert step(*base) == gdn.GDN_OK
+    # misaligned by one float
+    bad = list(base)
+    bad[3] = p(v) + 4
+    assert step(*bad) == gdn.GDN_EALIGN
+    # host memory (pageable and pinned)
+    for host_t in (torch.empty(1, 48, 128), torch.empty(1, 48, 128).pin_memory()):
+        bad = list(base)
+        bad[3] = host_t.data_ptr()
+        assert step(*bad) == gdn.GDN_EPTR
+    # output overlapping an input
+    bad = list(base)
+    bad[6] = p(S)
+    assert step(*bad) == gdn.GDN_EALIAS
+    # partial overlap of S_out and S_in
+    big = empty(2, 48, 128, 128)
+    r = lib.gdn_step_m(ctypes.byref(sh), 1, p(big), p(big) + 4096, None,
+                       p(q), p(q), p(v), p(g), p(g), p(o), st)
+    assert r == gdn.GDN_EALIAS
+    torch.cuda.synchronize()
