@@ -11,18 +11,27 @@
 // the rank-1 update follows; the state after the update is the same
 // expression as in the definition.
 //
-// Work split.  A head's 128 x 128 state is 64 KB.  Warp w of a head owns
-// value columns [8w, 8w+8) over all 128 key rows, so every reduction over
-// the key dimension stays inside one warp (no shared memory, no barriers):
-//   lane = 16 * h + p,  p in 0..15 -> key rows 8p .. 8p+7,
-//                       h in 0..1  -> value columns 8w + 4h .. 8w + 4h + 3.
+// Work split.  A head's 128 x 128 state is 64 KB.  A work unit is one head's
+// value columns [8c, 8c+8) over all 128 key rows (4 KB), so every reduction
+// over the key dimension stays inside one warp (no barriers):
+//   lane = 2 * p + h,  p in 0..15 -> key rows 8p .. 8p+7,
+//                      h in 0..1  -> value columns 8c + 4h .. 8c + 4h + 3.
 // Each lane keeps its 8 x 4 block of S in registers for all M tokens, so
 // the state is read from HBM once and written once per launch however many
 // tokens it covers (the register-resident idea of "27 · register-resident &
 // fused launch", section 3, split over 16 warps instead of one thread per
-// column).  Loads and stores are 128-bit; one warp instruction touches 16
-// full 32-byte sectors.  A CTA is 4 warps = a quarter head, so a batch of
-// B*vh heads launches 4*B*vh CTAs.
+// column).
+//
+// Memory pipeline.  The kernel is persistent (4 CTAs of 4 warps per SM, bound
+// by registers and shared memory): each warp walks a strided list
+// of units and keeps the next kStages - 1 of them in flight with cp.async
+// (16 bytes per lane per row, L2-only) into a private ring of 4 KB stages in
+// shared memory, so HBM reads continue while the warp computes.  A lane reads
+// back only the bytes it copied itself, so no barrier is needed; the stage
+// layout is XOR-swizzled so the 128-bit shared loads of a quarter warp hit
+// eight distinct 16-byte bank groups.  One warp instruction touches 16 full
+// 32-byte sectors of global memory.  Results go straight from registers to
+// global memory with 128-bit stores that skip L1.
 //
 // Determinism.  Every product and sum is an explicit round-to-nearest
 // intrinsic and the reduction tree is fixed, so a token gives the same bits
@@ -34,23 +43,51 @@
 namespace gdn {
 namespace {
 
-constexpr int kWarpsPerCta = 4;
-constexpr int kWarpsPerHead = kDim / 8;  // 16
-constexpr int kCtasPerHead = kWarpsPerHead / kWarpsPerCta;
+constexpr int kWarpsPerCta = 4;   // warps are independent; 4 per CTA
+constexpr int kStages = 3;        // cp.async ring depth per warp
+constexpr int kCtasPerSm = 4;     // 4 x 48 KB of shared memory per SM
+constexpr int kUnitsPerHead = kDim / 8;          // 16 column groups
+constexpr int kUnitFloats = kDim * 8;            // 4 KB
+constexpr int kSmemPerCta = kWarpsPerCta * kStages * kUnitFloats * 4;
 constexpr unsigned kFull = 0xffffffffu;
 
-__device__ __forceinline__ float4 ld_stream(const float *p) {
+__device__ __forceinline__ void st_stream(float *p, float4 v) {
+  asm volatile("st.global.L1::no_allocate.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p),
+               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t smem, const float *gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem),
+               "l"(gmem)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ float4 lds128(uint32_t smem) {
   float4 r;
-  asm("ld.global.cs.v4.f32 {%0, %1, %2, %3}, [%4];"
-      : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
-      : "l"(p));
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+               : "r"(smem));
   return r;
 }
 
-__device__ __forceinline__ void st_stream(float *p, float4 v) {
-  asm volatile("st.global.cs.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p),
-               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
-               : "memory");
+// Byte offset of (row j of lane p, half h) inside a 4 KB stage.  Row
+// r = 8p + j is 32 bytes (two 16-byte halves); the 32-byte slot inside each
+// 128-byte line is XOR-ed with p & 3 so that the eight lanes of a quarter
+// warp (p = 4q..4q+3, h = 0, 1) address eight different 16-byte groups.
+__device__ __forceinline__ uint32_t stage_off(int p, int h, int j) {
+  const int r = 8 * p + j;
+  const int slot = (r & 3) ^ (p & 3);
+  return (uint32_t)((r >> 2) * 128 + slot * 32 + h * 16);
 }
 
 __device__ __forceinline__ float comp(const float4 &a, int i) {
@@ -92,7 +129,7 @@ __device__ __forceinline__ float row_of(const TokenIn &t, bool isq, int j) {
 // Partial dot products of the lane's 8 rows with x (k or q), per column.
 __device__ __forceinline__ float4 partial_dot(const float4 (&s)[8],
                                               const TokenIn &t, bool isq) {
-  float x0 = row_of(t, isq, 0);
+  const float x0 = row_of(t, isq, 0);
   float4 a = make_float4(__fmul_rn(s[0].x, x0), __fmul_rn(s[0].y, x0),
                          __fmul_rn(s[0].z, x0), __fmul_rn(s[0].w, x0));
 #pragma unroll
@@ -106,13 +143,13 @@ __device__ __forceinline__ float4 partial_dot(const float4 (&s)[8],
   return a;
 }
 
-// One token for the lane's 8 x 4 block.  Updates s in place and, on the
-// lanes that own an output element, writes it to o_col[c] (c = 0..3 is the
-// column within the lane's half-group).
+// One token for the lane's 8 x 4 block (lane = 2p + h).  Updates s in place
+// and, on the lanes that own an output element, writes it to o_half[c]
+// (c = 0..3 is the column inside the lane's 4-column half).
 __device__ __forceinline__ void token_update(float4 (&s)[8], const TokenIn &t,
                                              int lane, float *o_half) {
-  const int p = lane & 15;
-  const int half_base = lane & 16;
+  const int p = lane >> 1;
+  const int h = lane & 1;
 
   // 1. Partials over this lane's rows: S^T k and S^T q for 4 columns, q.k.
   const float4 kv = partial_dot(s, t, false);
@@ -126,10 +163,10 @@ __device__ __forceinline__ void token_update(float4 (&s)[8], const TokenIn &t,
   qk = __fmaf_rn(t.q1.z, t.k1.z, qk);
   qk = __fmaf_rn(t.q1.w, t.k1.w, qk);
 
-  // 2. Reduce-scatter the 8 column partials over the 16 lanes of the half
-  // (xor 8, 4, 2, 1).  Afterwards the lane holds the full sum of value
-  // index idx = 4*[p&8] + 2*[p&4] + [p&2]: idx < 4 is kv of column idx,
-  // idx >= 4 is S^T q of column idx - 4.
+  // 2. Reduce-scatter the 8 column partials over the 16 lanes sharing h
+  // (p bits 8, 4, 2, 1 = lane xor 16, 8, 4, 2).  Afterwards the lane holds
+  // the full sum of value index idx = 4*[p&8] + 2*[p&4] + [p&2]: idx < 4 is
+  // S^T k of column idx, idx >= 4 is S^T q of column idx - 4.
   const bool b8 = p & 8, b4 = p & 4, b2 = p & 2;
   float r4[4];
   {
@@ -139,33 +176,33 @@ __device__ __forceinline__ void token_update(float4 (&s)[8], const TokenIn &t,
                            b8 ? kv.z : qs.z, b8 ? kv.w : qs.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-      r4[i] = __fadd_rn(keep[i], __shfl_xor_sync(kFull, send[i], 8));
+      r4[i] = __fadd_rn(keep[i], __shfl_xor_sync(kFull, send[i], 16));
   }
   float r2[2];
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const float keep = b4 ? r4[i + 2] : r4[i];
     const float send = b4 ? r4[i] : r4[i + 2];
-    r2[i] = __fadd_rn(keep, __shfl_xor_sync(kFull, send, 4));
+    r2[i] = __fadd_rn(keep, __shfl_xor_sync(kFull, send, 8));
   }
   float r1;
   {
     const float keep = b2 ? r2[1] : r2[0];
     const float send = b2 ? r2[0] : r2[1];
-    r1 = __fadd_rn(keep, __shfl_xor_sync(kFull, send, 2));
+    r1 = __fadd_rn(keep, __shfl_xor_sync(kFull, send, 4));
   }
-  const float red = __fadd_rn(r1, __shfl_xor_sync(kFull, r1, 1));
+  const float red = __fadd_rn(r1, __shfl_xor_sync(kFull, r1, 2));
   const int idx = (b8 ? 4 : 0) + (b4 ? 2 : 0) + (b2 ? 1 : 0);
 
-  // q . k over all 128 rows (each half holds every row once).
+  // q . k over all 128 rows (the 16 lanes of either half hold every row).
+  qk = __fadd_rn(qk, __shfl_xor_sync(kFull, qk, 16));
   qk = __fadd_rn(qk, __shfl_xor_sync(kFull, qk, 8));
   qk = __fadd_rn(qk, __shfl_xor_sync(kFull, qk, 4));
   qk = __fadd_rn(qk, __shfl_xor_sync(kFull, qk, 2));
-  qk = __fadd_rn(qk, __shfl_xor_sync(kFull, qk, 1));
 
-  // 3. tmp = (v - alpha kv) beta on the kv lanes, then broadcast the four
-  // columns' tmp to the whole half.  Column c's kv lives on p = 4*(c>>1) +
-  // 2*(c&1).
+  // 3. tmp = (v - alpha kv) beta on the S^T k lanes, then broadcast the four
+  // columns' tmp to every lane of the same h.  Column c's S^T k lives on
+  // p = 4*(c>>1) + 2*(c&1).
   const float alpha = expf(t.g);
   const int col = idx & 3;
   const float tmp_mine =
@@ -173,7 +210,8 @@ __device__ __forceinline__ void token_update(float4 (&s)[8], const TokenIn &t,
   float tmp[4];
 #pragma unroll
   for (int c = 0; c < 4; ++c)
-    tmp[c] = __shfl_sync(kFull, tmp_mine, half_base | (4 * (c >> 1) + 2 * (c & 1)));
+    tmp[c] = __shfl_sync(kFull, tmp_mine,
+                         ((4 * (c >> 1) + 2 * (c & 1)) << 1) | h);
 
   // 4. o = alpha (S^T q) + (q . k) tmp on the S^T q lanes (even p only).
   if (idx >= 4 && !(p & 1)) {
@@ -195,55 +233,113 @@ __device__ __forceinline__ void token_update(float4 (&s)[8], const TokenIn &t,
   }
 }
 
+// Start the copy of unit u's 4 KB into the stage at smem address `stage`.
+__device__ __forceinline__ void issue_unit(const float *S_in, size_t u,
+                                           uint32_t stage, int p, int h) {
+  const size_t head = u / kUnitsPerHead;
+  const int cg = (int)(u % kUnitsPerHead);
+  const float *src = S_in + head * (size_t)(kDim * kDim) +
+                     (size_t)(8 * p) * kDim + 8 * cg + 4 * h;
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    cp_async16(stage + stage_off(p, h, j), src + j * kDim);
+}
+
 template <bool kCkpt>
-__global__ void __launch_bounds__(kWarpsPerCta * 32)
+__global__ void __launch_bounds__(kWarpsPerCta * 32, kCtasPerSm)
     gdn_steps_kernel(const float *S_in, float *S_out,
                      float *__restrict__ ckpt, const float *__restrict__ q,
                      const float *__restrict__ k, const float *__restrict__ v,
                      const float *__restrict__ g,
                      const float *__restrict__ beta, float *__restrict__ o,
                      int vh, int kh, int rep, int M, size_t nheads) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const size_t head = blockIdx.x / kCtasPerHead;
-  const int cg = (blockIdx.x % kCtasPerHead) * kWarpsPerCta + warp;
-  const int b = static_cast<int>(head / vh);
-  const int vi = static_cast<int>(head % vh);
-  const int hh = vi / rep;
-  const int p = lane & 15;
-  const int row0 = 8 * p;
-  const int col0 = 8 * cg + 4 * (lane >> 4);
+  const int p = lane >> 1;
+  const int h = lane & 1;
+  const uint32_t ring =
+      (uint32_t)__cvta_generic_to_shared(smem_raw) +
+      (uint32_t)(warp * kStages * kUnitFloats * 4);
 
-  const size_t hoff = head * (size_t)(kDim * kDim);
-  const size_t eoff = (size_t)row0 * kDim + col0;
-  float4 s[8];
+  const size_t nunits = nheads * kUnitsPerHead;
+  const size_t gw = (size_t)blockIdx.x * kWarpsPerCta + warp;
+  const size_t nw = (size_t)gridDim.x * kWarpsPerCta;
+  const size_t mine = gw < nunits ? (nunits - gw + nw - 1) / nw : 0;
+
+  // Prologue: the first kStages - 1 units in flight (empty groups keep the
+  // group count uniform).
 #pragma unroll
-  for (int j = 0; j < 8; ++j) s[j] = ld_stream(S_in + hoff + eoff + j * kDim);
-
-  auto qk_row = [&](int m) {
-    return (((size_t)b * M + m) * kh + hh) * kDim + row0;
-  };
-  auto v_row = [&](int m) {
-    return (((size_t)b * M + m) * vh + vi) * kDim + col0;
-  };
-  auto g_idx = [&](int m) { return ((size_t)b * M + m) * vh + vi; };
-
-  TokenIn cur = load_token(q, k, v, g, beta, qk_row(0), v_row(0), g_idx(0));
-  for (int m = 0; m < M; ++m) {
-    TokenIn nxt = cur;
-    if (m + 1 < M)
-      nxt = load_token(q, k, v, g, beta, qk_row(m + 1), v_row(m + 1),
-                       g_idx(m + 1));
-    token_update(s, cur, lane, o + v_row(m));
-    if (kCkpt) {
-      float *cp = ckpt + (size_t)m * nheads * (kDim * kDim) + hoff + eoff;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) st_stream(cp + j * kDim, s[j]);
-    }
-    cur = nxt;
+  for (int st = 0; st < kStages - 1; ++st) {
+    if ((size_t)st < mine)
+      issue_unit(S_in, gw + st * nw, ring + st * kUnitFloats * 4, p, h);
+    cp_async_commit();
   }
+
+  // Token inputs are prefetched one token ahead along the flattened list of
+  // (unit, token) items, so the next unit's first token is in flight while
+  // the current unit computes.
+  auto unit_coords = [&](size_t i, int &b, int &vi, int &hh, int &cg,
+                         size_t &head) {
+    const size_t u = gw + i * nw;
+    head = u / kUnitsPerHead;
+    cg = (int)(u % kUnitsPerHead);
+    b = (int)(head / vh);
+    vi = (int)(head % vh);
+    hh = vi / rep;
+  };
+  auto token_at = [&](size_t i, int m) {
+    int b, vi, hh, cg;
+    size_t head;
+    unit_coords(i, b, vi, hh, cg, head);
+    const size_t bm = (size_t)b * M + m;
+    return load_token(q, k, v, g, beta, (bm * kh + hh) * kDim + 8 * p,
+                      (bm * vh + vi) * kDim + 8 * cg + 4 * h, bm * vh + vi);
+  };
+
+  TokenIn cur;
+  if (mine > 0) cur = token_at(0, 0);
+  for (size_t i = 0; i < mine; ++i) {
+    {
+      const size_t ahead = i + kStages - 1;
+      if (ahead < mine)
+        issue_unit(S_in, gw + ahead * nw,
+                   ring + (uint32_t)(ahead % kStages) * kUnitFloats * 4, p, h);
+      cp_async_commit();
+    }
+    cp_async_wait<kStages - 1>();  // unit i has landed (this lane's bytes)
+
+    int b, vi, hh, cg;
+    size_t head;
+    unit_coords(i, b, vi, hh, cg, head);
+    const int col0 = 8 * cg + 4 * h;
+    const uint32_t stage = ring + (uint32_t)(i % kStages) * kUnitFloats * 4;
+
+    float4 s[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) st_stream(S_out + hoff + eoff + j * kDim, s[j]);
+    for (int j = 0; j < 8; ++j) s[j] = lds128(stage + stage_off(p, h, j));
+
+    const size_t hoff = head * (size_t)(kDim * kDim);
+    const size_t eoff = (size_t)(8 * p) * kDim + col0;
+    for (int m = 0; m < M; ++m) {
+      TokenIn nxt = cur;
+      if (m + 1 < M)
+        nxt = token_at(i, m + 1);
+      else if (i + 1 < mine)
+        nxt = token_at(i + 1, 0);
+      token_update(s, cur, lane,
+                   o + (((size_t)b * M + m) * vh + vi) * kDim + col0);
+      if (kCkpt) {
+        float *cp = ckpt + (size_t)m * nheads * (kDim * kDim) + hoff + eoff;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) st_stream(cp + j * kDim, s[j]);
+      }
+      cur = nxt;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) st_stream(S_out + hoff + eoff + j * kDim, s[j]);
+  }
+  cp_async_wait<0>();
 }
 
 __global__ void copy_kernel(float4 *__restrict__ dst,
@@ -274,6 +370,17 @@ __global__ void rollback_seq_kernel(float4 *__restrict__ S,
   for (size_t i = threadIdx.x; i < n4; i += blockDim.x) dst[i] = __ldg(src + i);
 }
 
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
+          cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return 152;
+  }
+  return n;
+}
+
 }  // namespace
 
 cudaError_t launch_steps(const float *S_in, float *S_out, float *ckpt,
@@ -281,16 +388,28 @@ cudaError_t launch_steps(const float *S_in, float *S_out, float *ckpt,
                          const float *g, const float *beta, float *o, int B,
                          int kh, int vh, int M, cudaStream_t stream) {
   const size_t nheads = (size_t)B * vh;
-  const size_t nblocks = nheads * kCtasPerHead;
-  if (nblocks == 0) return cudaSuccess;
-  if (nblocks > 0x7fffffffull) return cudaErrorInvalidConfiguration;
-  const dim3 grid((unsigned)nblocks), block(kWarpsPerCta * 32);
-  if (ckpt)
-    gdn_steps_kernel<true><<<grid, block, 0, stream>>>(
+  const size_t nunits = nheads * kUnitsPerHead;
+  if (nunits == 0) return cudaSuccess;
+  size_t ctas = (nunits + kWarpsPerCta - 1) / kWarpsPerCta;
+  const size_t cap = (size_t)sm_count() * kCtasPerSm;
+  if (ctas > cap) ctas = cap;
+  const dim3 grid((unsigned)ctas), block(kWarpsPerCta * 32);
+  cudaError_t e;
+  if (ckpt) {
+    e = cudaFuncSetAttribute(gdn_steps_kernel<true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemPerCta);
+    if (e != cudaSuccess) return e;
+    gdn_steps_kernel<true><<<grid, block, kSmemPerCta, stream>>>(
         S_in, S_out, ckpt, q, k, v, g, beta, o, vh, kh, vh / kh, M, nheads);
-  else
-    gdn_steps_kernel<false><<<grid, block, 0, stream>>>(
+  } else {
+    e = cudaFuncSetAttribute(gdn_steps_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemPerCta);
+    if (e != cudaSuccess) return e;
+    gdn_steps_kernel<false><<<grid, block, kSmemPerCta, stream>>>(
         S_in, S_out, nullptr, q, k, v, g, beta, o, vh, kh, vh / kh, M, nheads);
+  }
   return cudaGetLastError();
 }
 
@@ -299,7 +418,8 @@ cudaError_t launch_copy(float *dst, const float *src, size_t n,
   const size_t n4 = n / 4;
   if (n4 == 0) return cudaSuccess;
   size_t blocks = (n4 + 255) / 256;
-  if (blocks > 152 * 16) blocks = 152 * 16;
+  const size_t cap = (size_t)sm_count() * 16;
+  if (blocks > cap) blocks = cap;
   copy_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
       reinterpret_cast<float4 *>(dst), reinterpret_cast<const float4 *>(src),
       n4);
