@@ -396,19 +396,40 @@ def main():
         Sp = tens(pin_.S)
         po = torch.empty(pin_.B, pin_.T, pin_.vh, D, device=dev)
 
-        def pstep(i):
-            Sp.zero_()
-            gdn.gdn_prefill(Sp, pq, pk, pv, pg, pb, po,
-                            precision=gdn.GDN_PREC_FP32, stream=stream)
-        pstep(0)
-        pms = time_launches(torch, pstep, 3, stream)
         toks = pin_.B * pin_.T
         flops = 7 * D * D * toks * pin_.vh
-        parts["prefill_b8_t4096_fp32"] = {
-            "ms": pms, "tokens_per_s": toks / (pms * 1e-3),
-            "head_steps_per_s": toks * pin_.vh / (pms * 1e-3),
-            "tflops_fp32_equiv": flops / (pms * 1e-3) / 1e12,
-            "note": "token-serial fp32 path (includes a state memset)"}
+        # executed tensor-core flops of the chunked form per 64-token chunk
+        # and head: [K;Q]K^T 2*128*64*128, W/U 2*(2*128*64*64), S[W;Q]
+        # 2*128*128*128, Delta P 2*128*64*64, Delta K 2*128*128*64
+        tc_flops = (2 * 128 * 64 * 128 + 4 * 128 * 64 * 64 +
+                    2 * 128 * 128 * 128 + 2 * 128 * 64 * 64 +
+                    2 * 128 * 128 * 64) * (pin_.T // 64) * pin_.B * pin_.vh
+        for prec, name, reps in ((gdn.GDN_PREC_FP32, "fp32", 3),
+                                 (gdn.GDN_PREC_BF16X3, "bf16x3", 10),
+                                 (gdn.GDN_PREC_TF32, "tf32", 10)):
+            def pstep(i, prec=prec):
+                gdn.gdn_prefill(Sp, pq, pk, pv, pg, pb, po, precision=prec,
+                                stream=stream)
+            pstep(0)
+            pms = time_launches(torch, pstep, reps, stream)
+            entry = {
+                "ms": pms, "tokens_per_s": toks / (pms * 1e-3),
+                "head_steps_per_s": toks * pin_.vh / (pms * 1e-3),
+                "tflops_fp32_equiv": flops / (pms * 1e-3) / 1e12}
+            if prec == gdn.GDN_PREC_FP32:
+                entry["note"] = "token-serial fp32 path"
+            else:
+                mult = 3 if prec == gdn.GDN_PREC_BF16X3 else 1
+                ach = tc_flops * mult / (pms * 1e-3) / 1e12
+                peak = float(peaks.get("bf16_tflops_sustained",
+                                       peaks.get("bf16_tflops", 1900.0)))
+                if prec == gdn.GDN_PREC_TF32:
+                    peak *= 0.5  # tf32 dense rate is half of bf16 (nominal)
+                entry.update({"tensor_tflops": ach, "tensor_peak_tflops": peak,
+                              "tensor_frac": ach / peak,
+                              "note": "chunk-parallel form on tcgen05; "
+                                      "executed MMA flops (x3 for split-bf16)"})
+            parts[f"prefill_b8_t4096_{name}"] = entry
         del pq, pk, pv, pg, pb, Sp, po
 
     sampler.stop()

@@ -25,18 +25,19 @@ __all__ = [
     "GDNError", "gdn_step", "gdn_step_m", "gdn_mark", "gdn_rollback",
     "gdn_rollback_seq", "gdn_prefill_workspace", "gdn_prefill",
     "gdn_strerror", "gdn_version", "library_path", "load",
-    "GDN_PREC_FP32", "GDN_PREC_3XTF32", "GDN_PREC_TF32", "GDN_MAX_TOKENS",
+    "GDN_PREC_FP32", "GDN_PREC_BF16X3", "GDN_PREC_TF32", "GDN_MAX_TOKENS",
+    "gdn_prefill_timeouts",
 ]
 
 GDN_OK, GDN_EINVAL, GDN_ESHAPE, GDN_EALIGN = 0, -1, -2, -3
 GDN_ECUDA, GDN_ERANGE, GDN_EPTR, GDN_EALIAS = -4, -5, -6, -7
-GDN_PREC_FP32, GDN_PREC_3XTF32, GDN_PREC_TF32 = 0, 1, 2
+GDN_PREC_FP32, GDN_PREC_BF16X3, GDN_PREC_TF32 = 0, 1, 2
 GDN_MAX_TOKENS = 1 << 20
 
 # Every symbol include/gdn.h declares.
 EXPORTS = ("gdn_step", "gdn_step_m", "gdn_mark", "gdn_rollback",
            "gdn_rollback_seq", "gdn_prefill_workspace", "gdn_prefill",
-           "gdn_strerror", "gdn_version")
+           "gdn_prefill_timeouts", "gdn_strerror", "gdn_version")
 
 
 class GDNError(RuntimeError):
@@ -83,6 +84,8 @@ def load():
         f.restype = ctypes.c_int
     lib.gdn_prefill_workspace.argtypes = [cp, ip, ip, ip]
     lib.gdn_prefill_workspace.restype = ctypes.c_size_t
+    lib.gdn_prefill_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+    lib.gdn_prefill_timeouts.restype = ctypes.c_int
     lib.gdn_strerror.argtypes = [ctypes.c_int]
     lib.gdn_strerror.restype = ctypes.c_char_p
     lib.gdn_version.restype = ctypes.c_int
@@ -203,9 +206,19 @@ def gdn_prefill_workspace(B, kh, vh, T, chunk=64, precision=GDN_PREC_FP32,
                                             int(chunk), int(precision)))
 
 
+def gdn_prefill_timeouts():
+    """Chunked-prefill CTAs that gave up waiting on the tensor cores (0)."""
+    c = ctypes.c_uint(0)
+    _check(load().gdn_prefill_timeouts(ctypes.byref(c)), "gdn_prefill_timeouts")
+    return int(c.value)
+
+
 def gdn_prefill(S, q, k, v, g, beta, o, precision=GDN_PREC_FP32, chunk=64,
                 workspace=None, stream=None):
-    """T = q.shape[1] tokens; S updated in place (S_0 -> S_T)."""
+    """T = q.shape[1] tokens; S updated in place (S_0 -> S_T).
+
+    precision: GDN_PREC_FP32 (token-serial, exact to the single-step path),
+    GDN_PREC_BF16X3 or GDN_PREC_TF32 (chunk-parallel on tensor cores)."""
     sh = _shape(S, q)
     B, kh, vh, kd, vd = sh.B, sh.kh, sh.vh, sh.kd, sh.vd
     T = int(q.shape[1])

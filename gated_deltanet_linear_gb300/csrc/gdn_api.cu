@@ -189,21 +189,50 @@ int gdn_rollback_seq(const gdn_shape *shape, int M, const int *m_dev,
 size_t gdn_prefill_workspace(const gdn_shape *shape, int T, int chunk,
                              int precision) {
   if (check_shape(shape) || T < 1 || T > GDN_MAX_TOKENS) return 0;
-  (void)chunk;
-  (void)precision;
-  return 0;
+  if (precision != GDN_PREC_FP32 && chunk != 64) return 0;
+  return gdn::prefill_workspace_bytes(shape->B, shape->kh, shape->vh, T, chunk,
+                                      precision);
 }
 
 int gdn_prefill(const gdn_shape *shape, int T, float *S, const float *q,
                 const float *k, const float *v, const float *g,
                 const float *beta, float *o, int chunk, int precision,
                 void *workspace, size_t ws_bytes, gdn_stream_t stream) {
-  (void)chunk;
   (void)workspace;
   (void)ws_bytes;
-  if (precision != GDN_PREC_FP32) return GDN_ERANGE;
-  return steps_common(shape, T, S, S, nullptr, q, k, v, g, beta, o,
-                      (cudaStream_t)stream);
+  if (precision == GDN_PREC_FP32)
+    return steps_common(shape, T, S, S, nullptr, q, k, v, g, beta, o,
+                        (cudaStream_t)stream);
+  if (precision != GDN_PREC_BF16X3 && precision != GDN_PREC_TF32)
+    return GDN_ERANGE;
+  int r = check_shape(shape);
+  if (r) return r;
+  if (T < 1 || T > GDN_MAX_TOKENS || chunk != 64) return GDN_ERANGE;
+  if (shape->B == 0) return GDN_OK;
+  const size_t sb = state_floats(shape) * 4;
+  const size_t qkb = (size_t)shape->B * T * shape->kh * shape->kd * 4;
+  const size_t vb = (size_t)shape->B * T * shape->vh * shape->vd * 4;
+  const size_t gb = (size_t)shape->B * T * shape->vh * 4;
+  Buf in[] = {{q, qkb}, {k, qkb}, {v, vb}, {g, gb}, {beta, gb}};
+  Buf out[] = {{S, sb}, {o, vb}};
+  r = check_bufs(in, 5);
+  if (r) return r;
+  r = check_bufs(out, 2);
+  if (r) return r;
+  for (int i = 0; i < 2; ++i)
+    for (int j = 0; j < 5; ++j)
+      if (overlaps(out[i], in[j])) return GDN_EALIAS;
+  if (overlaps(out[0], out[1])) return GDN_EALIAS;
+  cudaGetLastError();
+  return status_of(gdn::launch_prefill_chunked(
+      S, q, k, v, g, beta, o, shape->B, shape->kh, shape->vh, T, precision,
+      nullptr, (cudaStream_t)stream));
+}
+
+int gdn_prefill_timeouts(unsigned int *count) {
+  if (!count) return GDN_EINVAL;
+  cudaGetLastError();
+  return status_of(gdn::prefill_timeouts(count));
 }
 
 const char *gdn_strerror(int status) {

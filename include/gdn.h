@@ -78,9 +78,12 @@ enum {
 
 /* Prefill precisions. */
 enum {
-    GDN_PREC_FP32 = 0,   /* token-serial fp32: bit-identical to T gdn_step  */
-    GDN_PREC_3XTF32 = 1, /* chunked, tensor cores, split-tf32 operands      */
-    GDN_PREC_TF32 = 2    /* chunked, tensor cores, plain tf32 operands      */
+    GDN_PREC_FP32 = 0,   /* token-serial fp32: bit-identical to T gdn_step   */
+    GDN_PREC_BF16X3 = 1, /* chunked, tensor cores, operands split into bf16
+                            hi + lo, 3 products per term, fp32 accumulation:
+                            relative error ~1e-5                             */
+    GDN_PREC_TF32 = 2    /* chunked, tensor cores, operands rounded to tf32:
+                            relative error ~1e-3                             */
 };
 
 /*
@@ -163,15 +166,30 @@ size_t gdn_prefill_workspace(const gdn_shape *shape, int T, int chunk,
  * precision GDN_PREC_FP32: the token-serial path, bit-identical to T
  *   successive gdn_step calls; chunk and workspace are ignored (pass 0 /
  *   NULL).
- * GDN_PREC_3XTF32 / GDN_PREC_TF32: the chunk-parallel form with chunk == 64,
- *   its dense products on tcgen05 tensor cores; workspace of at least
- *   gdn_prefill_workspace() bytes (GDN_ERANGE if smaller).
- * 1 <= T <= GDN_MAX_TOKENS.
+ * GDN_PREC_BF16X3 / GDN_PREC_TF32: the chunk-parallel form with chunk ==
+ *   64 (GDN_ERANGE otherwise), its dense products on tcgen05 tensor cores
+ *   with fp32 accumulation and the state kept in tensor memory; one CTA
+ *   per (sequence, value head) walks the chunks in order.  The chunked form
+ *   regroups the token-serial recurrence of "24 · GDN linear attention to
+ *   GPU", section 4; the articles themselves never use it ("34 · batched M
+ *   rows", section 3.6).  Needs no workspace (gdn_prefill_workspace returns
+ *   0; pass NULL, 0).  Results agree with the token-serial definition to
+ *   the stated relative error, not bitwise.
+ * 1 <= T <= GDN_MAX_TOKENS.  Other precision values give GDN_ERANGE.
  */
 int gdn_prefill(const gdn_shape *shape, int T, float *S, const float *q,
                 const float *k, const float *v, const float *g,
                 const float *beta, float *o, int chunk, int precision,
                 void *workspace, size_t ws_bytes, gdn_stream_t stream);
+
+/*
+ * gdn_prefill_timeouts - number of chunked-prefill CTAs, since the library
+ * was loaded on the current device, that gave up waiting for a tensor-core
+ * operation (each wait is bounded) and left their head's state unwritten.
+ * Synchronises the current device.  Expected to stay 0; a non-zero count
+ * means the results of those launches are invalid.
+ */
+int gdn_prefill_timeouts(unsigned int *count);
 
 /* Static description of a status code (never NULL). */
 const char *gdn_strerror(int status);

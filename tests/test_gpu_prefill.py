@@ -1,0 +1,126 @@
+"""Chunk-parallel prefill on tensor cores against the CPU oracle.
+
+Tolerances (normwise max|x - ref| / max|ref|, per (sequence, token) over all
+value heads for o, per (sequence, value head) for the state):
+  GDN_PREC_BF16X3  1e-4, the bar for multi-token runs.  Each operand is split
+                   into bf16 hi + lo (about 16 significant bits) and three
+                   products are accumulated in fp32, so the expected error
+                   is ~1e-5.
+  GDN_PREC_TF32    8 * 2^-11 = 3.9e-3.  tf32 keeps 10 explicit mantissa bits
+                   (unit roundoff 2^-11); a few roundings compound through
+                   the chunk products.
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import gated_deltanet_linear_gb300 as gdn
+import gdn_inputs
+from oracle.ref64 import max_rel
+from gpu_util import dev, empty, host
+
+pytestmark = pytest.mark.gpu
+
+TOL = {gdn.GDN_PREC_BF16X3: 1e-4, gdn.GDN_PREC_TF32: 8 * 2.0 ** -11}
+NAME = {gdn.GDN_PREC_BF16X3: "bf16x3", gdn.GDN_PREC_TF32: "tf32"}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def run_prefill(inp, precision):
+    S = dev(inp.S)
+    o = empty(inp.B, inp.T, inp.vh, inp.vd)
+    gdn.gdn_prefill(S, dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.g),
+                    dev(inp.beta), o, precision=precision)
+    torch.cuda.synchronize()
+    return S, o
+
+
+def errs(S, o, S_ref, o_ref):
+    return (max_rel(S, S_ref, axes=(-2, -1)), max_rel(o, o_ref, axes=(-2, -1)))
+
+
+@pytest.mark.parametrize("precision", [gdn.GDN_PREC_BF16X3, gdn.GDN_PREC_TF32],
+                         ids=lambda p: NAME[p])
+@pytest.mark.parametrize("T,zero,g_scale", [(150, True, 0.1), (150, False, 1.0),
+                                            (1, False, 1.0), (64, True, 0.1),
+                                            (65, False, 0.1)])
+def test_chunked_vs_oracle(oracle_mod, precision, T, zero, g_scale):
+    """Several chunks with a ragged last one, zero and random initial
+    states, mild and strong decay."""
+    inp = gdn_inputs.make_inputs(500 + T, B=2, T=T, kh=16, vh=48,
+                                 zero_state=zero, g_scale=g_scale)
+    S, o = run_prefill(inp, precision)
+    S_ref, o_ref = oracle_mod.run_inputs(inp)
+    es, eo = errs(host(S), host(o), S_ref, o_ref)
+    print(f"{NAME[precision]} T={T} zero={zero}: state {es:.3e} o {eo:.3e}")
+    assert es < TOL[precision] and eo < TOL[precision]
+    assert gdn.gdn_prefill_timeouts() == 0
+
+
+@pytest.mark.parametrize("precision", [gdn.GDN_PREC_BF16X3, gdn.GDN_PREC_TF32],
+                         ids=lambda p: NAME[p])
+def test_chunked_full_size_sampled(oracle_mod, precision):
+    """8 sequences x 4096 tokens x 48 heads in one launch; the oracle
+    recomputes two key-head groups (6 value heads) of two sequences over
+    all 4096 tokens."""
+    inp = gdn_inputs.make_workload("prefill_b8_t4096")
+    S, o = run_prefill(inp, precision)
+    bs, vis = [0, 7], [0, 1, 2, 45, 46, 47]
+    S_ref, o_ref = oracle_mod.run_inputs(inp.heads(bs, vis))
+    S_h = host(S)[np.ix_(bs, vis)]
+    o_h = host(o)[bs][:, :, vis]
+    es, eo = errs(S_h, o_h, S_ref, o_ref)
+    print(f"{NAME[precision]} B=8 T=4096 (sampled heads): state {es:.3e} "
+          f"o {eo:.3e}")
+    assert es < TOL[precision] and eo < TOL[precision]
+    assert torch.isfinite(o).all() and torch.isfinite(S).all()
+    assert gdn.gdn_prefill_timeouts() == 0
+
+
+def test_chunked_matches_token_serial_gpu():
+    """The chunked form and the token-serial fp32 path agree (both on the
+    GPU) to the split-bf16 tolerance on a 300-token run."""
+    inp = gdn_inputs.make_inputs(777, B=3, T=300, kh=16, vh=48)
+    S_c, o_c = run_prefill(inp, gdn.GDN_PREC_BF16X3)
+    S_s, o_s = run_prefill(inp, gdn.GDN_PREC_FP32)
+    es, eo = errs(host(S_c), host(o_c), host(S_s), host(o_s))
+    assert es < 1e-4 and eo < 1e-4
+
+
+def test_chunked_deterministic():
+    inp = gdn_inputs.make_inputs(778, B=2, T=130, kh=16, vh=48)
+    S1, o1 = run_prefill(inp, gdn.GDN_PREC_BF16X3)
+    S2, o2 = run_prefill(inp, gdn.GDN_PREC_BF16X3)
+    assert torch.equal(S1, S2) and torch.equal(o1, o2)
+
+
+def test_chunked_refusals():
+    lib = gdn.load()
+    sh = gdn.Shape(1, 16, 48, 128, 128)
+    T = 64
+    S = empty(1, 48, 128, 128)
+    q = empty(1, T, 16, 128)
+    v = empty(1, T, 48, 128)
+    g = empty(1, T, 48)
+    o = empty(1, T, 48, 128)
+    st = torch.cuda.current_stream().cuda_stream
+    ptrs = [S.data_ptr(), q.data_ptr(), q.data_ptr(), v.data_ptr(),
+            g.data_ptr(), g.data_ptr(), o.data_ptr()]
+    for chunk, prec in ((32, gdn.GDN_PREC_BF16X3), (64, 3), (64, -1)):
+        assert lib.gdn_prefill(ctypes.byref(sh), T, *ptrs, chunk, prec, None,
+                               0, st) == gdn.GDN_ERANGE
+    bad = list(ptrs)
+    bad[6] = S.data_ptr()  # o overlapping S
+    assert lib.gdn_prefill(ctypes.byref(sh), T, *bad, 64, gdn.GDN_PREC_TF32,
+                           None, 0, st) == gdn.GDN_EALIAS
+    assert gdn.gdn_prefill_workspace(1, 16, 48, T, 64,
+                                     gdn.GDN_PREC_BF16X3) == 0
