@@ -150,6 +150,30 @@ class ClockSampler:
                           "shorter than the sampling period)"}
 
 
+# ------------------------------------------------------------ multi-rank
+
+def shard_range(n, world, rank):
+    """Contiguous share [lo, hi) of n independent units for `rank` of
+    `world` (the first n % world ranks take one extra)."""
+    base, extra = divmod(n, world)
+    lo = rank * base + min(rank, extra)
+    return lo, lo + base + (1 if rank < extra else 0)
+
+
+def aggregate(ms_local, units_local, dist=None, device=None):
+    """Whole-job rate: the slowest rank's time and the units all ranks
+    processed.  Returns (ms_max, total_units, units_per_second)."""
+    import torch
+    if dist is None or not dist.is_initialized():
+        return ms_local, units_local, units_local / (ms_local * 1e-3)
+    t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+    u = torch.tensor([units_local], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    ms, units = float(t.item()), float(u.item())
+    return ms, units, units / (ms * 1e-3)
+
+
 # --------------------------------------------------------------- timing
 
 def time_launches(torch, fn, n, stream):
@@ -253,6 +277,54 @@ def run_reference(args, rank, world):
     return 0
 
 
+def tens_fn(torch, dev):
+    return lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+
+def prefill_parts(torch, gdn, tens, stream, peaks, parts):
+    """Time the 8 x 4096-token prefill in its three precisions."""
+    pin_ = gdn_inputs.make_workload("prefill_b8_t4096")
+    pq, pk, pv, pg, pb = (tens(x) for x in
+                          (pin_.q, pin_.k, pin_.v, pin_.g, pin_.beta))
+    Sp = tens(pin_.S)
+    po = torch.empty(pin_.B, pin_.T, pin_.vh, D, device=pq.device)
+
+    toks = pin_.B * pin_.T
+    flops = 7 * D * D * toks * pin_.vh
+    # executed tensor-core flops of the chunked form per 64-token chunk
+    # and head: [K;Q]K^T 2*128*64*128, W^T and U^T 2*(2*128*64*64),
+    # S^T[W^T|(gQ)^T] 2*128*128*128, Delta^T P^T 2*128*64*64,
+    # Delta^T K~ 2*128*128*64
+    tc_flops = (2 * 128 * 64 * 128 + 4 * 128 * 64 * 64 +
+                2 * 128 * 128 * 128 + 2 * 128 * 64 * 64 +
+                2 * 128 * 128 * 64) * (pin_.T // 64) * pin_.B * pin_.vh
+    for prec, name, reps in ((gdn.GDN_PREC_FP32, "fp32", 3),
+                             (gdn.GDN_PREC_BF16X3, "bf16x3", 10),
+                             (gdn.GDN_PREC_BF16, "bf16", 10)):
+        def pstep(i, prec=prec):
+            gdn.gdn_prefill(Sp, pq, pk, pv, pg, pb, po, precision=prec,
+                            stream=stream)
+        pstep(0)
+        pms = time_launches(torch, pstep, reps, stream)
+        entry = {
+            "ms": pms, "tokens_per_s": toks / (pms * 1e-3),
+            "head_steps_per_s": toks * pin_.vh / (pms * 1e-3),
+            "tflops_fp32_equiv": flops / (pms * 1e-3) / 1e12}
+        if prec == gdn.GDN_PREC_FP32:
+            entry["note"] = "token-serial fp32 path"
+        else:
+            mult = 3 if prec == gdn.GDN_PREC_BF16X3 else 1
+            ach = tc_flops * mult / (pms * 1e-3) / 1e12
+            peak = float(peaks.get("bf16_tflops_sustained",
+                                   peaks.get("bf16_tflops", 1900.0)))
+            entry.update({"tensor_tflops": ach, "tensor_peak_tflops": peak,
+                          "tensor_frac": ach / peak,
+                          "note": "chunk-parallel form on tcgen05; "
+                                  "executed MMA flops (x3 for split-bf16)"})
+        parts[f"prefill_b8_t4096_{name}"] = entry
+    del pq, pk, pv, pg, pb, Sp, po
+
+
 # ------------------------------------------------------------- main arm
 
 def main():
@@ -265,6 +337,8 @@ def main():
                     help="skip the verify / prefill sub-measurements")
     ap.add_argument("--no-cpu", action="store_true",
                     help="skip the CPU-baseline leg")
+    ap.add_argument("--only", choices=["prefill"], default=None,
+                    help="time only the prefill parts (used for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -298,12 +372,12 @@ def main():
             dist.barrier()
         torch.cuda.synchronize()
 
-    def max_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+
+    if args.only == "prefill":
+        parts = {}
+        prefill_parts(torch, gdn, tens_fn(torch, dev), stream, peaks, parts)
+        print(json.dumps({"only": "prefill", "parts": parts}), flush=True)
+        return 0
 
     # ---- headline workload: batched decode step
     inp = gdn_inputs.make_workload("decode_b64")
@@ -325,14 +399,13 @@ def main():
         step(i)
     barrier()
     t_wall0 = time.time()
-    ms = time_launches(torch, step, args.steps, stream)
+    ms_local = time_launches(torch, step, args.steps, stream)
     t_wall1 = time.time()
     barrier()
-    ms = max_over_ranks(ms)
     bytes_step = decode_bytes(B, kh, vh)
     heads_per_step = B * vh
-    value = heads_per_step * world / (ms * 1e-3)
-    achieved_gbs = bytes_step / (ms * 1e-3) / 1e9
+    ms, _, value = aggregate(ms_local, heads_per_step, dist, dev)
+    achieved_gbs = bytes_step / (ms_local * 1e-3) / 1e9
 
     # ---- end to end through the public API with host buffers
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
@@ -351,8 +424,10 @@ def main():
     for i in range(args.warmup):
         e2e_step(i)
     barrier()
-    ms_e2e = max_over_ranks(time_launches(torch, e2e_step, args.steps, stream))
-    e2e = {"value": heads_per_step * world / (ms_e2e * 1e-3), "unit": UNIT,
+    ms_e2e, _, e2e_value = aggregate(
+        time_launches(torch, e2e_step, args.steps, stream), heads_per_step,
+        dist, dev)
+    e2e = {"value": e2e_value, "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "ms_per_step": ms_e2e,
            "note": "q, k, v, g, beta copied from pinned host memory and o "
@@ -390,47 +465,7 @@ def main():
                     "bytes_per_launch": nb}
         del Sv, ck
         torch.cuda.empty_cache()
-        pin_ = gdn_inputs.make_workload("prefill_b8_t4096")
-        pq, pk, pv, pg, pb = (tens(x) for x in
-                              (pin_.q, pin_.k, pin_.v, pin_.g, pin_.beta))
-        Sp = tens(pin_.S)
-        po = torch.empty(pin_.B, pin_.T, pin_.vh, D, device=dev)
-
-        toks = pin_.B * pin_.T
-        flops = 7 * D * D * toks * pin_.vh
-        # executed tensor-core flops of the chunked form per 64-token chunk
-        # and head: [K;Q]K^T 2*128*64*128, W/U 2*(2*128*64*64), S[W;Q]
-        # 2*128*128*128, Delta P 2*128*64*64, Delta K 2*128*128*64
-        tc_flops = (2 * 128 * 64 * 128 + 4 * 128 * 64 * 64 +
-                    2 * 128 * 128 * 128 + 2 * 128 * 64 * 64 +
-                    2 * 128 * 128 * 64) * (pin_.T // 64) * pin_.B * pin_.vh
-        for prec, name, reps in ((gdn.GDN_PREC_FP32, "fp32", 3),
-                                 (gdn.GDN_PREC_BF16X3, "bf16x3", 10),
-                                 (gdn.GDN_PREC_TF32, "tf32", 10)):
-            def pstep(i, prec=prec):
-                gdn.gdn_prefill(Sp, pq, pk, pv, pg, pb, po, precision=prec,
-                                stream=stream)
-            pstep(0)
-            pms = time_launches(torch, pstep, reps, stream)
-            entry = {
-                "ms": pms, "tokens_per_s": toks / (pms * 1e-3),
-                "head_steps_per_s": toks * pin_.vh / (pms * 1e-3),
-                "tflops_fp32_equiv": flops / (pms * 1e-3) / 1e12}
-            if prec == gdn.GDN_PREC_FP32:
-                entry["note"] = "token-serial fp32 path"
-            else:
-                mult = 3 if prec == gdn.GDN_PREC_BF16X3 else 1
-                ach = tc_flops * mult / (pms * 1e-3) / 1e12
-                peak = float(peaks.get("bf16_tflops_sustained",
-                                       peaks.get("bf16_tflops", 1900.0)))
-                if prec == gdn.GDN_PREC_TF32:
-                    peak *= 0.5  # tf32 dense rate is half of bf16 (nominal)
-                entry.update({"tensor_tflops": ach, "tensor_peak_tflops": peak,
-                              "tensor_frac": ach / peak,
-                              "note": "chunk-parallel form on tcgen05; "
-                                      "executed MMA flops (x3 for split-bf16)"})
-            parts[f"prefill_b8_t4096_{name}"] = entry
-        del pq, pk, pv, pg, pb, Sp, po
+        prefill_parts(torch, gdn, tens, stream, peaks, parts)
 
     sampler.stop()
     uuid = None

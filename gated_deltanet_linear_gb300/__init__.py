@@ -25,13 +25,13 @@ __all__ = [
     "GDNError", "gdn_step", "gdn_step_m", "gdn_mark", "gdn_rollback",
     "gdn_rollback_seq", "gdn_prefill_workspace", "gdn_prefill",
     "gdn_strerror", "gdn_version", "library_path", "load",
-    "GDN_PREC_FP32", "GDN_PREC_BF16X3", "GDN_PREC_TF32", "GDN_MAX_TOKENS",
+    "GDN_PREC_FP32", "GDN_PREC_BF16X3", "GDN_PREC_BF16", "GDN_MAX_TOKENS",
     "gdn_prefill_timeouts",
 ]
 
 GDN_OK, GDN_EINVAL, GDN_ESHAPE, GDN_EALIGN = 0, -1, -2, -3
 GDN_ECUDA, GDN_ERANGE, GDN_EPTR, GDN_EALIAS = -4, -5, -6, -7
-GDN_PREC_FP32, GDN_PREC_BF16X3, GDN_PREC_TF32 = 0, 1, 2
+GDN_PREC_FP32, GDN_PREC_BF16X3, GDN_PREC_BF16 = 0, 1, 2
 GDN_MAX_TOKENS = 1 << 20
 
 # Every symbol include/gdn.h declares.
@@ -218,7 +218,7 @@ def gdn_prefill(S, q, k, v, g, beta, o, precision=GDN_PREC_FP32, chunk=64,
     """T = q.shape[1] tokens; S updated in place (S_0 -> S_T).
 
     precision: GDN_PREC_FP32 (token-serial, exact to the single-step path),
-    GDN_PREC_BF16X3 or GDN_PREC_TF32 (chunk-parallel on tensor cores)."""
+    GDN_PREC_BF16X3 or GDN_PREC_BF16 (chunk-parallel on tensor cores)."""
     sh = _shape(S, q)
     B, kh, vh, kd, vd = sh.B, sh.kh, sh.vh, sh.kd, sh.vd
     T = int(q.shape[1])

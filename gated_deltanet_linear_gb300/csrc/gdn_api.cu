@@ -203,7 +203,7 @@ int gdn_prefill(const gdn_shape *shape, int T, float *S, const float *q,
   if (precision == GDN_PREC_FP32)
     return steps_common(shape, T, S, S, nullptr, q, k, v, g, beta, o,
                         (cudaStream_t)stream);
-  if (precision != GDN_PREC_BF16X3 && precision != GDN_PREC_TF32)
+  if (precision != GDN_PREC_BF16X3 && precision != GDN_PREC_BF16)
     return GDN_ERANGE;
   int r = check_shape(shape);
   if (r) return r;

@@ -29,7 +29,7 @@ cudaError_t launch_rollback_seq(float *S, const float *snap, const float *ckpt,
 // Chunked tensor-core prefill (defined in gdn_prefill.cu).
 size_t prefill_workspace_bytes(int B, int kh, int vh, int T, int chunk,
                                int precision);
-// precision: 1 = split-bf16, 2 = tf32.
+// precision: 1 = split-bf16 (three products), 2 = bf16 (one product).
 cudaError_t launch_prefill_chunked(float *S, const float *q, const float *k,
                                    const float *v, const float *g,
                                    const float *beta, float *o, int B, int kh,

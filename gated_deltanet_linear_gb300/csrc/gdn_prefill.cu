@@ -12,27 +12,32 @@
 //   Delta = U - W S0                      (the per-token corrections)
 //   O = diag(gamma) Q S0 + P Delta,  P[t,s] = exp(Gamma_t - Gamma_s) q_t.k_s (s <= t)
 //   S_C = gamma_63 S0 + (diag(w) K)^T Delta
-// Everything is computed in the transposed orientation so that the value /
-// key dimension (128) is the MMA's M and the state lives in tensor memory as
-// S^T with one TMEM lane per value column.
 //
 // One CTA per (sequence, value head) walks the chunks in order; the fp32
-// master copy of S^T stays in TMEM for the whole sequence.  Per chunk:
-//   MMA-a  [K;Q] K^T           -> G = K K^T, H = Q K^T           (TMEM)
-//   SIMT   A from G, T = (I+A)^-1 by column-parallel forward substitution
-//   MMA-d  K^T (T diag(beta gamma))^T -> W^T,  V^T (T diag(beta))^T -> U^T
-//   MMA-1  S^T [W; diag(gamma) Q]^T -> (W S)^T, (diag(gamma) Q S)^T
-//   SIMT   Delta^T = U^T - (W S)^T;  S^T *= gamma_63 in TMEM
-//   MMA-3  (diag(gamma) Q S)^T += Delta^T P^T     -> O^T
-//   MMA-4  S^T += Delta^T (diag(w) K)               -> next chunk's S^T
+// state is kept transposed (S^T: one TMEM lane per value column dv, one
+// column per key row dk) in tensor memory for the whole sequence.  Per
+// chunk (D = M x N accumulator in TMEM, lanes = M):
+//   MMA-a  G,H  [t'][s]  = [K; Q] K^T                       (A, B K-major)
+//   SIMT   A from G; T = (I + A)^-1, blocked 16 x 16, fp32
+//   MMA-w  W^T  [dk][t]  = K^T (T diag(beta gamma))^T       (A = K, MN-major)
+//   MMA-u  U^T  [dv][t]  = V^T (T diag(beta))^T             (A = V, MN-major)
+//   MMA-1  (W S)^T [dv][t] = S^T W^T;  (Q S)^T [dv][t] = S^T Q^T
+//                                                           (B = W^T, MN-major)
+//   SIMT   Delta^T = U^T - (W S)^T, also scaled by w;  S^T *= gamma_63;  P
+//   MMA-3  (P Delta)^T = Delta^T P^T
+//   MMA-4  S^T += (Delta^T diag(w)) K                        (B = K, MN-major)
+//   SIMT   O^T = diag(gamma) (Q S)^T + (P Delta)^T  -> o
+// Every operand a thread writes is a row it owns (a row of an input, or a
+// TMEM lane of an earlier result), stored 8 elements at a time; transposes
+// happen in the MMA descriptors (MN-major operands), never in memory.  The
+// next chunk's K, Q, V rows and gates are loaded into registers while the
+// current chunk's last products run.
 //
-// Precision.  Operands live in shared memory in one of two formats:
+// Precision.  Operands are bf16 in shared memory:
 //   split-bf16 ("BF16X3"): x = hi + lo with hi = bf16(x), lo = bf16(x - hi);
-//     a product is hi*hi + hi*lo + lo*hi, three bf16 MMAs with fp32
-//     accumulation (about 16 significant bits per operand, relative error
-//     ~1e-5 on the results);
-//   TF32: x rounded to tf32 (10 explicit mantissa bits), one tf32 MMA
-//     (relative error ~1e-3).
+//     a product is hi*hi + hi*lo + lo*hi, three MMAs with fp32 accumulation
+//     (about 16 significant bits per operand; ~1e-5 relative error);
+//   plain bf16: hi only, one MMA per product (~1e-2 relative error).
 // The triangular solve, the gating exponentials and every accumulation are
 // fp32.
 
@@ -53,88 +58,114 @@ constexpr int kC = 64;       // chunk length
 constexpr int kD = kDim;     // 128
 constexpr int kThreads = 256;
 
-// Shared memory (byte offsets from a 1024-aligned base).  Operand tiles
-// hold R x K elements in 4 bytes each (fp32, or bf16 hi tile + bf16 lo tile).
-constexpr uint32_t OFF_KQ = 0;         // 128 x 128: [K; Q], later [W; gamma Q]
-constexpr uint32_t OFF_KT = 65536;     // 128 x 64: K^T, later (diag(w) K)^T
-constexpr uint32_t OFF_VT = 98304;     // 128 x 64: V^T, later Delta^T
-constexpr uint32_t OFF_TB = 131072;    // 64 x 64: T diag(beta gamma) (and A scratch)
-constexpr uint32_t OFF_TB2 = 147456;   // 64 x 64: T diag(beta), later P
-constexpr uint32_t OFF_ST = 163840;    // 128 x 128: S^T
-constexpr uint32_t OFF_VEC = 229376;   // Gamma, gamma, w, beta: 4 x 64 floats
-constexpr uint32_t OFF_BAR = 230400;   // 4 mbarriers, TMEM address
+// Operand tiles: R rows x C bf16 columns, 128-byte-swizzled blocks of 64
+// columns (see gdn_tc.cuh), hi tile followed by lo tile (R * C * 2 bytes
+// each).  Regions (byte offsets from a 1024-aligned base) are reused by
+// phase:
+//   Ra 64 KB: [K; Q] (128 x 128), the whole chunk
+//   Rb 32 KB: V (64 x 128)            -> Delta^T (128 x 64)
+//   Rc 32 KB: A, T scratch (fp32)     -> T diag(bg), T diag(b) (64 x 64 each)
+//                                     -> W^T (128 x 64) -> Delta^T diag(w)
+//   Rd 64 KB: S^T (128 x 128)         -> P (64 x 64)
+constexpr uint32_t RA = 0, RB = 65536, RC = 98304, RD = 131072;
+constexpr uint32_t OFF_KQ = RA;             // 128 x 128
+constexpr uint32_t OFF_V = RB;              // 64 x 128
+constexpr uint32_t OFF_DT = RB;             // 128 x 64 (after MMA-u)
+constexpr uint32_t OFF_SCR = RC;            // fp32 A [64][64] + T [64][64]
+constexpr uint32_t OFF_TB = RC;             // 64 x 64: T diag(beta gamma)
+constexpr uint32_t OFF_TB2 = RC + 16384;    // 64 x 64: T diag(beta)
+constexpr uint32_t OFF_WT = RC;             // 128 x 64 (after MMA-w/u)
+constexpr uint32_t OFF_DTW = RC;            // 128 x 64 (after MMA-1)
+constexpr uint32_t OFF_ST = RD;             // 128 x 128
+constexpr uint32_t OFF_P = RD;              // 64 x 64 (after MMA-1)
+constexpr uint32_t OFF_VEC = RD + 65536;    // Gamma, gamma, w, beta
+constexpr uint32_t OFF_BAR = OFF_VEC + 1024;
 constexpr uint32_t kSmemUsed = OFF_BAR + 64;
 constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;  // room to align the base
 
 // TMEM columns (512 allocated).
-constexpr uint32_t T_SACC = 0;    // S^T, fp32 master (128 columns = dk)
+constexpr uint32_t T_SACC = 0;    // S^T: lanes dv, 128 columns dk
 constexpr uint32_t T_GH = 128;    // G (lanes 0-63), H (lanes 64-127): 64 columns
 constexpr uint32_t T_W = 192;     // W^T: lanes dk, columns t
 constexpr uint32_t T_U = 256;     // U^T: lanes dv, columns t
 constexpr uint32_t T_D1 = 320;    // (W S)^T: lanes dv, columns t
-constexpr uint32_t T_O = 384;     // (gamma Q S)^T + Delta^T P^T = O^T
+constexpr uint32_t T_QS = 384;    // (Q S)^T: lanes dv, columns t
+constexpr uint32_t T_PD = 448;    // (P Delta)^T: lanes dv, columns t
 
 constexpr uint32_t kWaitLimit = 1u << 24;
+
+// ----------------------------------------------------------- operands
 
 __device__ __forceinline__ uint32_t bf2_bits(__nv_bfloat162 v) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// Store 4 consecutive K elements (k0 % 4 == 0) of row r of an R x K tile.
-template <bool kBF16>
-__device__ __forceinline__ void put4(unsigned char *gb, uint32_t off, int R,
-                                     int K, int r, int k0, float4 x) {
-  if (kBF16) {
-    const __nv_bfloat162 h01 = __floats2bfloat162_rn(x.x, x.y);
-    const __nv_bfloat162 h23 = __floats2bfloat162_rn(x.z, x.w);
-    const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
-    const __nv_bfloat162 l01 = __floats2bfloat162_rn(x.x - f01.x, x.y - f01.y);
-    const __nv_bfloat162 l23 = __floats2bfloat162_rn(x.z - f23.x, x.w - f23.y);
-    const uint32_t o = off + sw128_off(R, r, k0, 2);
-    *reinterpret_cast<uint2 *>(gb + o) = make_uint2(bf2_bits(h01), bf2_bits(h23));
-    *reinterpret_cast<uint2 *>(gb + o + (uint32_t)(R * K * 2)) =
-        make_uint2(bf2_bits(l01), bf2_bits(l23));
-  } else {
-    *reinterpret_cast<float4 *>(gb + off + sw128_off(R, r, k0, 4)) =
-        make_float4(to_tf32(x.x), to_tf32(x.y), to_tf32(x.z), to_tf32(x.w));
-  }
-}
-
-template <bool kBF16>
-__device__ __forceinline__ void put1(unsigned char *gb, uint32_t off, int R,
-                                     int K, int r, int k, float x) {
-  if (kBF16) {
-    const __nv_bfloat16 h = __float2bfloat16_rn(x);
-    const __nv_bfloat16 l = __float2bfloat16_rn(x - __bfloat162float(h));
-    const uint32_t o = off + sw128_off(R, r, k, 2);
-    *reinterpret_cast<__nv_bfloat16 *>(gb + o) = h;
-    *reinterpret_cast<__nv_bfloat16 *>(gb + o + (uint32_t)(R * K * 2)) = l;
-  } else {
-    *reinterpret_cast<float *>(gb + off + sw128_off(R, r, k, 4)) = to_tf32(x);
-  }
-}
-
-// D[M][N] (+)= A[M][K] B[N][K]^T with A an aR x K tile at a, B a bR x K tile
-// at b (the first N rows are used).  Issued by one thread.
-template <bool kBF16>
-__device__ __forceinline__ void gemm(uint32_t d, uint32_t a, int aR,
-                                     uint32_t b, int bR, int K, int M, int N,
-                                     bool accumulate) {
-  if (kBF16) {
-    const uint32_t id = idesc(kFmtBF16, M, N);
-    const uint32_t a_lo = a + (uint32_t)(aR * K * 2);
-    const uint32_t b_lo = b + (uint32_t)(bR * K * 2);
-    for (int ks = 0; ks < K / 16; ++ks) {
-      const uint64_t ah = desc_kstep(a, aR, ks), bh = desc_kstep(b, bR, ks);
-      mma_bf16(d, ah, bh, id, (accumulate || ks > 0) ? 1u : 0u);
-      mma_bf16(d, ah, desc_kstep(b_lo, bR, ks), id, 1u);
-      mma_bf16(d, desc_kstep(a_lo, aR, ks), bh, id, 1u);
+// Store columns c0..c0+7 (c0 % 8 == 0) of row r of an R x C tile.
+template <bool kLo>
+__device__ __forceinline__ void put8(unsigned char *gb, uint32_t off, int R,
+                                     int C, int r, int c0, const float *x) {
+  uint32_t hi[4], lo[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+    hi[i] = bf2_bits(h);
+    if (kLo) {
+      const float2 f = __bfloat1622float2(h);
+      lo[i] = bf2_bits(__floats2bfloat162_rn(x[2 * i] - f.x, x[2 * i + 1] - f.y));
     }
-  } else {
-    const uint32_t id = idesc(kFmtTF32, M, N);
-    for (int ks = 0; ks < K / 8; ++ks)
-      mma_tf32(d, desc_kstep(a, aR, ks), desc_kstep(b, bR, ks), id,
-               (accumulate || ks > 0) ? 1u : 0u);
+  }
+  const uint32_t o = off + sw128_off(R, r, c0, 2);
+  *reinterpret_cast<uint4 *>(gb + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+  if (kLo)
+    *reinterpret_cast<uint4 *>(gb + o + (uint32_t)(R * C * 2)) =
+        make_uint4(lo[0], lo[1], lo[2], lo[3]);
+}
+
+// Shared-memory descriptor of K step ks (16 bf16 of K) of a tile:
+//   K-major: rows are the M (or N) index, columns the K index.
+//   MN-major: rows are the K index, columns the M (or N) index; 64-column
+//   blocks are R * 128 bytes apart (leading byte offset), 8-row groups
+//   1024 bytes apart (stride byte offset), one K step = 16 rows.
+__device__ __forceinline__ uint64_t kmajor(uint32_t base, int R, int ks) {
+  return desc_kstep(base, R, ks);
+}
+
+__device__ __forceinline__ uint64_t mnmajor(uint32_t base, int R, int ks) {
+  uint64_t d = desc_sw128(base + (uint32_t)ks * 2048u);
+  d &= ~((uint64_t)0x3FFF << 16);
+  d |= (uint64_t)(((uint32_t)R * 128u) >> 4) << 16;
+  return d;
+}
+
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn,
+                                                  int b_mn) {
+  return idesc(kFmtBF16, M, N) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16);
+}
+
+struct Operand {
+  uint32_t base;  // hi tile (shared address)
+  int R, C;       // tile shape
+  bool mn;        // MN-major use
+};
+
+// D[M][N] (+)= A B^T over K = 16 * ksteps, issued by one thread.
+template <bool kLo>
+__device__ __forceinline__ void gemm(uint32_t d, const Operand &a,
+                                     const Operand &b, int M, int N,
+                                     int ksteps, bool accumulate) {
+  const uint32_t id = idesc_bf16(M, N, a.mn, b.mn);
+  const uint32_t a_lo = a.base + (uint32_t)(a.R * a.C * 2);
+  const uint32_t b_lo = b.base + (uint32_t)(b.R * b.C * 2);
+  for (int ks = 0; ks < ksteps; ++ks) {
+    const uint64_t ah = a.mn ? mnmajor(a.base, a.R, ks) : kmajor(a.base, a.R, ks);
+    const uint64_t bh = b.mn ? mnmajor(b.base, b.R, ks) : kmajor(b.base, b.R, ks);
+    mma_bf16(d, ah, bh, id, (accumulate || ks > 0) ? 1u : 0u);
+    if (kLo) {
+      const uint64_t bl = b.mn ? mnmajor(b_lo, b.R, ks) : kmajor(b_lo, b.R, ks);
+      const uint64_t al = a.mn ? mnmajor(a_lo, a.R, ks) : kmajor(a_lo, a.R, ks);
+      mma_bf16(d, ah, bl, id, 1u);
+      mma_bf16(d, al, bh, id, 1u);
+    }
   }
 }
 
@@ -144,7 +175,84 @@ __device__ __forceinline__ void cta_sync_tc() {
   fence_after_sync();
 }
 
-template <bool kBF16>
+// fp32 scratch for the triangular solve: A and T, 64 x 64 each, rows of 64
+// floats with the 16-byte groups of row r XOR-ed by (r & 7) so that eight
+// consecutive rows at the same column hit different banks.
+__device__ __forceinline__ int sidx(int r, int c) {
+  return r * 64 + ((((c >> 2) ^ (r & 7)) << 2) | (c & 3));
+}
+
+// T = (I + A)^-1 for strictly lower-triangular A (64 x 64), blocked in
+// 16 x 16 blocks.  All 256 threads; reads Asc, writes Tsc.
+__device__ __forceinline__ void tri_inverse(const float *Asc, float *Tsc,
+                                            int tid) {
+  // 1. Diagonal blocks E_i = (I + A_ii)^-1 by forward substitution: column
+  //    j of block i on 4 lanes, rows split by r mod 4.
+  {
+    const int col = tid >> 2;          // 0..63: block i = col / 16
+    const int q4 = tid & 3;
+    const int blk = col >> 4, jj = col & 15, r0 = blk * 16;
+    float x[4] = {0.f, 0.f, 0.f, 0.f};  // rows r0 + q4 + 4i
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      float part = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        part = fmaf(Asc[sidx(r0 + t, r0 + q4 + 4 * i)], x[i], part);
+      part += __shfl_xor_sync(0xffffffffu, part, 1);
+      part += __shfl_xor_sync(0xffffffffu, part, 2);
+      const float xt = (t == jj ? 1.f : 0.f) - part;
+      if ((t & 3) == q4) x[t >> 2] = xt;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) Tsc[sidx(r0 + q4 + 4 * i, r0 + jj)] = x[i];
+    // zero the strictly-upper blocks of this column (rows above block i)
+    for (int r = q4; r < r0; r += 4) Tsc[sidx(r, r0 + jj)] = 0.f;
+  }
+  __syncthreads();
+  // 2. Off-diagonal blocks by distance d = i - j:
+  //    T_ij = -E_i sum_{k=j}^{i-1} A_ik T_kj.
+  // Thread element (r, c) inside a 16 x 16 block: r = tid >> 4, c = tid & 15.
+  const int er = tid >> 4, ec = tid & 15;
+  for (int d = 1; d < 4; ++d) {
+    float xv[3];
+    const int nb = 4 - d;  // blocks (i, j = i - d), i = d .. 3
+    for (int bi = 0; bi < nb; ++bi) {
+      const int i = d + bi, j = i - d;
+      float acc = 0.f;
+      for (int kb = j; kb < i; ++kb)
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          acc = fmaf(Asc[sidx(16 * i + er, 16 * kb + u)],
+                     Tsc[sidx(16 * kb + u, 16 * j + ec)], acc);
+      xv[bi] = acc;
+    }
+    __syncthreads();
+    // X_ij -> scratch in the (still zero) T_ij block, then T_ij = -E_i X_ij
+    for (int bi = 0; bi < nb; ++bi) {
+      const int i = d + bi, j = i - d;
+      Tsc[sidx(16 * i + er, 16 * j + ec)] = xv[bi];
+    }
+    __syncthreads();
+    for (int bi = 0; bi < nb; ++bi) {
+      const int i = d + bi, j = i - d;
+      float acc = 0.f;
+#pragma unroll
+      for (int u = 0; u < 16; ++u)
+        acc = fmaf(Tsc[sidx(16 * i + er, 16 * i + u)],
+                   Tsc[sidx(16 * i + u, 16 * j + ec)], acc);
+      xv[bi] = -acc;
+    }
+    __syncthreads();
+    for (int bi = 0; bi < nb; ++bi) {
+      const int i = d + bi, j = i - d;
+      Tsc[sidx(16 * i + er, 16 * j + ec)] = xv[bi];
+    }
+    __syncthreads();
+  }
+}
+
+template <bool kLo>
 __global__ void __launch_bounds__(kThreads, 1)
     gdn_chunk_kernel(float *__restrict__ S, const float *__restrict__ q,
                      const float *__restrict__ k, const float *__restrict__ v,
@@ -161,6 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   float *bet = Gam + 192;
   const uint32_t bar0 = sb + OFF_BAR;
   volatile uint32_t *slot = reinterpret_cast<volatile uint32_t *>(gb + OFF_BAR + 32);
+  float *Asc = reinterpret_cast<float *>(gb + OFF_SCR);
+  float *Tsc = Asc + 64 * 64;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -174,11 +284,61 @@ __global__ void __launch_bounds__(kThreads, 1)
   const size_t head_off = (size_t)head * kD * kD;
   const int nchunks = (T + kC - 1) / kC;
 
+  const Operand opKQ{sb + OFF_KQ, 128, 128, false};   // MMA-a A
+  const Operand opKb{sb + OFF_KQ, 128, 128, false};   // MMA-a B (rows 0-63)
+  const Operand opKmn{sb + OFF_KQ, 128, 128, true};   // MMA-w A (rows 0-63)
+  const Operand opVmn{sb + OFF_V, 64, 128, true};     // MMA-u A
+  const Operand opTB{sb + OFF_TB, 64, 64, false};     // MMA-w B
+  const Operand opTB2{sb + OFF_TB2, 64, 64, false};   // MMA-u B
+  const Operand opST{sb + OFF_ST, 128, 128, false};   // MMA-1 A
+  const Operand opWT{sb + OFF_WT, 128, 64, true};     // MMA-1 B (W part)
+  const Operand opQb{sb + OFF_KQ + 64 * 128, 128, 128, false};  // MMA-1 B (Q rows)
+  const Operand opDT{sb + OFF_DT, 128, 64, false};    // MMA-3 A
+  const Operand opP{sb + OFF_P, 64, 64, false};       // MMA-3 B
+  const Operand opDTW{sb + OFF_DTW, 128, 64, false};  // MMA-4 A
+  const Operand opKnB{sb + OFF_KQ, 128, 128, true};   // MMA-4 B (K rows)
+
   if (warp == 0) tmem_alloc(sb + OFF_BAR + 32, 512);
   if (tid == 0)
     for (int i = 0; i < 4; ++i) mbar_init(bar0 + 8 * i, 1);
   cta_sync_tc();
   const uint32_t tmem = *slot;
+  const uint32_t tl = tmem + lane_base;
+
+  // Inputs of one chunk held in registers: rows (tid >> 4) + 16 i of
+  // [K; Q; V] (i = 0..11), columns (tid & 15) * 8 .. + 7; and, on warp 0,
+  // the gates of tokens lane and lane + 32.
+  float4 pre[24];
+  float pg[2], pb[2];
+  auto prefetch = [&](int c) {
+    const int t0 = c * kC;
+    const int n = min(kC, T - t0);
+    const size_t qk_base = ((size_t)b * T + t0) * kh + hh;
+    const size_t v_base = ((size_t)b * T + t0) * vh + vi;
+    const int c0 = (tid & 15) * 8;
+#pragma unroll
+    for (int i = 0; i < 12; ++i) {
+      const int row = (tid >> 4) + 16 * i;
+      const int t = row & (kC - 1);
+      const float *src = i < 4 ? k : (i < 8 ? q : v);
+      if (t < n) {
+        const size_t base = i < 8 ? (qk_base + (size_t)t * kh) * kD
+                                  : (v_base + (size_t)t * vh) * kD;
+        pre[2 * i] = __ldg(reinterpret_cast<const float4 *>(src + base + c0));
+        pre[2 * i + 1] = __ldg(reinterpret_cast<const float4 *>(src + base + c0 + 4));
+      } else {
+        pre[2 * i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        pre[2 * i + 1] = pre[2 * i];
+      }
+    }
+    if (warp == 0) {
+      pg[0] = lane < n ? __ldg(g + v_base + (size_t)lane * vh) : 0.f;
+      pg[1] = lane + 32 < n ? __ldg(g + v_base + (size_t)(lane + 32) * vh) : 0.f;
+      pb[0] = lane < n ? __ldg(beta + v_base + (size_t)lane * vh) : 0.f;
+      pb[1] = lane + 32 < n ? __ldg(beta + v_base + (size_t)(lane + 32) * vh) : 0.f;
+    }
+  };
+  prefetch(0);
 
   // State in: S[dk][dv] -> TMEM lane dv, column dk.
   {
@@ -187,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float r[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) r[j] = __ldg(Sh + (size_t)(c0 + j) * kD + myrow);
-      tmem_st16(tmem + lane_base + T_SACC + c0, r);
+      tmem_st16(tl + T_SACC + c0, r);
     }
   }
   cta_sync_tc();
@@ -197,16 +357,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int c = 0; c < nchunks; ++c) {
     const int t0 = c * kC;
     const int n = min(kC, T - t0);
-    const size_t qk_base = ((size_t)b * T + t0) * kh + hh;   // row of token t0
-    const size_t v_base = ((size_t)b * T + t0) * vh + vi;
+    const size_t v_base = ((size_t)b * T + t0) * vh + vi;   // row of token t0
 
-    // ---------------------------------------------------------- phase 0
+    // ------------------------------------------ phase 0: inputs, S^T operand
     if (warp == 0) {
-      const float ga = lane < n ? __ldg(g + v_base + (size_t)lane * vh) : 0.f;
-      const float gb2 = lane + 32 < n ? __ldg(g + v_base + (size_t)(lane + 32) * vh) : 0.f;
-      bet[lane] = lane < n ? __ldg(beta + v_base + (size_t)lane * vh) : 0.f;
-      bet[lane + 32] = lane + 32 < n ? __ldg(beta + v_base + (size_t)(lane + 32) * vh) : 0.f;
-      float sa = ga, sc = gb2;
+      bet[lane] = pb[0];
+      bet[lane + 32] = pb[1];
+      float sa = pg[0], sc = pg[1];
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const float ya = __shfl_up_sync(0xffffffffu, sa, off);
@@ -225,214 +382,170 @@ __global__ void __launch_bounds__(kThreads, 1)
       wv[lane] = expf(last - sa);
       wv[lane + 32] = expf(last - sc);
     }
-    // [K; Q] rows (token-major), one row per warp iteration, 4 elements/lane.
-    for (int rr = warp; rr < 2 * kC; rr += kThreads / 32) {
-      const int t = rr & (kC - 1);
-      const float *src = rr < kC ? k : q;
-      float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (t < n)
-        x = __ldg(reinterpret_cast<const float4 *>(
-            src + (qk_base + (size_t)t * kh) * kD + 4 * lane));
-      put4<kBF16>(gb, OFF_KQ, 128, 128, rr, 4 * lane, x);
-    }
-    // K^T and V^T: thread owns row r (dk or dv), 4 tokens per store.
-    {
-      const int r = tid & 127;
-      for (int t4 = (tid >> 7) * 4; t4 < kC; t4 += 8) {
-        float kx[4], vx[4];
+    // [K; Q] rows and V rows from the prefetched registers.
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int t = t4 + j;
-          kx[j] = t < n ? __ldg(k + (qk_base + (size_t)t * kh) * kD + r) : 0.f;
-          vx[j] = t < n ? __ldg(v + (v_base + (size_t)t * vh) * kD + r) : 0.f;
-        }
-        put4<kBF16>(gb, OFF_KT, 128, kC, r, t4, make_float4(kx[0], kx[1], kx[2], kx[3]));
-        put4<kBF16>(gb, OFF_VT, 128, kC, r, t4, make_float4(vx[0], vx[1], vx[2], vx[3]));
-      }
+    for (int i = 0; i < 12; ++i) {
+      const int row = (tid >> 4) + 16 * i, c0 = (tid & 15) * 8;
+      const float x[8] = {pre[2 * i].x, pre[2 * i].y, pre[2 * i].z, pre[2 * i].w,
+                          pre[2 * i + 1].x, pre[2 * i + 1].y, pre[2 * i + 1].z,
+                          pre[2 * i + 1].w};
+      if (i < 8)
+        put8<kLo>(gb, OFF_KQ, 128, 128, row, c0, x);
+      else
+        put8<kLo>(gb, OFF_V, 64, 128, row & (kC - 1), c0, x);
     }
-    // S^T operand from the TMEM master copy.
+    // S^T operand (rows dv, columns dk) from the TMEM master copy.
     for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
       float r[16];
-      tmem_ld16(tmem + lane_base + T_SACC + c0, r);
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        put4<kBF16>(gb, OFF_ST, 128, 128, myrow, c0 + 4 * i,
-                    make_float4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]));
+      tmem_ld16(tl + T_SACC + c0, r);
+      put8<kLo>(gb, OFF_ST, 128, 128, myrow, c0, r);
+      put8<kLo>(gb, OFF_ST, 128, 128, myrow, c0 + 8, r + 8);
     }
     fence_proxy_async();
     cta_sync_tc();
 
-    // ------------------------------------------- phase 1: G, H = [K;Q] K^T
+    // --------------------------------------- phase 1: G, H = [K;Q] K^T
     if (tid == 0) {
-      gemm<kBF16>(tmem + T_GH, sb + OFF_KQ, 128, sb + OFF_KQ, 128, kD, 128, kC, false);
+      gemm<kLo>(tmem + T_GH, opKQ, opKb, 128, kC, kD / 16, false);
       commit(bar0);
     }
     if (!__syncthreads_and(mbar_wait(bar0, parity, kWaitLimit))) { failed = true; break; }
     fence_after_sync();
 
-    // ------------------------------- phase 2: A and T = (I + A)^-1 (fp32)
-    // A scratch, fp32 [64][64], permuted so that the 16 entries a solver
-    // thread needs for one row are contiguous: (t, s) -> t*64 + (s&3)*16 + s/4.
-    float *Asc = reinterpret_cast<float *>(gb + OFF_TB);
-    if (quad < 2) {
+    // -------------------------- phase 2: A, T = (I + A)^-1, T diag operands
+    if (quad < 2) {  // lanes 0-63 hold G rows t
       const int t = myrow;
+      const float bt = bet[t], Gt = Gam[t];
       for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
         float r[16];
-        tmem_ld16(tmem + lane_base + T_GH + c0, r);
+        tmem_ld16(tl + T_GH + c0, r);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int s = c0 + j;
-          const float a = s < t ? bet[t] * expf(Gam[t] - Gam[s]) * r[j] : 0.f;
-          Asc[t * 64 + (s & 3) * 16 + (s >> 2)] = a;
+        for (int j4 = 0; j4 < 4; ++j4) {
+          float4 a4;
+          float *a = &a4.x;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int s = c0 + 4 * j4 + e;
+            a[e] = s < t ? bt * expf(Gt - Gam[s]) * r[4 * j4 + e] : 0.f;
+          }
+          *reinterpret_cast<float4 *>(Asc + sidx(t, c0 + 4 * j4)) = a4;
         }
       }
     }
     __syncthreads();
-    float x[16];
+    tri_inverse(Asc, Tsc, tid);
     {
-      // Column j of T, rows split over 4 lanes by t mod 4.
-      const int j = tid >> 2, q4 = tid & 3;
+      // each thread takes one row-half of T: row t = tid >> 2, 16 columns
+      const int t = tid >> 2, cq = (tid & 3) * 16;
+      float tr[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) x[i] = 0.f;
+      for (int e = 0; e < 16; ++e) tr[e] = Tsc[sidx(t, cq + e)];
+      __syncthreads();  // everyone holds its T values; scratch may be reused
+      float x1[8], x2[8];
 #pragma unroll
-      for (int t = 0; t < kC; ++t) {
-        const float4 *arow = reinterpret_cast<const float4 *>(Asc + t * 64 + q4 * 16);
-        float part = 0.f;
+      for (int h8 = 0; h8 < 2; ++h8) {
 #pragma unroll
-        for (int i4 = 0; i4 < 4; ++i4) {
-          const float4 a = arow[i4];
-          part = fmaf(a.x, x[4 * i4 + 0], part);
-          part = fmaf(a.y, x[4 * i4 + 1], part);
-          part = fmaf(a.z, x[4 * i4 + 2], part);
-          part = fmaf(a.w, x[4 * i4 + 3], part);
+        for (int e = 0; e < 8; ++e) {
+          const int s = cq + 8 * h8 + e;
+          x1[e] = tr[8 * h8 + e] * bet[s] * gam[s];
+          x2[e] = tr[8 * h8 + e] * bet[s];
         }
-        part += __shfl_xor_sync(0xffffffffu, part, 1);
-        part += __shfl_xor_sync(0xffffffffu, part, 2);
-        const float xt = (t == j ? 1.f : 0.f) - part;
-        if ((t & 3) == q4) x[t >> 2] = xt;
-      }
-    }
-    __syncthreads();  // everyone is done with the A scratch
-    {
-      const int j = tid >> 2, q4 = tid & 3;
-      const float bg = bet[j] * gam[j], bj = bet[j];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int t = q4 + 4 * i;
-        put1<kBF16>(gb, OFF_TB, kC, kC, t, j, x[i] * bg);
-        put1<kBF16>(gb, OFF_TB2, kC, kC, t, j, x[i] * bj);
+        put8<kLo>(gb, OFF_TB, kC, kC, t, cq + 8 * h8, x1);
+        put8<kLo>(gb, OFF_TB2, kC, kC, t, cq + 8 * h8, x2);
       }
     }
     fence_proxy_async();
     cta_sync_tc();
 
-    // ------------------------------------------------- phase 3: W^T, U^T
+    // ------------------------------------------------ phase 3: W^T, U^T
     if (tid == 0) {
-      gemm<kBF16>(tmem + T_W, sb + OFF_KT, 128, sb + OFF_TB, kC, kC, 128, kC, false);
-      gemm<kBF16>(tmem + T_U, sb + OFF_VT, 128, sb + OFF_TB2, kC, kC, 128, kC, false);
+      gemm<kLo>(tmem + T_W, opKmn, opTB, 128, kC, kC / 16, false);
+      gemm<kLo>(tmem + T_U, opVmn, opTB2, 128, kC, kC / 16, false);
       commit(bar0 + 8);
     }
     if (!__syncthreads_and(mbar_wait(bar0 + 8, parity, kWaitLimit))) { failed = true; break; }
     fence_after_sync();
 
-    // ----------------- phase 4: [W; gamma Q], (diag(w) K)^T and P operands
+    // ------------------------------------------- phase 4: W^T operand
     for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
       float r[16];
-      tmem_ld16(tmem + lane_base + T_W + c0, r);  // lane dk, columns t
-#pragma unroll
-      for (int jj = 0; jj < 16; ++jj) put1<kBF16>(gb, OFF_KQ, 128, 128, c0 + jj, myrow, r[jj]);
-    }
-    for (int t = warp; t < kC; t += kThreads / 32) {
-      float4 x4 = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (t < n) {
-        x4 = __ldg(reinterpret_cast<const float4 *>(
-            q + (qk_base + (size_t)t * kh) * kD + 4 * lane));
-        const float gt = gam[t];
-        x4.x *= gt; x4.y *= gt; x4.z *= gt; x4.w *= gt;
-      }
-      put4<kBF16>(gb, OFF_KQ, 128, 128, kC + t, 4 * lane, x4);
-    }
-    {
-      const int r = tid & 127;
-      for (int t4 = (tid >> 7) * 4; t4 < kC; t4 += 8) {
-        float kx[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int t = t4 + j;
-          kx[j] = t < n ? __ldg(k + (qk_base + (size_t)t * kh) * kD + r) * wv[t] : 0.f;
-        }
-        put4<kBF16>(gb, OFF_KT, 128, kC, r, t4, make_float4(kx[0], kx[1], kx[2], kx[3]));
-      }
-    }
-    if (quad >= 2) {
-      const int t = myrow - kC;
-      for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
-        float r[16];
-        tmem_ld16(tmem + lane_base + T_GH + c0, r);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float pv[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int s = c0 + 4 * i + e;
-            pv[e] = s <= t ? expf(Gam[t] - Gam[s]) * r[4 * i + e] : 0.f;
-          }
-          put4<kBF16>(gb, OFF_TB2, kC, kC, t, c0 + 4 * i, make_float4(pv[0], pv[1], pv[2], pv[3]));
-        }
-      }
+      tmem_ld16(tl + T_W + c0, r);  // lane dk, columns t
+      put8<kLo>(gb, OFF_WT, 128, kC, myrow, c0, r);
+      put8<kLo>(gb, OFF_WT, 128, kC, myrow, c0 + 8, r + 8);
     }
     fence_proxy_async();
     cta_sync_tc();
 
-    // ---------------------------- phase 5: S^T [W; gamma Q]^T -> D1, O
+    // ----------------------------- phase 5: (W S)^T, (Q S)^T = S^T [W^T | Q^T]
     if (tid == 0) {
-      gemm<kBF16>(tmem + T_D1, sb + OFF_ST, 128, sb + OFF_KQ, 128, kD, 128, 2 * kC, false);
+      gemm<kLo>(tmem + T_D1, opST, opWT, 128, kC, kD / 16, false);
+      gemm<kLo>(tmem + T_QS, opST, opQb, 128, kC, kD / 16, false);
       commit(bar0 + 16);
     }
     if (!__syncthreads_and(mbar_wait(bar0 + 16, parity, kWaitLimit))) { failed = true; break; }
     fence_after_sync();
 
-    // ------------------- phase 6: Delta^T = U^T - (W S)^T; S^T *= gamma_63
+    // ---- phase 6: Delta^T = U^T - (W S)^T, Delta^T diag(w); P; S^T *= gamma_63
     for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
       float u[16], d[16];
-      tmem_ld16(tmem + lane_base + T_U + c0, u);
-      tmem_ld16(tmem + lane_base + T_D1 + c0, d);
+      tmem_ld16(tl + T_U + c0, u);
+      tmem_ld16(tl + T_D1 + c0, d);
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        put4<kBF16>(gb, OFF_VT, 128, kC, myrow, c0 + 4 * i,
-                    make_float4(u[4 * i] - d[4 * i], u[4 * i + 1] - d[4 * i + 1],
-                                u[4 * i + 2] - d[4 * i + 2], u[4 * i + 3] - d[4 * i + 3]));
+      for (int e = 0; e < 16; ++e) u[e] -= d[e];
+      put8<kLo>(gb, OFF_DT, 128, kC, myrow, c0, u);
+      put8<kLo>(gb, OFF_DT, 128, kC, myrow, c0 + 8, u + 8);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) u[e] *= wv[c0 + e];
+      put8<kLo>(gb, OFF_DTW, 128, kC, myrow, c0, u);
+      put8<kLo>(gb, OFF_DTW, 128, kC, myrow, c0 + 8, u + 8);
+    }
+    if (quad >= 2) {  // lanes 64-127 hold H rows t
+      const int t = myrow - kC;
+      const float Gt = Gam[t];
+      for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
+        float r[16];
+        tmem_ld16(tl + T_GH + c0, r);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int s = c0 + e;
+          r[e] = s <= t ? expf(Gt - Gam[s]) * r[e] : 0.f;
+        }
+        put8<kLo>(gb, OFF_P, kC, kC, t, c0, r);
+        put8<kLo>(gb, OFF_P, kC, kC, t, c0 + 8, r + 8);
+      }
     }
     {
       const float gC = gam[kC - 1];
       for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
         float r[16];
-        tmem_ld16(tmem + lane_base + T_SACC + c0, r);
+        tmem_ld16(tl + T_SACC + c0, r);
 #pragma unroll
         for (int j = 0; j < 16; ++j) r[j] *= gC;
-        tmem_st16(tmem + lane_base + T_SACC + c0, r);
+        tmem_st16(tl + T_SACC + c0, r);
       }
     }
     fence_proxy_async();
     cta_sync_tc();
 
-    // -------------------- phase 7: O^T += Delta^T P^T; S^T += Delta^T K~
+    // ---------- phase 7: (P Delta)^T = Delta^T P^T; S^T += Delta^T diag(w) K
     if (tid == 0) {
-      gemm<kBF16>(tmem + T_O, sb + OFF_VT, 128, sb + OFF_TB2, kC, kC, 128, kC, true);
-      gemm<kBF16>(tmem + T_SACC, sb + OFF_VT, 128, sb + OFF_KT, 128, kC, 128, kD, true);
+      gemm<kLo>(tmem + T_PD, opDT, opP, 128, kC, kC / 16, false);
+      gemm<kLo>(tmem + T_SACC, opDTW, opKnB, 128, kD, kC / 16, true);
       commit(bar0 + 24);
     }
+    if (c + 1 < nchunks) prefetch(c + 1);  // overlaps the products above
     if (!__syncthreads_and(mbar_wait(bar0 + 24, parity, kWaitLimit))) { failed = true; break; }
     fence_after_sync();
 
-    // ------------------------------------------------ phase 8: o out
+    // --------------------------- phase 8: o = diag(gamma) Q S + P Delta
     for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
-      float r[16];
-      tmem_ld16(tmem + lane_base + T_O + c0, r);
+      float r[16], pd[16];
+      tmem_ld16(tl + T_QS + c0, r);
+      tmem_ld16(tl + T_PD + c0, pd);
 #pragma unroll
       for (int jj = 0; jj < 16; ++jj) {
         const int t = c0 + jj;
-        if (t < n) o[(v_base + (size_t)t * vh) * kD + myrow] = r[jj];
+        if (t < n) o[(v_base + (size_t)t * vh) * kD + myrow] = fmaf(gam[t], r[jj], pd[jj]);
       }
     }
     cta_sync_tc();
@@ -443,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *Sh = S + head_off;
     for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
       float r[16];
-      tmem_ld16(tmem + lane_base + T_SACC + c0, r);
+      tmem_ld16(tl + T_SACC + c0, r);
 #pragma unroll
       for (int j = 0; j < 16; ++j) Sh[(size_t)(c0 + j) * kD + myrow] = r[j];
     }

@@ -38,8 +38,10 @@
  *     returns GDN_ECUDA.  Asynchronous faults surface on the stream as
  *     usual CUDA errors.
  *   - Precision: fp32 throughout (expf from CUDA's math library, fused
- *     multiply-adds, fixed reduction trees).  Results are deterministic: the
- *     same inputs and shape give the same bits on every call.
+ *     multiply-adds, fixed reduction trees), except the chunked prefill
+ *     modes, whose tensor-core products take bf16 operands (see
+ *     gdn_prefill).  Results are deterministic: the same inputs and shape
+ *     give the same bits on every call.
  */
 #ifndef GDN_GB300_H
 #define GDN_GB300_H
@@ -82,8 +84,8 @@ enum {
     GDN_PREC_BF16X3 = 1, /* chunked, tensor cores, operands split into bf16
                             hi + lo, 3 products per term, fp32 accumulation:
                             relative error ~1e-5                             */
-    GDN_PREC_TF32 = 2    /* chunked, tensor cores, operands rounded to tf32:
-                            relative error ~1e-3                             */
+    GDN_PREC_BF16 = 2    /* chunked, tensor cores, operands rounded to bf16,
+                            one product per term: relative error ~1e-2       */
 };
 
 /*
@@ -166,7 +168,7 @@ size_t gdn_prefill_workspace(const gdn_shape *shape, int T, int chunk,
  * precision GDN_PREC_FP32: the token-serial path, bit-identical to T
  *   successive gdn_step calls; chunk and workspace are ignored (pass 0 /
  *   NULL).
- * GDN_PREC_BF16X3 / GDN_PREC_TF32: the chunk-parallel form with chunk ==
+ * GDN_PREC_BF16X3 / GDN_PREC_BF16: the chunk-parallel form with chunk ==
  *   64 (GDN_ERANGE otherwise), its dense products on tcgen05 tensor cores
  *   with fp32 accumulation and the state kept in tensor memory; one CTA
  *   per (sequence, value head) walks the chunks in order.  The chunked form

@@ -6,8 +6,8 @@ value heads for o, per (sequence, value head) for the state):
                    into bf16 hi + lo (about 16 significant bits) and three
                    products are accumulated in fp32, so the expected error
                    is ~1e-5.
-  GDN_PREC_TF32    8 * 2^-11 = 3.9e-3.  tf32 keeps 10 explicit mantissa bits
-                   (unit roundoff 2^-11); a few roundings compound through
+  GDN_PREC_BF16    8 * 2^-9 = 1.6e-2.  bf16 keeps 7 explicit mantissa bits
+                   (unit roundoff 2^-9); a few roundings compound through
                    the chunk products.
 """
 
@@ -24,8 +24,8 @@ from gpu_util import dev, empty, host
 
 pytestmark = pytest.mark.gpu
 
-TOL = {gdn.GDN_PREC_BF16X3: 1e-4, gdn.GDN_PREC_TF32: 8 * 2.0 ** -11}
-NAME = {gdn.GDN_PREC_BF16X3: "bf16x3", gdn.GDN_PREC_TF32: "tf32"}
+TOL = {gdn.GDN_PREC_BF16X3: 1e-4, gdn.GDN_PREC_BF16: 8 * 2.0 ** -9}
+NAME = {gdn.GDN_PREC_BF16X3: "bf16x3", gdn.GDN_PREC_BF16: "bf16"}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -48,7 +48,7 @@ def errs(S, o, S_ref, o_ref):
     return (max_rel(S, S_ref, axes=(-2, -1)), max_rel(o, o_ref, axes=(-2, -1)))
 
 
-@pytest.mark.parametrize("precision", [gdn.GDN_PREC_BF16X3, gdn.GDN_PREC_TF32],
+@pytest.mark.parametrize("precision", [gdn.GDN_PREC_BF16X3, gdn.GDN_PREC_BF16],
                          ids=lambda p: NAME[p])
 @pytest.mark.parametrize("T,zero,g_scale", [(150, True, 0.1), (150, False, 1.0),
                                             (1, False, 1.0), (64, True, 0.1),
@@ -66,7 +66,7 @@ def test_chunked_vs_oracle(oracle_mod, precision, T, zero, g_scale):
     assert gdn.gdn_prefill_timeouts() == 0
 
 
-@pytest.mark.parametrize("precision", [gdn.GDN_PREC_BF16X3, gdn.GDN_PREC_TF32],
+@pytest.mark.parametrize("precision", [gdn.GDN_PREC_BF16X3, gdn.GDN_PREC_BF16],
                          ids=lambda p: NAME[p])
 def test_chunked_full_size_sampled(oracle_mod, precision):
     """8 sequences x 4096 tokens x 48 heads in one launch; the oracle
@@ -120,7 +120,7 @@ def test_chunked_refusals():
                                0, st) == gdn.GDN_ERANGE
     bad = list(ptrs)
     bad[6] = S.data_ptr()  # o overlapping S
-    assert lib.gdn_prefill(ctypes.byref(sh), T, *bad, 64, gdn.GDN_PREC_TF32,
+    assert lib.gdn_prefill(ctypes.byref(sh), T, *bad, 64, gdn.GDN_PREC_BF16,
                            None, 0, st) == gdn.GDN_EALIAS
     assert gdn.gdn_prefill_workspace(1, 16, 48, T, 64,
                                      gdn.GDN_PREC_BF16X3) == 0
