@@ -21,12 +21,13 @@
 //   SIMT   A from G; T = (I + A)^-1, blocked 16 x 16, fp32
 //   MMA-w  W^T  [dk][t]  = K^T (T diag(beta gamma))^T       (A = K, MN-major)
 //   MMA-u  U^T  [dv][t]  = V^T (T diag(beta))^T             (A = V, MN-major)
-//   MMA-1  (W S)^T [dv][t] = S^T W^T;  (Q S)^T [dv][t] = S^T Q^T
-//                                                           (B = W^T, MN-major)
-//   SIMT   Delta^T = U^T - (W S)^T, also scaled by w;  S^T *= gamma_63;  P
+//   MMA-1  Delta^T = U^T - S^T W^T (negated A, accumulated onto U^T);
+//          (Q S)^T [dv][t] = S^T Q^T                        (B = W^T, MN-major)
+//   SIMT   Delta^T also scaled by w;  S^T *= gamma_63;  P (built with A)
 //   MMA-3  (P Delta)^T = Delta^T P^T
 //   MMA-4  S^T += (Delta^T diag(w)) K                        (B = K, MN-major)
-//   SIMT   O^T = diag(gamma) (Q S)^T + (P Delta)^T  -> o
+//   SIMT   O^T = diag(gamma) (Q S)^T + (P Delta)^T  -> o, emitted while the
+//          next chunk's first product runs
 // Every operand a thread writes is a row it owns (a row of an input, or a
 // TMEM lane of an earlier result), stored 8 elements at a time; transposes
 // happen in the MMA descriptors (MN-major operands), never in memory.  The
@@ -78,17 +79,16 @@ constexpr uint32_t OFF_WT = RC;             // 128 x 64 (after MMA-w/u)
 constexpr uint32_t OFF_DTW = RC;            // 128 x 64 (after MMA-1)
 constexpr uint32_t OFF_ST = RD;             // 128 x 128
 constexpr uint32_t OFF_P = RD;              // 64 x 64 (after MMA-1)
-constexpr uint32_t OFF_VEC = RD + 65536;    // Gamma, gamma, w, beta
-constexpr uint32_t OFF_BAR = OFF_VEC + 1024;
+constexpr uint32_t OFF_VEC = RD + 65536;    // Gamma, gamma, w, beta, gamma x 2
+constexpr uint32_t OFF_BAR = OFF_VEC + 2048;
 constexpr uint32_t kSmemUsed = OFF_BAR + 64;
 constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;  // room to align the base
 
 // TMEM columns (512 allocated).
 constexpr uint32_t T_SACC = 0;    // S^T: lanes dv, 128 columns dk
-constexpr uint32_t T_GH = 128;    // G (lanes 0-63), H (lanes 64-127): 64 columns
+constexpr uint32_t T_GH = 128;    // G (lanes 0-63), H then P (lanes 64-127): 64 columns
 constexpr uint32_t T_W = 192;     // W^T: lanes dk, columns t
-constexpr uint32_t T_U = 256;     // U^T: lanes dv, columns t
-constexpr uint32_t T_D1 = 320;    // (W S)^T: lanes dv, columns t
+constexpr uint32_t T_U = 256;     // U^T, then Delta^T = U^T - (W S)^T: lanes dv
 constexpr uint32_t T_QS = 384;    // (Q S)^T: lanes dv, columns t
 constexpr uint32_t T_PD = 448;    // (P Delta)^T: lanes dv, columns t
 
@@ -152,8 +152,9 @@ struct Operand {
 template <bool kLo>
 __device__ __forceinline__ void gemm(uint32_t d, const Operand &a,
                                      const Operand &b, int M, int N,
-                                     int ksteps, bool accumulate) {
-  const uint32_t id = idesc_bf16(M, N, a.mn, b.mn);
+                                     int ksteps, bool accumulate,
+                                     bool negate_a = false) {
+  const uint32_t id = idesc_bf16(M, N, a.mn, b.mn) | (negate_a ? (1u << 13) : 0u);
   const uint32_t a_lo = a.base + (uint32_t)(a.R * a.C * 2);
   const uint32_t b_lo = b.base + (uint32_t)(b.R * b.C * 2);
   for (int ks = 0; ks < ksteps; ++ks) {
@@ -182,12 +183,40 @@ __device__ __forceinline__ int sidx(int r, int c) {
   return r * 64 + ((((c >> 2) ^ (r & 7)) << 2) | (c & 3));
 }
 
-// T = (I + A)^-1 for strictly lower-triangular A (64 x 64), blocked in
-// 16 x 16 blocks.  All 256 threads; reads Asc, writes Tsc.
-__device__ __forceinline__ void tri_inverse(const float *Asc, float *Tsc,
-                                            int tid) {
-  // 1. Diagonal blocks E_i = (I + A_ii)^-1 by forward substitution: column
-  //    j of block i on 4 lanes, rows split by r mod 4.
+// Y[r][c0..c0+3] = sum_{u < n} X[xr][xc + u] * Z[zr + u][zc + c0 .. +3] over
+// the fp32 scratch layout; returns the four sums.
+__device__ __forceinline__ float4 row_times(const float *X, int xr, int xc,
+                                            const float *Z, int zr, int zc,
+                                            int n) {
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int u4 = 0; u4 < n; u4 += 4) {
+    const float4 a = *reinterpret_cast<const float4 *>(X + sidx(xr, xc + u4));
+    const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float4 z = *reinterpret_cast<const float4 *>(Z + sidx(zr + u4 + e, zc));
+      acc.x = fmaf(av[e], z.x, acc.x);
+      acc.y = fmaf(av[e], z.y, acc.y);
+      acc.z = fmaf(av[e], z.z, acc.z);
+      acc.w = fmaf(av[e], z.w, acc.w);
+    }
+  }
+  return acc;
+}
+
+__device__ __forceinline__ void put_row4(float *X, int r, int c, float4 v) {
+  *reinterpret_cast<float4 *>(X + sidx(r, c)) = v;
+}
+
+// T = (I + A)^-1 for strictly lower-triangular A (64 x 64), by divide and
+// conquer: invert the four 16 x 16 diagonal blocks, merge them into 32 x 32
+// inverses, then into the 64 x 64 inverse, using
+//   [[E1, 0], [A21, E2]]^-1 = [[E1^-1, 0], [-E2^-1 A21 E1^-1, E2^-1]].
+// All 256 threads.  Reads the lower triangle of Asc; its upper triangle
+// (zero, never read as A) holds the intermediate products.  Writes Tsc.
+__device__ __forceinline__ void tri_inverse(float *Asc, float *Tsc, int tid) {
+  // 1. Diagonal blocks by forward substitution: column j of block i on 4
+  //    lanes, rows split by r mod 4.
   {
     const int col = tid >> 2;          // 0..63: block i = col / 16
     const int q4 = tid & 3;
@@ -206,50 +235,54 @@ __device__ __forceinline__ void tri_inverse(const float *Asc, float *Tsc,
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) Tsc[sidx(r0 + q4 + 4 * i, r0 + jj)] = x[i];
-    // zero the strictly-upper blocks of this column (rows above block i)
+    // zero the strictly-upper part of this column
     for (int r = q4; r < r0; r += 4) Tsc[sidx(r, r0 + jj)] = 0.f;
   }
   __syncthreads();
-  // 2. Off-diagonal blocks by distance d = i - j:
-  //    T_ij = -E_i sum_{k=j}^{i-1} A_ik T_kj.
-  // Thread element (r, c) inside a 16 x 16 block: r = tid >> 4, c = tid & 15.
-  const int er = tid >> 4, ec = tid & 15;
-  for (int d = 1; d < 4; ++d) {
-    float xv[3];
-    const int nb = 4 - d;  // blocks (i, j = i - d), i = d .. 3
-    for (int bi = 0; bi < nb; ++bi) {
-      const int i = d + bi, j = i - d;
-      float acc = 0.f;
-      for (int kb = j; kb < i; ++kb)
-#pragma unroll
-        for (int u = 0; u < 16; ++u)
-          acc = fmaf(Asc[sidx(16 * i + er, 16 * kb + u)],
-                     Tsc[sidx(16 * kb + u, 16 * j + ec)], acc);
-      xv[bi] = acc;
-    }
-    __syncthreads();
-    // X_ij -> scratch in the (still zero) T_ij block, then T_ij = -E_i X_ij
-    for (int bi = 0; bi < nb; ++bi) {
-      const int i = d + bi, j = i - d;
-      Tsc[sidx(16 * i + er, 16 * j + ec)] = xv[bi];
-    }
-    __syncthreads();
-    for (int bi = 0; bi < nb; ++bi) {
-      const int i = d + bi, j = i - d;
-      float acc = 0.f;
-#pragma unroll
-      for (int u = 0; u < 16; ++u)
-        acc = fmaf(Tsc[sidx(16 * i + er, 16 * i + u)],
-                   Tsc[sidx(16 * i + u, 16 * j + ec)], acc);
-      xv[bi] = -acc;
-    }
-    __syncthreads();
-    for (int bi = 0; bi < nb; ++bi) {
-      const int i = d + bi, j = i - d;
-      Tsc[sidx(16 * i + er, 16 * j + ec)] = xv[bi];
-    }
-    __syncthreads();
+  // 2. 16 -> 32: blocks (1,0) and (3,2).  Thread: block pair p, row r,
+  //    columns 4 c4 .. 4 c4 + 3.  X = A_{i,i-1} E_{i-1} goes to the upper
+  //    block (i-1, i) of the A scratch.
+  if (tid < 128) {
+    const int pr = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
+    const int i = 2 * pr + 1, j = i - 1;
+    put_row4(Asc, 16 * j + r, 16 * i + c4,
+             row_times(Asc, 16 * i + r, 16 * j, Tsc, 16 * j, 16 * j + c4, 16));
   }
+  __syncthreads();
+  if (tid < 128) {
+    const int pr = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
+    const int i = 2 * pr + 1, j = i - 1;
+    // T_ij = -E_i X  (E_i = T block (i, i), X in A scratch block (j, i))
+    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int u4 = 0; u4 < 16; u4 += 4) {
+      const float4 e = *reinterpret_cast<const float4 *>(Tsc + sidx(16 * i + r, 16 * i + u4));
+      const float ev[4] = {e.x, e.y, e.z, e.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 z = *reinterpret_cast<const float4 *>(Asc + sidx(16 * j + u4 + q, 16 * i + c4));
+        y.x = fmaf(ev[q], z.x, y.x);
+        y.y = fmaf(ev[q], z.y, y.y);
+        y.z = fmaf(ev[q], z.z, y.z);
+        y.w = fmaf(ev[q], z.w, y.w);
+      }
+    }
+    put_row4(Tsc, 16 * i + r, 16 * j + c4, make_float4(-y.x, -y.y, -y.z, -y.w));
+  }
+  __syncthreads();
+  // 3. 32 -> 64: X = A[32:64, 0:32] T[0:32, 0:32] goes to A scratch
+  //    [0:32, 32:64]; then T[32:64, 0:32] = -T[32:64, 32:64] X.
+  {
+    const int r = tid >> 3, c4 = (tid & 7) * 4;
+    put_row4(Asc, r, 32 + c4, row_times(Asc, 32 + r, 0, Tsc, 0, c4, 32));
+  }
+  __syncthreads();
+  {
+    const int r = tid >> 3, c4 = (tid & 7) * 4;
+    const float4 y = row_times(Tsc, 32 + r, 32, Asc, 0, 32 + c4, 32);
+    put_row4(Tsc, 32 + r, c4, make_float4(-y.x, -y.y, -y.z, -y.w));
+  }
+  __syncthreads();
 }
 
 template <bool kLo>
@@ -267,6 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float *gam = Gam + 64;
   float *wv = Gam + 128;
   float *bet = Gam + 192;
+  float *gam_o = Gam + 256;       // [2][64]: gamma of the chunk whose o is pending
   const uint32_t bar0 = sb + OFF_BAR;
   volatile uint32_t *slot = reinterpret_cast<volatile uint32_t *>(gb + OFF_BAR + 32);
   float *Asc = reinterpret_cast<float *>(gb + OFF_SCR);
@@ -352,13 +386,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   cta_sync_tc();
 
+  // o for chunk cc = diag(gamma) (Q S)^T + (P Delta)^T, read from TMEM.
+  auto emit_o = [&](int cc) {
+    const int nn = min(kC, T - cc * kC);
+    const size_t vb = ((size_t)b * T + (size_t)cc * kC) * vh + vi;
+    const float *gm = gam_o + (cc & 1) * 64;
+    for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
+      float r[16], pd[16];
+      tmem_ld16(tl + T_QS + c0, r);
+      tmem_ld16(tl + T_PD + c0, pd);
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) {
+        const int t = c0 + jj;
+        if (t < nn) o[(vb + (size_t)t * vh) * kD + myrow] = fmaf(gm[t], r[jj], pd[jj]);
+      }
+    }
+  };
+
   uint32_t parity = 0;
   bool failed = false;
   for (int c = 0; c < nchunks; ++c) {
-    const int t0 = c * kC;
-    const int n = min(kC, T - t0);
-    const size_t v_base = ((size_t)b * T + t0) * vh + vi;   // row of token t0
-
     // ------------------------------------------ phase 0: inputs, S^T operand
     if (warp == 0) {
       bet[lane] = pb[0];
@@ -379,6 +426,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       Gam[lane + 32] = sc;
       gam[lane] = expf(sa);
       gam[lane + 32] = expf(sc);
+      gam_o[(c & 1) * 64 + lane] = gam[lane];
+      gam_o[(c & 1) * 64 + lane + 32] = gam[lane + 32];
       wv[lane] = expf(last - sa);
       wv[lane + 32] = expf(last - sc);
     }
@@ -409,6 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       gemm<kLo>(tmem + T_GH, opKQ, opKb, 128, kC, kD / 16, false);
       commit(bar0);
     }
+    if (c > 0) emit_o(c - 1);  // the previous chunk's output, under this product
     if (!__syncthreads_and(mbar_wait(bar0, parity, kWaitLimit))) { failed = true; break; }
     fence_after_sync();
 
@@ -430,6 +480,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           *reinterpret_cast<float4 *>(Asc + sidx(t, c0 + 4 * j4)) = a4;
         }
+      }
+    }
+    if (quad >= 2) {  // lanes 64-127 hold H rows t: P in place of H
+      const int t = myrow - kC;
+      const float Gt = Gam[t];
+      for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
+        float r[16];
+        tmem_ld16(tl + T_GH + c0, r);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int s = c0 + e;
+          r[e] = s <= t ? expf(Gt - Gam[s]) * r[e] : 0.f;
+        }
+        tmem_st16(tl + T_GH + c0, r);
       }
     }
     __syncthreads();
@@ -478,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ----------------------------- phase 5: (W S)^T, (Q S)^T = S^T [W^T | Q^T]
     if (tid == 0) {
-      gemm<kLo>(tmem + T_D1, opST, opWT, 128, kC, kD / 16, false);
+      gemm<kLo>(tmem + T_U, opST, opWT, 128, kC, kD / 16, true, true);
       gemm<kLo>(tmem + T_QS, opST, opQb, 128, kC, kD / 16, false);
       commit(bar0 + 16);
     }
@@ -487,11 +551,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- phase 6: Delta^T = U^T - (W S)^T, Delta^T diag(w); P; S^T *= gamma_63
     for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
-      float u[16], d[16];
-      tmem_ld16(tl + T_U + c0, u);
-      tmem_ld16(tl + T_D1 + c0, d);
-#pragma unroll
-      for (int e = 0; e < 16; ++e) u[e] -= d[e];
+      float u[16];
+      tmem_ld16(tl + T_U + c0, u);  // Delta^T = U^T - (W S)^T
       put8<kLo>(gb, OFF_DT, 128, kC, myrow, c0, u);
       put8<kLo>(gb, OFF_DT, 128, kC, myrow, c0 + 8, u + 8);
 #pragma unroll
@@ -499,17 +560,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       put8<kLo>(gb, OFF_DTW, 128, kC, myrow, c0, u);
       put8<kLo>(gb, OFF_DTW, 128, kC, myrow, c0 + 8, u + 8);
     }
-    if (quad >= 2) {  // lanes 64-127 hold H rows t
+    if (quad >= 2) {  // lanes 64-127 hold P rows t (built in phase 2)
       const int t = myrow - kC;
-      const float Gt = Gam[t];
       for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
         float r[16];
         tmem_ld16(tl + T_GH + c0, r);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int s = c0 + e;
-          r[e] = s <= t ? expf(Gt - Gam[s]) * r[e] : 0.f;
-        }
         put8<kLo>(gb, OFF_P, kC, kC, t, c0, r);
         put8<kLo>(gb, OFF_P, kC, kC, t, c0 + 8, r + 8);
       }
@@ -537,22 +592,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!__syncthreads_and(mbar_wait(bar0 + 24, parity, kWaitLimit))) { failed = true; break; }
     fence_after_sync();
 
-    // --------------------------- phase 8: o = diag(gamma) Q S + P Delta
-    for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
-      float r[16], pd[16];
-      tmem_ld16(tl + T_QS + c0, r);
-      tmem_ld16(tl + T_PD + c0, pd);
-#pragma unroll
-      for (int jj = 0; jj < 16; ++jj) {
-        const int t = c0 + jj;
-        if (t < n) o[(v_base + (size_t)t * vh) * kD + myrow] = fmaf(gam[t], r[jj], pd[jj]);
-      }
-    }
     cta_sync_tc();
     parity ^= 1u;
   }
 
   if (!failed) {
+    emit_o(nchunks - 1);
     float *Sh = S + head_off;
     for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
       float r[16];
