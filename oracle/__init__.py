@@ -12,6 +12,9 @@ Contents
              ``build()`` into _build/libgdn_oracle.so.
   ref64.py   fp64 restatements: matrix form, explicit closed form of the
              linear recurrence, and the chunk-parallel form.
+  gdn_ref.c also holds the layer core around the recurrence (conv1d + SiLU
+             with rolling history, q/k normalisation, gate computation),
+             ``run_layer``.
 
 Pins (each checked by tests that do not use the oracle's own code):
   run_f32     pinned by closed forms (alpha = 1 & beta = 0 identity, beta = 1
@@ -21,6 +24,10 @@ Pins (each checked by tests that do not use the oracle's own code):
   ref64.*     the matrix form and the closed form are pinned against each
               other and against the same closed-form special cases; the
               chunked form is pinned against the closed form.
+  run_layer   pinned by closed forms of each step (identity convolution,
+              SiLU/softplus/sigmoid values, unit norms, the +-20 softplus
+              branches, history shift) and by equality with run_f32 when the
+              layer steps are bypassed by construction.
 """
 
 from __future__ import annotations
@@ -70,6 +77,8 @@ def _load():
         lib.gdn_oracle_run.argtypes = [ctypes.c_int] * 6 + [fp] * 8
         lib.gdn_oracle_run.restype = ctypes.c_int
         lib.gdn_oracle_threads.restype = ctypes.c_int
+        lib.gdn_oracle_layer.argtypes = [ctypes.c_int] * 7 + [ctypes.c_float] + [fp] * 10
+        lib.gdn_oracle_layer.restype = ctypes.c_int
         lib.gdn_oracle_set_threads.argtypes = [ctypes.c_int]
         _lib = lib
     return _lib
@@ -116,6 +125,31 @@ def run_f32(S, q, k, v, g, beta, ckpt: bool = False):
     if rc != 0:
         raise RuntimeError(f"gdn_oracle_run failed ({rc})")
     return (S, o, ck) if ckpt else (S, o)
+
+
+def run_layer(S, hist, x, conv_w, a, b, A_log, dt_bias, kh, eps=1e-6,
+              ckpt: bool = False):
+    """The layer core (conv1d + SiLU with history, q/k normalisation, gates,
+    recurrence) over T tokens.  Shapes: S [B][vh][kd][vd], hist
+    [B][ck-1][conv_dim], x [B][T][conv_dim], conv_w [conv_dim][ck], a, b
+    [B][T][vh], A_log, dt_bias [vh].  Returns (S_T, hist_T, o[, ckpt])."""
+    lib = _load()
+    S = _f32c(S).copy()
+    hist = _f32c(hist).copy()
+    x, conv_w, a, b, A_log, dt_bias = map(_f32c, (x, conv_w, a, b, A_log, dt_bias))
+    B, vh, kd, vd = S.shape
+    T = x.shape[1]
+    ck = conv_w.shape[1]
+    if x.shape != (B, T, 2 * kh * kd + vh * vd) or hist.shape != (B, ck - 1, x.shape[2]):
+        raise ValueError("inconsistent layer shapes")
+    o = np.zeros((B, T, vh, vd), dtype=np.float32)
+    ck_ = np.zeros((T, B, vh, kd, vd), dtype=np.float32) if ckpt else None
+    rc = lib.gdn_oracle_layer(B, T, kh, vh, kd, vd, ck, float(eps), _ptr(S),
+                              _ptr(hist), _ptr(x), _ptr(conv_w), _ptr(a), _ptr(b),
+                              _ptr(A_log), _ptr(dt_bias), _ptr(o), _ptr(ck_))
+    if rc != 0:
+        raise RuntimeError(f"gdn_oracle_layer failed ({rc})")
+    return (S, hist, o, ck_) if ckpt else (S, hist, o)
 
 
 def run_inputs(inp, ckpt: bool = False):

@@ -138,3 +138,116 @@ void gdn_oracle_set_threads(int n) {
     (void)n;
 #endif
 }
+
+/* ------------------------------------------------------------------------
+ * The per-token layer steps around the recurrence ("Kestrel_VLLM - 24 · GDN
+ * linear attention to GPU", section 3, figure 1 steps 2-5):
+ *   conv:  for every channel ch of the mixed q|k|v projection (conv_dim =
+ *          2*kh*kd + vh*vd channels, q first, then k, then v), a depthwise
+ *          causal convolution of width ck over the last ck-1 inputs (the
+ *          history, oldest first) and the current input, then SiLU; the
+ *          history stores the convolution INPUTS and shifts by one per
+ *          token;
+ *   norm:  q and k scaled to unit L2 norm per key head, x / sqrt(sum x^2 +
+ *          eps) (the article names the step but prints no formula; this is
+ *          the plain reading, with eps a parameter);
+ *   gates: xa = a + dt_bias;  softplus = xa (xa > 20), exp(xa) (xa < -20),
+ *          log1p(exp(xa)) otherwise;  g = -exp(A_log) * softplus;
+ *          beta = 1 / (1 + exp(-b));
+ *   then the single-token update above with these q, k, v, g, beta.
+ * fp32, separately rounded, left-to-right sums.
+ */
+
+/* Advance the whole layer core over T tokens for every sequence.
+ *   S      [B][vh][kd][vd]       in/out
+ *   hist   [B][ck-1][conv_dim]   in/out (oldest row first)
+ *   x      [B][T][conv_dim]      raw mixed projections
+ *   conv_w [conv_dim][ck]
+ *   a, b   [B][T][vh];  A_log, dt_bias [vh]
+ *   o      [B][T][vh][vd]
+ *   ckpt   [T][B][vh][kd][vd] or NULL
+ * Returns 0, -1 on a bad shape, -2 when scratch cannot be allocated. */
+int gdn_oracle_layer(int B, int T, int kh, int vh, int kd, int vd, int ck,
+                     float eps, float *S, float *hist, const float *x,
+                     const float *conv_w, const float *a, const float *b,
+                     const float *A_log, const float *dt_bias, float *o,
+                     float *ckpt) {
+    if (B < 0 || T < 0 || kh <= 0 || vh <= 0 || kd <= 0 || vd <= 0 ||
+        ck < 1 || vh % kh)
+        return -1;
+    const int conv_dim = 2 * kh * kd + vh * vd;
+    const int nprev = ck - 1;
+    const size_t hsz = (size_t)kd * (size_t)vd;
+    float *xc = (float *)malloc(sizeof(float) * (size_t)conv_dim);
+    float *qn = (float *)malloc(sizeof(float) * (size_t)kh * kd);
+    float *kn = (float *)malloc(sizeof(float) * (size_t)kh * kd);
+    float *gg = (float *)malloc(sizeof(float) * (size_t)vh);
+    float *bb = (float *)malloc(sizeof(float) * (size_t)vh);
+    float *ot = (float *)malloc(sizeof(float) * (size_t)vh * vd);
+    if (!xc || !qn || !kn || !gg || !bb || !ot) {
+        free(xc); free(qn); free(kn); free(gg); free(bb); free(ot);
+        return -2;
+    }
+    int rc = 0;
+    for (int bi = 0; bi < B && rc == 0; bi++) {
+        float *hb = hist + (size_t)bi * (size_t)nprev * (size_t)conv_dim;
+        for (int t = 0; t < T && rc == 0; t++) {
+            const float *xr = x + ((size_t)bi * T + t) * (size_t)conv_dim;
+            /* conv + SiLU, history advanced per channel (read, then shift) */
+            for (int ch = 0; ch < conv_dim; ch++) {
+                const float *cw = conv_w + (size_t)ch * (size_t)ck;
+                const float raw = xr[ch];
+                float acc = 0.0f;
+                for (int j = 0; j < nprev; j++) {
+                    const float p = cw[j] * hb[(size_t)j * conv_dim + ch];
+                    acc = acc + p;
+                }
+                const float p = cw[nprev] * raw;
+                acc = acc + p;
+                for (int j = 0; j + 1 < nprev; j++)
+                    hb[(size_t)j * conv_dim + ch] = hb[(size_t)(j + 1) * conv_dim + ch];
+                if (nprev > 0) hb[(size_t)(nprev - 1) * conv_dim + ch] = raw;
+                xc[ch] = acc / (1.0f + expf(-acc));
+            }
+            /* q, k normalised per key head */
+            for (int h = 0; h < kh; h++) {
+                const float *qs = xc + (size_t)h * kd;
+                const float *ks = xc + (size_t)kh * kd + (size_t)h * kd;
+                float sq = 0.0f, sk = 0.0f;
+                for (int d = 0; d < kd; d++) {
+                    const float pq = qs[d] * qs[d];
+                    sq = sq + pq;
+                    const float pk = ks[d] * ks[d];
+                    sk = sk + pk;
+                }
+                const float nq = sqrtf(sq + eps), nk = sqrtf(sk + eps);
+                for (int d = 0; d < kd; d++) {
+                    qn[(size_t)h * kd + d] = qs[d] / nq;
+                    kn[(size_t)h * kd + d] = ks[d] / nk;
+                }
+            }
+            /* gates */
+            for (int h = 0; h < vh; h++) {
+                const size_t gi = ((size_t)bi * T + t) * vh + h;
+                const float xa = a[gi] + dt_bias[h];
+                float sp;
+                if (xa > 20.0f) sp = xa;
+                else if (xa < -20.0f) sp = expf(xa);
+                else sp = log1pf(expf(xa));
+                gg[h] = -expf(A_log[h]) * sp;
+                bb[h] = 1.0f / (1.0f + expf(-b[gi]));
+            }
+            /* the recurrence, one token, this sequence */
+            const float *vs = xc + (size_t)2 * kh * kd;
+            rc = gdn_oracle_run(1, 1, kh, vh, kd, vd, S + (size_t)bi * vh * hsz,
+                                qn, kn, vs, gg, bb, ot, NULL);
+            for (size_t e = 0; e < (size_t)vh * vd; e++)
+                o[((size_t)bi * T + t) * (size_t)vh * vd + e] = ot[e];
+            if (ckpt)
+                memcpy(ckpt + ((size_t)t * B + bi) * vh * hsz,
+                       S + (size_t)bi * vh * hsz, sizeof(float) * vh * hsz);
+        }
+    }
+    free(xc); free(qn); free(kn); free(gg); free(bb); free(ot);
+    return rc;
+}

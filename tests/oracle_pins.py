@@ -152,3 +152,127 @@ def pin_alpha_value(run):
 
 ALL_PINS = [pin_golden_tiny, pin_identity, pin_beta1_readback, pin_zero_state,
             pin_alpha0, pin_closed_form, pin_alpha_value]
+
+
+# ------------------------------------------------------------ layer core
+#
+# The layer core around the recurrence ("24 · GDN linear attention to GPU",
+# section 3 and figure 1 steps 2-5): depthwise causal conv1d + SiLU over the
+# mixed q|k|v projection with a history of the last ck-1 inputs (oldest
+# first), q/k scaled to unit L2 norm per key head, and the gates
+# beta = sigmoid(b), g = -exp(A_log) * softplus(a + dt_bias).  Each pin
+# below recomputes one of those steps in fp64 NumPy from its closed form and
+# feeds the result to the already-pinned recurrence.
+
+
+def _layer_case(seed, B=2, T=6, kh=2, vh=4, kd=8, vd=6, ck=4):
+    r = _rng(seed)
+    conv_dim = 2 * kh * kd + vh * vd
+    S = (r.standard_normal((B, vh, kd, vd)) * 0.3).astype(np.float32)
+    hist = r.standard_normal((B, ck - 1, conv_dim)).astype(np.float32)
+    x = r.standard_normal((B, T, conv_dim)).astype(np.float32)
+    w = (r.standard_normal((conv_dim, ck)) * 0.5).astype(np.float32)
+    a = r.standard_normal((B, T, vh)).astype(np.float32)
+    b = r.standard_normal((B, T, vh)).astype(np.float32)
+    A_log = (r.standard_normal(vh) * 0.5).astype(np.float32)
+    dt = (r.standard_normal(vh) * 0.5).astype(np.float32)
+    return S, hist, x, w, a, b, A_log, dt, kh
+
+
+def _layer_inputs64(hist, x, w, a, b, A_log, dt, kh, kd, vh, vd, eps=1e-6):
+    """q, k, v, g, beta of every token from the closed forms (fp64)."""
+    hist, x, w = (np.asarray(t, np.float64) for t in (hist, x, w))
+    B, T, C = x.shape
+    ck = w.shape[1]
+    seq = np.concatenate([hist, x], axis=1)          # [B][ck-1+T][C]
+    conv = np.zeros((B, T, C))
+    for t in range(T):
+        window = seq[:, t:t + ck]                    # oldest first
+        conv[:, t] = np.einsum("bjc,cj->bc", window, w)
+    act = conv / (1.0 + np.exp(-conv))               # SiLU
+    q = act[:, :, :kh * kd].reshape(B, T, kh, kd)
+    k = act[:, :, kh * kd:2 * kh * kd].reshape(B, T, kh, kd)
+    v = act[:, :, 2 * kh * kd:].reshape(B, T, vh, vd)
+    q = q / np.sqrt(np.sum(q * q, -1, keepdims=True) + eps)
+    k = k / np.sqrt(np.sum(k * k, -1, keepdims=True) + eps)
+    xa = np.asarray(a, np.float64) + np.asarray(dt, np.float64)
+    g = -np.exp(np.asarray(A_log, np.float64)) * np.logaddexp(0.0, xa)
+    beta = 1.0 / (1.0 + np.exp(-np.asarray(b, np.float64)))
+    return q, k, v, g, beta, seq[:, -(ck - 1):] if ck > 1 else seq[:, :0]
+
+
+def layer_pin_closed_forms(run_layer, run_f32):
+    """Conv (general kernel, history carried across tokens), SiLU, norm and
+    gates against their closed forms: the layer's o and S equal the pinned
+    recurrence fed with fp64-derived q, k, v, g, beta (to fp32 rounding),
+    and the final history is the last ck-1 inputs exactly."""
+    S, hist, x, w, a, b, A_log, dt, kh = _layer_case(31)
+    B, vh, kd, vd = S.shape
+    S1, h1, o1 = run_layer(S, hist, x, w, a, b, A_log, dt, kh)
+    q, k, v, g, beta, hist_ref = _layer_inputs64(hist, x, w, a, b, A_log, dt,
+                                                 kh, kd, vh, vd)
+    S2, o2 = run_f32(S, q, k, v, g, beta)
+    assert ref64.max_rel(o1, o2, axes=(-2, -1)) < 2e-5
+    assert ref64.max_rel(S1, S2, axes=(-2, -1)) < 2e-5
+    assert np.array_equal(h1, hist_ref.astype(np.float32))
+
+
+def layer_pin_identity_conv(run_layer, run_f32):
+    """conv_w = (0, ..., 0, 1) makes the convolution the identity: q, k, v
+    are SiLU of the raw input, unit-normalised for q and k."""
+    S, hist, x, w, a, b, A_log, dt, kh = _layer_case(32)
+    w[:] = 0
+    w[:, -1] = 1
+    B, vh, kd, vd = S.shape
+    _, _, o1 = run_layer(S, hist, x, w, a, b, A_log, dt, kh)
+    x64 = x.astype(np.float64)
+    act = x64 / (1 + np.exp(-x64))
+    q = act[:, :, :kh * kd].reshape(B, -1, kh, kd)
+    k = act[:, :, kh * kd:2 * kh * kd].reshape(B, -1, kh, kd)
+    v = act[:, :, 2 * kh * kd:].reshape(B, -1, vh, vd)
+    q = q / np.linalg.norm(q, axis=-1, keepdims=True)
+    k = k / np.linalg.norm(k, axis=-1, keepdims=True)
+    g = -np.exp(A_log.astype(np.float64)) * np.logaddexp(0, a.astype(np.float64) + dt)
+    beta = 1 / (1 + np.exp(-b.astype(np.float64)))
+    _, o2 = run_f32(S, q, k, v, g, beta)
+    assert ref64.max_rel(o1, o2, axes=(-2, -1)) < 2e-5
+
+
+def layer_pin_softplus_branches(run_layer, run_f32):
+    """a + dt_bias beyond +-20 selects the linear and exponential branches:
+    g = -exp(A_log) * xa and -exp(A_log) * exp(xa) respectively."""
+    S, hist, x, w, a, b, A_log, dt, kh = _layer_case(33, T=2)
+    a[:, 0] = 25.0 - dt      # xa = 25
+    a[:, 1] = -25.0 - dt     # xa = -25
+    A_log[:] = np.float32(np.log(0.01))   # keep g = -0.25 visible in alpha
+    B, vh, kd, vd = S.shape
+    S1, _, o1 = run_layer(S, hist, x, w, a, b, A_log, dt, kh)
+    q, k, v, _, beta, _ = _layer_inputs64(hist, x, w, a, b, A_log, dt, kh,
+                                          kd, vh, vd)
+    g = np.empty((B, 2, vh))
+    g[:, 0] = -np.exp(A_log.astype(np.float64)) * 25.0
+    g[:, 1] = -np.exp(A_log.astype(np.float64)) * np.exp(-25.0)
+    S2, o2 = run_f32(S, q, k, v, g, beta)
+    assert ref64.max_rel(S1, S2, axes=(-2, -1)) < 2e-5
+    assert ref64.max_rel(o1, o2, axes=(-2, -1)) < 2e-5
+
+
+def layer_pin_gate_values(run_layer, run_f32):
+    """a = -dt_bias, b = 0, A_log = 0: softplus(0) = ln 2 and sigmoid(0) =
+    1/2, so g = -ln 2 (alpha = 1/2) and beta = 1/2 for every head."""
+    S, hist, x, w, a, b, A_log, dt, kh = _layer_case(34, T=3)
+    a[:] = -dt
+    b[:] = 0
+    A_log[:] = 0
+    B, vh, kd, vd = S.shape
+    S1, _, o1 = run_layer(S, hist, x, w, a, b, A_log, dt, kh)
+    q, k, v, _, _, _ = _layer_inputs64(hist, x, w, a, b, A_log, dt, kh, kd,
+                                       vh, vd)
+    g = np.full((B, 3, vh), -np.log(2.0))
+    beta = np.full((B, 3, vh), 0.5)
+    S2, o2 = run_f32(S, q, k, v, g, beta)
+    assert ref64.max_rel(S1, S2, axes=(-2, -1)) < 2e-5
+
+
+LAYER_PINS = [layer_pin_closed_forms, layer_pin_identity_conv,
+              layer_pin_softplus_branches, layer_pin_gate_values]
