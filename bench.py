@@ -465,6 +465,33 @@ def main():
                     "bytes_per_launch": nb}
         del Sv, ck
         torch.cuda.empty_cache()
+        # the fused layer core (conv1d + SiLU + q/k norm + gates + update)
+        L = gdn_inputs.make_layer_inputs(gdn_inputs.SEED_BASE + 100, B=64, T=1)
+        SL = [tens(L.S) for _ in range(NSETS)]
+        hL = [tens(L.hist), tens(L.hist)]
+        lx, lw, la, lb = (tens(t) for t in (L.x, L.conv_w, L.a, L.b))
+        lA, ldt = tens(L.A_log), tens(L.dt_bias)
+        lo = torch.empty(64, 1, 48, D, device=dev)
+
+        def lstep(i):
+            s_ = SL[i % NSETS]
+            gdn.gdn_layer_step_m(s_, s_, None, hL[i % 2], hL[(i + 1) % 2], lx,
+                                 lw, la, lb, lA, ldt, lo, L.kh, stream=stream)
+        for i in range(5):
+            lstep(i)
+        n = max(20, min(200, args.steps))
+        lms = time_launches(torch, lstep, n, stream)
+        conv_dim = 2 * 16 * D + 48 * D
+        lbytes = decode_bytes(64, 16, 48) + 64 * 4 * (conv_dim + 6 * conv_dim)
+        parts["layer_decode_b64"] = {
+            "ms": lms, "head_steps_per_s": 64 * 48 / (lms * 1e-3),
+            "gbs": lbytes / (lms * 1e-3) / 1e9,
+            "frac_of_measured_hbm": lbytes / (lms * 1e-3) / 1e9 / hbm_peak,
+            "bytes_per_launch": lbytes,
+            "note": "raw projections in: conv1d+SiLU with history, q/k norm "
+                    "and gates fused into the update"}
+        del SL, hL
+        torch.cuda.empty_cache()
         prefill_parts(torch, gdn, tens, stream, peaks, parts)
 
     sampler.stop()

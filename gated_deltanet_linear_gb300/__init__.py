@@ -26,7 +26,7 @@ __all__ = [
     "gdn_rollback_seq", "gdn_prefill_workspace", "gdn_prefill",
     "gdn_strerror", "gdn_version", "library_path", "load",
     "GDN_PREC_FP32", "GDN_PREC_BF16X3", "GDN_PREC_BF16", "GDN_MAX_TOKENS",
-    "gdn_prefill_timeouts",
+    "gdn_prefill_timeouts", "gdn_layer_step_m", "gdn_layer_hist_rollback",
 ]
 
 GDN_OK, GDN_EINVAL, GDN_ESHAPE, GDN_EALIGN = 0, -1, -2, -3
@@ -37,7 +37,8 @@ GDN_MAX_TOKENS = 1 << 20
 # Every symbol include/gdn.h declares.
 EXPORTS = ("gdn_step", "gdn_step_m", "gdn_mark", "gdn_rollback",
            "gdn_rollback_seq", "gdn_prefill_workspace", "gdn_prefill",
-           "gdn_prefill_timeouts", "gdn_strerror", "gdn_version")
+           "gdn_prefill_timeouts", "gdn_layer_step_m",
+           "gdn_layer_hist_rollback", "gdn_strerror", "gdn_version")
 
 
 class GDNError(RuntimeError):
@@ -84,6 +85,10 @@ def load():
         f.restype = ctypes.c_int
     lib.gdn_prefill_workspace.argtypes = [cp, ip, ip, ip]
     lib.gdn_prefill_workspace.restype = ctypes.c_size_t
+    lib.gdn_layer_step_m.argtypes = [cp, ip, ip, ctypes.c_float] + [vp] * 13
+    lib.gdn_layer_step_m.restype = ctypes.c_int
+    lib.gdn_layer_hist_rollback.argtypes = [cp, ip, ip] + [vp] * 6
+    lib.gdn_layer_hist_rollback.restype = ctypes.c_int
     lib.gdn_prefill_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint)]
     lib.gdn_prefill_timeouts.restype = ctypes.c_int
     lib.gdn_strerror.argtypes = [ctypes.c_int]
@@ -235,3 +240,46 @@ def gdn_prefill(S, q, k, v, g, beta, o, precision=GDN_PREC_FP32, chunk=64,
     _check(load().gdn_prefill(ctypes.byref(sh), T, *args, int(chunk),
                               int(precision), ws_ptr, ws_bytes,
                               _stream(stream)), "gdn_prefill")
+
+
+def gdn_layer_step_m(S_in, S_out, ckpt, hist_in, hist_out, x, conv_w, a, b,
+                     A_log, dt_bias, o, kh, eps=1e-6, stream=None):
+    """Layer core (conv1d + SiLU with history, q/k norm, gates) and the
+    recurrence over M = x.shape[1] tokens.  Shapes as in include/gdn.h."""
+    if S_in.dim() != 4:
+        raise ValueError("S must be [B][vh][kd][vd]")
+    B, vh, kd, vd = S_in.shape
+    sh = Shape(B, int(kh), vh, kd, vd)
+    M = int(x.shape[1])
+    ck = int(conv_w.shape[1])
+    conv_dim = 2 * int(kh) * kd + vh * vd
+    n = B * vh * kd * vd
+    args = (_t(S_in, "S_in", n), _t(S_out, "S_out", n),
+            _t(ckpt, "ckpt", M * n),
+            _t(hist_in, "hist_in", B * (ck - 1) * conv_dim),
+            _t(hist_out, "hist_out", B * (ck - 1) * conv_dim),
+            _t(x, "x", B * M * conv_dim), _t(conv_w, "conv_w", conv_dim * ck),
+            _t(a, "a", B * M * vh), _t(b, "b", B * M * vh),
+            _t(A_log, "A_log", vh), _t(dt_bias, "dt_bias", vh),
+            _t(o, "o", B * M * vh * vd))
+    _check(load().gdn_layer_step_m(ctypes.byref(sh), M, ck, float(eps), *args,
+                                   _stream(stream)), "gdn_layer_step_m")
+
+
+def gdn_layer_hist_rollback(hist, M, m_dev, hist_snap, x, kh, kd=128, vd=128,
+                            err_dev=None, stream=None):
+    """Conv history after m_dev[b] of the M tokens of a layer launch."""
+    B, ck1, conv_dim = hist.shape
+    vh = (conv_dim - 2 * int(kh) * kd) // vd
+    sh = Shape(B, int(kh), vh, kd, vd)
+    for t_, name, cnt in ((m_dev, "m_dev", B), (err_dev, "err_dev", 1)):
+        if t_ is not None and (not t_.is_cuda or t_.dtype != torch.int32 or
+                               not t_.is_contiguous() or t_.numel() != cnt):
+            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor "
+                             f"of {cnt} elements")
+    _check(load().gdn_layer_hist_rollback(
+        ctypes.byref(sh), int(M), ck1 + 1, m_dev.data_ptr(),
+        _t(hist_snap, "hist_snap", hist.numel()),
+        _t(x, "x", B * int(M) * conv_dim), _t(hist, "hist", hist.numel()),
+        None if err_dev is None else err_dev.data_ptr(), _stream(stream)),
+        "gdn_layer_hist_rollback")

@@ -235,6 +235,77 @@ int gdn_prefill_timeouts(unsigned int *count) {
   return status_of(gdn::prefill_timeouts(count));
 }
 
+int gdn_layer_step_m(const gdn_shape *s, int M, int ck, float eps,
+                     const float *S_in, float *S_out, float *ckpt,
+                     const float *hist_in, float *hist_out, const float *x,
+                     const float *conv_w, const float *a, const float *b,
+                     const float *A_log, const float *dt_bias, float *o,
+                     gdn_stream_t stream) {
+  int r = check_shape(s);
+  if (r) return r;
+  if (ck != 4) return GDN_ESHAPE;
+  if (M < 1 || M > GDN_MAX_TOKENS) return GDN_ERANGE;
+  if (!(eps >= 0.0f) || eps > 3.0e38f) return GDN_EINVAL;
+  if (s->B == 0) return GDN_OK;
+  const size_t conv_dim = (size_t)2 * s->kh * s->kd + (size_t)s->vh * s->vd;
+  const size_t sb = state_floats(s) * 4;
+  const size_t hb = (size_t)s->B * (ck - 1) * conv_dim * 4;
+  const size_t xb = (size_t)s->B * M * conv_dim * 4;
+  const size_t wb = conv_dim * ck * 4;
+  const size_t ab = (size_t)s->B * M * s->vh * 4;
+  const size_t pb = (size_t)s->vh * 4;
+  const size_t ob = (size_t)s->B * M * s->vh * s->vd * 4;
+  Buf in[] = {{S_in, sb}, {hist_in, hb}, {x, xb}, {conv_w, wb}, {a, ab},
+              {b, ab}, {A_log, pb}, {dt_bias, pb}};
+  Buf out[] = {{S_out, sb}, {hist_out, hb}, {o, ob}, {ckpt, sb * (size_t)M}};
+  const int nin = 8, nout = ckpt ? 4 : 3;
+  r = check_bufs(in, nin);
+  if (r) return r;
+  r = check_bufs(out, nout);
+  if (r) return r;
+  for (int i = 0; i < nout; ++i) {
+    for (int j = 0; j < nin; ++j) {
+      if (i == 0 && j == 0 && out[0].p == in[0].p) continue;
+      if (overlaps(out[i], in[j])) return GDN_EALIAS;
+    }
+    for (int j = i + 1; j < nout; ++j)
+      if (overlaps(out[i], out[j])) return GDN_EALIAS;
+  }
+  cudaGetLastError();
+  return status_of(gdn::launch_layer_steps(S_in, S_out, ckpt, hist_in, hist_out,
+                                           x, conv_w, a, b, A_log, dt_bias, eps,
+                                           o, s->B, s->kh, s->vh, M,
+                                           (cudaStream_t)stream));
+}
+
+int gdn_layer_hist_rollback(const gdn_shape *s, int M, int ck,
+                            const int *m_dev, const float *hist_snap,
+                            const float *x, float *hist, int *err_dev,
+                            gdn_stream_t stream) {
+  int r = check_shape(s);
+  if (r) return r;
+  if (ck != 4) return GDN_ESHAPE;
+  if (M < 1 || M > GDN_MAX_TOKENS) return GDN_ERANGE;
+  if (s->B == 0) return GDN_OK;
+  const size_t conv_dim = (size_t)2 * s->kh * s->kd + (size_t)s->vh * s->vd;
+  const size_t hb = (size_t)s->B * (ck - 1) * conv_dim * 4;
+  Buf b[] = {{hist_snap, hb}, {x, (size_t)s->B * M * conv_dim * 4}, {hist, hb},
+             {m_dev, (size_t)s->B * 4}};
+  r = check_bufs(b, 4);
+  if (r) return r;
+  if (err_dev) {
+    if (((uintptr_t)err_dev & 3u) != 0) return GDN_EALIGN;
+    r = check_device_ptr(err_dev);
+    if (r) return r;
+  }
+  for (int j = 0; j < 4; ++j)
+    if (j != 2 && overlaps(b[2], b[j])) return GDN_EALIAS;
+  cudaGetLastError();
+  return status_of(gdn::launch_hist_rollback(hist, hist_snap, x, m_dev, err_dev,
+                                             s->B, M, (int)conv_dim,
+                                             (cudaStream_t)stream));
+}
+
 const char *gdn_strerror(int status) {
   switch (status) {
     case GDN_OK: return "success";

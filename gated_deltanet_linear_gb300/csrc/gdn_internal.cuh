@@ -17,6 +17,23 @@ cudaError_t launch_steps(const float *S_in, float *S_out, float *ckpt,
                          const float *g, const float *beta, float *o, int B,
                          int kh, int vh, int M, cudaStream_t stream);
 
+// The same kernel with the layer core (conv1d + SiLU with a width-4
+// history, q/k normalisation, gates) computing its token inputs from raw
+// projections.  hist_in and hist_out must not overlap.
+cudaError_t launch_layer_steps(const float *S_in, float *S_out, float *ckpt,
+                               const float *hist_in, float *hist_out,
+                               const float *x, const float *conv_w,
+                               const float *a, const float *b,
+                               const float *A_log, const float *dt_bias,
+                               float eps, float *o, int B, int kh, int vh,
+                               int M, cudaStream_t stream);
+
+// Per-sequence conv-history rollback (see gdn_layer_hist_rollback).
+cudaError_t launch_hist_rollback(float *hist, const float *hist_snap,
+                                 const float *x, const int *m_dev, int *err_dev,
+                                 int B, int M, int conv_dim,
+                                 cudaStream_t stream);
+
 // dst[i] = src[i] for n floats (n % 4 == 0, both 16-byte aligned).
 cudaError_t launch_copy(float *dst, const float *src, size_t n,
                         cudaStream_t stream);

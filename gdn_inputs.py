@@ -143,3 +143,43 @@ def make_workload(name: str, **overrides) -> GDNInputs:
     kw = dict(WORKLOADS[name])
     kw.update(overrides)
     return make_inputs(WORKLOAD_SEED[name], **kw)
+
+
+@dataclasses.dataclass
+class LayerInputs:
+    S: np.ndarray        # [B][vh][kd][vd]
+    hist: np.ndarray     # [B][ck-1][conv_dim]
+    x: np.ndarray        # [B][T][conv_dim]
+    conv_w: np.ndarray   # [conv_dim][ck]
+    a: np.ndarray        # [B][T][vh]
+    b: np.ndarray        # [B][T][vh]
+    A_log: np.ndarray    # [vh]
+    dt_bias: np.ndarray  # [vh]
+    kh: int
+    T: int
+
+
+def make_layer_inputs(seed: int, B: int, T: int, kh: int = 16, vh: int = 48,
+                      kd: int = 128, vd: int = 128, ck: int = 4,
+                      s_std: float = 0.02) -> LayerInputs:
+    """Raw inputs of the layer core (before convolution, normalisation and
+    gates), drawn in this order from one PCG64 generator:
+      S ~ N(0, s_std^2); hist, x ~ N(0, 1) (raw projections);
+      conv_w ~ N(0, 1/ck) (unit-variance convolution outputs);
+      a, b ~ N(0, 1);
+      A_log = log(U(1, 16)) per head and dt_bias = softplus^-1(dt) with
+      dt = exp(U(log 1e-3, log 1e-1)) per head, a common initialisation of
+      such gates (no trained weights are available)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    conv_dim = 2 * kh * kd + vh * vd
+    S = (rng.standard_normal((B, vh, kd, vd)) * s_std).astype(np.float32)
+    hist = rng.standard_normal((B, ck - 1, conv_dim)).astype(np.float32)
+    x = rng.standard_normal((B, T, conv_dim)).astype(np.float32)
+    conv_w = (rng.standard_normal((conv_dim, ck)) / np.sqrt(ck)).astype(np.float32)
+    a = rng.standard_normal((B, T, vh)).astype(np.float32)
+    b = rng.standard_normal((B, T, vh)).astype(np.float32)
+    A_log = np.log(rng.uniform(1.0, 16.0, vh)).astype(np.float32)
+    dt = np.exp(rng.uniform(np.log(1e-3), np.log(1e-1), vh))
+    dt_bias = (dt + np.log(-np.expm1(-dt))).astype(np.float32)
+    return LayerInputs(S=S, hist=hist, x=x, conv_w=conv_w, a=a, b=b,
+                       A_log=A_log, dt_bias=dt_bias, kh=kh, T=T)

@@ -193,6 +193,54 @@ int gdn_prefill(const gdn_shape *shape, int T, float *S, const float *q,
  */
 int gdn_prefill_timeouts(unsigned int *count);
 
+/*
+ * gdn_layer_step_m - the per-token layer core around the recurrence, fused
+ * into the M-token kernel: for every token, a depthwise causal convolution
+ * of width ck over the raw mixed q|k|v projection with a rolling history of
+ * the previous ck-1 inputs (oldest first), SiLU, q and k divided by
+ * sqrt(sum of squares + eps) per key head, the gates
+ *     beta = 1 / (1 + exp(-b)),
+ *     g    = -exp(A_log) * softplus(a + dt_bias)
+ *            (softplus(x) = x above 20, exp(x) below -20,
+ *             log1p(exp(x)) otherwise),
+ * then the update above.  These are steps 2-5 of figure 1 of "24 · GDN
+ * linear attention to GPU" (conv + SiLU and gates listed in its section 3;
+ * the q/k normalisation formula is not printed there: x / sqrt(|x|^2 + eps)
+ * is this library's reading).
+ *   ck       must be 4 (GDN_ESHAPE otherwise); conv_dim = 2*kh*kd + vh*vd
+ *   S_in, S_out, ckpt, o     as gdn_step_m
+ *   hist_in  [B][ck-1][conv_dim]  in: the previous ck-1 raw inputs
+ *   hist_out [B][ck-1][conv_dim]  out: the last ck-1 raw inputs after
+ *            token M-1; must not overlap hist_in (use two buffers in turn)
+ *   x        [B][M][conv_dim]  raw projections, channels q (kh*kd), then k
+ *            (kh*kd), then v (vh*vd)
+ *   conv_w   [conv_dim][ck]
+ *   a, b     [B][M][vh];   A_log, dt_bias [vh]
+ *   eps      >= 0 (GDN_EINVAL otherwise)
+ * Output m and ckpt[m] are bit-identical to the m-th of M successive calls
+ * with M = 1 that pass the history forward.
+ */
+int gdn_layer_step_m(const gdn_shape *shape, int M, int ck, float eps,
+                     const float *S_in, float *S_out, float *ckpt,
+                     const float *hist_in, float *hist_out, const float *x,
+                     const float *conv_w, const float *a, const float *b,
+                     const float *A_log, const float *dt_bias, float *o,
+                     gdn_stream_t stream);
+
+/*
+ * gdn_layer_hist_rollback - the convolution history after m_dev[b] of the
+ * M tokens of a gdn_layer_step_m call, for every sequence b: rows
+ * m .. m+ck-2 of the sequence [hist_snap rows, x rows], where hist_snap is
+ * that call's hist_in and x its raw inputs (the history stores inputs, so
+ * no per-token copy is needed).  m_dev: device int [B]; a value outside
+ * 0..M leaves that sequence's hist untouched and sets *err_dev (may be
+ * NULL) to 1.  hist must not overlap hist_snap or x.  ck must be 4.
+ */
+int gdn_layer_hist_rollback(const gdn_shape *shape, int M, int ck,
+                            const int *m_dev, const float *hist_snap,
+                            const float *x, float *hist, int *err_dev,
+                            gdn_stream_t stream);
+
 /* Static description of a status code (never NULL). */
 const char *gdn_strerror(int status);
 
