@@ -473,10 +473,14 @@ def main():
         lA, ldt = tens(L.A_log), tens(L.dt_bias)
         lo = torch.empty(64, 1, 48, D, device=dev)
 
+        lws = torch.empty(gdn.gdn_layer_workspace(64, 16, 48, 1),
+                          dtype=torch.uint8, device=dev)
+
         def lstep(i):
             s_ = SL[i % NSETS]
             gdn.gdn_layer_step_m(s_, s_, None, hL[i % 2], hL[(i + 1) % 2], lx,
-                                 lw, la, lb, lA, ldt, lo, L.kh, stream=stream)
+                                 lw, la, lb, lA, ldt, lo, L.kh, lws,
+                                 stream=stream)
         for i in range(5):
             lstep(i)
         n = max(20, min(200, args.steps))
@@ -488,8 +492,8 @@ def main():
             "gbs": lbytes / (lms * 1e-3) / 1e9,
             "frac_of_measured_hbm": lbytes / (lms * 1e-3) / 1e9 / hbm_peak,
             "bytes_per_launch": lbytes,
-            "note": "raw projections in: conv1d+SiLU with history, q/k norm "
-                    "and gates fused into the update"}
+            "note": "raw projections in: layer prologue (conv1d+SiLU with "
+                    "history, q/k norm, gates) then the update, two launches"}
         del SL, hL
         torch.cuda.empty_cache()
         prefill_parts(torch, gdn, tens, stream, peaks, parts)

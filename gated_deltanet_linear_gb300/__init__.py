@@ -26,7 +26,8 @@ __all__ = [
     "gdn_rollback_seq", "gdn_prefill_workspace", "gdn_prefill",
     "gdn_strerror", "gdn_version", "library_path", "load",
     "GDN_PREC_FP32", "GDN_PREC_BF16X3", "GDN_PREC_BF16", "GDN_MAX_TOKENS",
-    "gdn_prefill_timeouts", "gdn_layer_step_m", "gdn_layer_hist_rollback",
+    "gdn_prefill_timeouts", "gdn_layer_prologue_m", "gdn_layer_workspace",
+    "gdn_layer_step_m", "gdn_layer_hist_rollback",
 ]
 
 GDN_OK, GDN_EINVAL, GDN_ESHAPE, GDN_EALIGN = 0, -1, -2, -3
@@ -37,7 +38,8 @@ GDN_MAX_TOKENS = 1 << 20
 # Every symbol include/gdn.h declares.
 EXPORTS = ("gdn_step", "gdn_step_m", "gdn_mark", "gdn_rollback",
            "gdn_rollback_seq", "gdn_prefill_workspace", "gdn_prefill",
-           "gdn_prefill_timeouts", "gdn_layer_step_m",
+           "gdn_prefill_timeouts", "gdn_layer_prologue_m",
+           "gdn_layer_workspace", "gdn_layer_step_m",
            "gdn_layer_hist_rollback", "gdn_strerror", "gdn_version")
 
 
@@ -85,7 +87,12 @@ def load():
         f.restype = ctypes.c_int
     lib.gdn_prefill_workspace.argtypes = [cp, ip, ip, ip]
     lib.gdn_prefill_workspace.restype = ctypes.c_size_t
-    lib.gdn_layer_step_m.argtypes = [cp, ip, ip, ctypes.c_float] + [vp] * 13
+    lib.gdn_layer_prologue_m.argtypes = [cp, ip, ip, ctypes.c_float] + [vp] * 14
+    lib.gdn_layer_prologue_m.restype = ctypes.c_int
+    lib.gdn_layer_workspace.argtypes = [cp, ip]
+    lib.gdn_layer_workspace.restype = ctypes.c_size_t
+    lib.gdn_layer_step_m.argtypes = [cp, ip, ip, ctypes.c_float] + [vp] * 13 + \
+        [ctypes.c_size_t, vp]
     lib.gdn_layer_step_m.restype = ctypes.c_int
     lib.gdn_layer_hist_rollback.argtypes = [cp, ip, ip] + [vp] * 6
     lib.gdn_layer_hist_rollback.restype = ctypes.c_int
@@ -242,10 +249,40 @@ def gdn_prefill(S, q, k, v, g, beta, o, precision=GDN_PREC_FP32, chunk=64,
                               _stream(stream)), "gdn_prefill")
 
 
+def _layer_shape(hist, x, kh, vh=None, kd=128, vd=128):
+    B, ck1, conv_dim = hist.shape
+    vh = (conv_dim - 2 * int(kh) * kd) // vd if vh is None else vh
+    return Shape(B, int(kh), vh, kd, vd), int(x.shape[1]), ck1 + 1, conv_dim
+
+
+def gdn_layer_prologue_m(hist_in, hist_out, x, conv_w, a, b, A_log, dt_bias,
+                         q, k, v, g, beta, kh, eps=1e-6, stream=None):
+    """conv1d + SiLU with history, q/k norm and gates for M = x.shape[1]
+    tokens, writing q, k, v, g, beta (the inputs of gdn_step_m)."""
+    sh, M, ck, conv_dim = _layer_shape(hist_in, x, kh)
+    B, vh = sh.B, sh.vh
+    nh = B * (ck - 1) * conv_dim
+    args = (_t(hist_in, "hist_in", nh), _t(hist_out, "hist_out", nh),
+            _t(x, "x", B * M * conv_dim), _t(conv_w, "conv_w", conv_dim * ck),
+            _t(a, "a", B * M * vh), _t(b, "b", B * M * vh),
+            _t(A_log, "A_log", vh), _t(dt_bias, "dt_bias", vh),
+            _t(q, "q", B * M * sh.kh * 128), _t(k, "k", B * M * sh.kh * 128),
+            _t(v, "v", B * M * vh * 128), _t(g, "g", B * M * vh),
+            _t(beta, "beta", B * M * vh))
+    _check(load().gdn_layer_prologue_m(ctypes.byref(sh), M, ck, float(eps),
+                                       *args, _stream(stream)),
+           "gdn_layer_prologue_m")
+
+
+def gdn_layer_workspace(B, kh, vh, M, kd=128, vd=128):
+    sh = Shape(B, kh, vh, kd, vd)
+    return int(load().gdn_layer_workspace(ctypes.byref(sh), int(M)))
+
+
 def gdn_layer_step_m(S_in, S_out, ckpt, hist_in, hist_out, x, conv_w, a, b,
-                     A_log, dt_bias, o, kh, eps=1e-6, stream=None):
-    """Layer core (conv1d + SiLU with history, q/k norm, gates) and the
-    recurrence over M = x.shape[1] tokens.  Shapes as in include/gdn.h."""
+                     A_log, dt_bias, o, kh, workspace, eps=1e-6, stream=None):
+    """Layer prologue + update over M = x.shape[1] tokens; the intermediate
+    q, k, v, g, beta live in `workspace` (gdn_layer_workspace bytes)."""
     if S_in.dim() != 4:
         raise ValueError("S must be [B][vh][kd][vd]")
     B, vh, kd, vd = S_in.shape
@@ -254,6 +291,8 @@ def gdn_layer_step_m(S_in, S_out, ckpt, hist_in, hist_out, x, conv_w, a, b,
     ck = int(conv_w.shape[1])
     conv_dim = 2 * int(kh) * kd + vh * vd
     n = B * vh * kd * vd
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
     args = (_t(S_in, "S_in", n), _t(S_out, "S_out", n),
             _t(ckpt, "ckpt", M * n),
             _t(hist_in, "hist_in", B * (ck - 1) * conv_dim),
@@ -262,8 +301,10 @@ def gdn_layer_step_m(S_in, S_out, ckpt, hist_in, hist_out, x, conv_w, a, b,
             _t(a, "a", B * M * vh), _t(b, "b", B * M * vh),
             _t(A_log, "A_log", vh), _t(dt_bias, "dt_bias", vh),
             _t(o, "o", B * M * vh * vd))
-    _check(load().gdn_layer_step_m(ctypes.byref(sh), M, ck, float(eps), *args,
-                                   _stream(stream)), "gdn_layer_step_m")
+    _check(load().gdn_layer_step_m(
+        ctypes.byref(sh), M, ck, float(eps), *args, workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream(stream)),
+        "gdn_layer_step_m")
 
 
 def gdn_layer_hist_rollback(hist, M, m_dev, hist_snap, x, kh, kd=128, vd=128,

@@ -78,10 +78,10 @@ size_t state_floats(const gdn_shape *s) {
 
 // Validate and launch M serial tokens (shared by gdn_step, gdn_step_m and
 // the fp32 prefill path).
-int steps_common(const gdn_shape *s, int M, const float *S_in, float *S_out,
-                 float *ckpt, const float *q, const float *k, const float *v,
-                 const float *g, const float *beta, float *o,
-                 cudaStream_t stream) {
+int steps_common_check(const gdn_shape *s, int M, const float *S_in,
+                       float *S_out, float *ckpt, const float *q,
+                       const float *k, const float *v, const float *g,
+                       const float *beta, float *o) {
   int r = check_shape(s);
   if (r) return r;
   if (M < 1 || M > GDN_MAX_TOKENS) return GDN_ERANGE;
@@ -107,6 +107,15 @@ int steps_common(const gdn_shape *s, int M, const float *S_in, float *S_out,
     for (int j = i + 1; j < nout; ++j)
       if (overlaps(out[i], out[j])) return GDN_EALIAS;
   }
+  return GDN_OK;
+}
+
+int steps_common(const gdn_shape *s, int M, const float *S_in, float *S_out,
+                 float *ckpt, const float *q, const float *k, const float *v,
+                 const float *g, const float *beta, float *o,
+                 cudaStream_t stream) {
+  const int r = steps_common_check(s, M, S_in, S_out, ckpt, q, k, v, g, beta, o);
+  if (r || s->B == 0) return r;
   cudaGetLastError();  // start from a clean per-thread error state
   return status_of(gdn::launch_steps(S_in, S_out, ckpt, q, k, v, g, beta, o,
                                      s->B, s->kh, s->vh, M, stream));
@@ -235,47 +244,131 @@ int gdn_prefill_timeouts(unsigned int *count) {
   return status_of(gdn::prefill_timeouts(count));
 }
 
-int gdn_layer_step_m(const gdn_shape *s, int M, int ck, float eps,
-                     const float *S_in, float *S_out, float *ckpt,
-                     const float *hist_in, float *hist_out, const float *x,
-                     const float *conv_w, const float *a, const float *b,
-                     const float *A_log, const float *dt_bias, float *o,
-                     gdn_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+size_t round16(size_t n) { return (n + 15) & ~(size_t)15; }
+
+struct LayerSizes {
+  size_t conv_dim, hb, xb, wb, ab, pb, qb, vb, gb;
+};
+
+LayerSizes layer_sizes(const gdn_shape *s, int M, int ck) {
+  LayerSizes z;
+  z.conv_dim = (size_t)2 * s->kh * s->kd + (size_t)s->vh * s->vd;
+  z.hb = (size_t)s->B * (ck - 1) * z.conv_dim * 4;
+  z.xb = (size_t)s->B * M * z.conv_dim * 4;
+  z.wb = z.conv_dim * ck * 4;
+  z.ab = (size_t)s->B * M * s->vh * 4;
+  z.pb = (size_t)s->vh * 4;
+  z.qb = (size_t)s->B * M * s->kh * s->kd * 4;
+  z.vb = (size_t)s->B * M * s->vh * s->vd * 4;
+  z.gb = z.ab;
+  return z;
+}
+
+// Validation shared by the two layer entry points; outputs q..beta may be
+// NULL (checked by the caller).
+int check_layer(const gdn_shape *s, int M, int ck, float eps,
+                const float *hist_in, float *hist_out, const float *x,
+                const float *conv_w, const float *a, const float *b,
+                const float *A_log, const float *dt_bias) {
   int r = check_shape(s);
   if (r) return r;
   if (ck != 4) return GDN_ESHAPE;
   if (M < 1 || M > GDN_MAX_TOKENS) return GDN_ERANGE;
   if (!(eps >= 0.0f) || eps > 3.0e38f) return GDN_EINVAL;
   if (s->B == 0) return GDN_OK;
-  const size_t conv_dim = (size_t)2 * s->kh * s->kd + (size_t)s->vh * s->vd;
-  const size_t sb = state_floats(s) * 4;
-  const size_t hb = (size_t)s->B * (ck - 1) * conv_dim * 4;
-  const size_t xb = (size_t)s->B * M * conv_dim * 4;
-  const size_t wb = conv_dim * ck * 4;
-  const size_t ab = (size_t)s->B * M * s->vh * 4;
-  const size_t pb = (size_t)s->vh * 4;
-  const size_t ob = (size_t)s->B * M * s->vh * s->vd * 4;
-  Buf in[] = {{S_in, sb}, {hist_in, hb}, {x, xb}, {conv_w, wb}, {a, ab},
-              {b, ab}, {A_log, pb}, {dt_bias, pb}};
-  Buf out[] = {{S_out, sb}, {hist_out, hb}, {o, ob}, {ckpt, sb * (size_t)M}};
-  const int nin = 8, nout = ckpt ? 4 : 3;
-  r = check_bufs(in, nin);
+  const LayerSizes z = layer_sizes(s, M, ck);
+  Buf in[] = {{hist_in, z.hb}, {x, z.xb}, {conv_w, z.wb}, {a, z.ab},
+              {b, z.ab}, {A_log, z.pb}, {dt_bias, z.pb}, {hist_out, z.hb}};
+  r = check_bufs(in, 8);
   if (r) return r;
-  r = check_bufs(out, nout);
+  for (int j = 0; j < 7; ++j)
+    if (overlaps(in[7], in[j])) return GDN_EALIAS;
+  return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdn_layer_prologue_m(const gdn_shape *s, int M, int ck, float eps,
+                         const float *hist_in, float *hist_out,
+                         const float *x, const float *conv_w, const float *a,
+                         const float *b, const float *A_log,
+                         const float *dt_bias, float *q, float *k, float *v,
+                         float *g, float *beta, gdn_stream_t stream) {
+  int r = check_layer(s, M, ck, eps, hist_in, hist_out, x, conv_w, a, b, A_log,
+                      dt_bias);
+  if (r || s->B == 0) return r;
+  const LayerSizes z = layer_sizes(s, M, ck);
+  Buf in[] = {{hist_in, z.hb}, {x, z.xb}, {conv_w, z.wb}, {a, z.ab},
+              {b, z.ab}, {A_log, z.pb}, {dt_bias, z.pb}, {hist_out, z.hb}};
+  Buf out[] = {{q, z.qb}, {k, z.qb}, {v, z.vb}, {g, z.gb}, {beta, z.gb}};
+  r = check_bufs(out, 5);
   if (r) return r;
-  for (int i = 0; i < nout; ++i) {
-    for (int j = 0; j < nin; ++j) {
-      if (i == 0 && j == 0 && out[0].p == in[0].p) continue;
+  for (int i = 0; i < 5; ++i) {
+    for (int j = 0; j < 8; ++j)
       if (overlaps(out[i], in[j])) return GDN_EALIAS;
-    }
-    for (int j = i + 1; j < nout; ++j)
+    for (int j = i + 1; j < 5; ++j)
       if (overlaps(out[i], out[j])) return GDN_EALIAS;
   }
   cudaGetLastError();
-  return status_of(gdn::launch_layer_steps(S_in, S_out, ckpt, hist_in, hist_out,
-                                           x, conv_w, a, b, A_log, dt_bias, eps,
-                                           o, s->B, s->kh, s->vh, M,
-                                           (cudaStream_t)stream));
+  return status_of(gdn::launch_layer_prologue(
+      hist_in, hist_out, x, conv_w, a, b, A_log, dt_bias, eps, q, k, v, g,
+      beta, s->B, s->kh, s->vh, M, (cudaStream_t)stream));
+}
+
+size_t gdn_layer_workspace(const gdn_shape *s, int M) {
+  if (check_shape(s) || M < 1 || M > GDN_MAX_TOKENS) return 0;
+  const LayerSizes z = layer_sizes(s, M, 4);
+  return round16(z.qb) * 2 + round16(z.vb) + round16(z.gb) * 2;
+}
+
+int gdn_layer_step_m(const gdn_shape *s, int M, int ck, float eps,
+                     const float *S_in, float *S_out, float *ckpt,
+                     const float *hist_in, float *hist_out, const float *x,
+                     const float *conv_w, const float *a, const float *b,
+                     const float *A_log, const float *dt_bias, float *o,
+                     void *workspace, size_t ws_bytes, gdn_stream_t stream) {
+  int r = check_layer(s, M, ck, eps, hist_in, hist_out, x, conv_w, a, b, A_log,
+                      dt_bias);
+  if (r || s->B == 0) return r;
+  const size_t need = gdn_layer_workspace(s, M);
+  if (ws_bytes < need) return GDN_ERANGE;
+  const LayerSizes z = layer_sizes(s, M, ck);
+  Buf ws{workspace, need};
+  r = check_bufs(&ws, 1);
+  if (r) return r;
+  // the workspace must not overlap any argument of either step
+  const size_t sb = state_floats(s) * 4;
+  Buf all[] = {{S_in, sb}, {S_out, sb}, {ckpt, sb * (size_t)M},
+               {hist_in, z.hb}, {hist_out, z.hb}, {x, z.xb}, {conv_w, z.wb},
+               {a, z.ab}, {b, z.ab}, {A_log, z.pb}, {dt_bias, z.pb},
+               {o, z.vb}};
+  for (int j = 0; j < 12; ++j)
+    if (overlaps(ws, all[j])) return GDN_EALIAS;
+  char *w = static_cast<char *>(workspace);
+  float *q = reinterpret_cast<float *>(w);
+  float *k = reinterpret_cast<float *>(w + round16(z.qb));
+  float *v = reinterpret_cast<float *>(w + 2 * round16(z.qb));
+  float *g = reinterpret_cast<float *>(w + 2 * round16(z.qb) + round16(z.vb));
+  float *beta = reinterpret_cast<float *>(w + 2 * round16(z.qb) + round16(z.vb) +
+                                          round16(z.gb));
+  // the state call validates its own arguments before anything is launched
+  const gdn_shape *sh = s;
+  r = steps_common_check(sh, M, S_in, S_out, ckpt, q, k, v, g, beta, o);
+  if (r) return r;
+  cudaGetLastError();
+  cudaError_t e = gdn::launch_layer_prologue(
+      hist_in, hist_out, x, conv_w, a, b, A_log, dt_bias, eps, q, k, v, g,
+      beta, s->B, s->kh, s->vh, M, (cudaStream_t)stream);
+  if (e != cudaSuccess) return GDN_ECUDA;
+  return status_of(gdn::launch_steps(S_in, S_out, ckpt, q, k, v, g, beta, o,
+                                     s->B, s->kh, s->vh, M,
+                                     (cudaStream_t)stream));
 }
 
 int gdn_layer_hist_rollback(const gdn_shape *s, int M, int ck,

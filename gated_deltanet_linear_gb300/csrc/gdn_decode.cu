@@ -233,145 +233,6 @@ __device__ __forceinline__ void token_update(float4 (&s)[8], const TokenIn &t,
   }
 }
 
-// ------------------------------------------------------------- layer core
-//
-// The per-token steps around the recurrence ("24 · GDN linear attention to
-// GPU", section 3, figure 1 steps 2-4), fused into the lane's token load:
-//   conv:  channel c of the mixed q|k|v projection (q channels first, then
-//          k, then v) is a width-4 causal convolution over the previous
-//          three inputs (the history, oldest first) and the current one,
-//          then SiLU;
-//   norm:  q and k divided by sqrt(sum of squares + eps) per key head;
-//   gates: beta = 1 / (1 + exp(-b)),
-//          g = -exp(A_log) softplus(a + dt_bias) with softplus(x) = x above
-//          20, exp(x) below -20, log1p(exp(x)) otherwise.
-// Each lane convolves the channels it needs (8 q rows, 8 k rows, 4 v
-// columns); lanes that share a key head repeat that small amount of work.
-
-constexpr int kConvK = 4;
-
-struct LayerArgs {
-  const float *x;        // [B][M][conv_dim] raw projections of this launch
-  const float *conv_w;   // [conv_dim][kConvK]
-  const float *hist_in;  // [B][kConvK-1][conv_dim], oldest row first
-  float *hist_out;       // [B][kConvK-1][conv_dim]
-  const float *a, *b;    // [B][M][vh]
-  const float *A_log, *dt_bias;  // [vh]
-  float eps;
-  int conv_dim;
-};
-
-// Row i of the window sequence [hist_in rows, x rows of this launch].
-__device__ __forceinline__ const float *seq_row(const LayerArgs &L, int b,
-                                                int M, int i) {
-  return i < kConvK - 1
-             ? L.hist_in + ((size_t)b * (kConvK - 1) + i) * L.conv_dim
-             : L.x + ((size_t)b * M + (i - (kConvK - 1))) * L.conv_dim;
-}
-
-// conv + SiLU of channels c .. c+3 for token m (window rows m .. m+3).
-__device__ __forceinline__ float4 conv4(const LayerArgs &L, int b, int M,
-                                        int m, int c) {
-  const float4 *w = reinterpret_cast<const float4 *>(L.conv_w + (size_t)c * kConvK);
-  const float4 wc[4] = {__ldg(w), __ldg(w + 1), __ldg(w + 2), __ldg(w + 3)};
-  float acc[4];
-#pragma unroll
-  for (int j = 0; j < kConvK; ++j) {
-    const float4 r = __ldg(reinterpret_cast<const float4 *>(seq_row(L, b, M, m + j) + c));
-    const float rv[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float we = comp(wc[e], j);
-      acc[e] = j == 0 ? __fmul_rn(we, rv[e]) : __fmaf_rn(we, rv[e], acc[e]);
-    }
-  }
-  float out[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) out[e] = __fdiv_rn(acc[e], __fadd_rn(1.0f, expf(-acc[e])));
-  return make_float4(out[0], out[1], out[2], out[3]);
-}
-
-// Sum over the 128 rows of a key-head vector held 8 per lane (lanes 2p + h,
-// both halves hold every row).
-__device__ __forceinline__ float rows_sum(float x) {
-  x = __fadd_rn(x, __shfl_xor_sync(kFull, x, 16));
-  x = __fadd_rn(x, __shfl_xor_sync(kFull, x, 8));
-  x = __fadd_rn(x, __shfl_xor_sync(kFull, x, 4));
-  x = __fadd_rn(x, __shfl_xor_sync(kFull, x, 2));
-  return x;
-}
-
-__device__ __forceinline__ void unit_norm(float4 &x0, float4 &x1, float eps) {
-  float ss = __fmul_rn(x0.x, x0.x);
-  ss = __fmaf_rn(x0.y, x0.y, ss);
-  ss = __fmaf_rn(x0.z, x0.z, ss);
-  ss = __fmaf_rn(x0.w, x0.w, ss);
-  ss = __fmaf_rn(x1.x, x1.x, ss);
-  ss = __fmaf_rn(x1.y, x1.y, ss);
-  ss = __fmaf_rn(x1.z, x1.z, ss);
-  ss = __fmaf_rn(x1.w, x1.w, ss);
-  const float n = __fsqrt_rn(__fadd_rn(rows_sum(ss), eps));
-  x0 = make_float4(__fdiv_rn(x0.x, n), __fdiv_rn(x0.y, n), __fdiv_rn(x0.z, n), __fdiv_rn(x0.w, n));
-  x1 = make_float4(__fdiv_rn(x1.x, n), __fdiv_rn(x1.y, n), __fdiv_rn(x1.z, n), __fdiv_rn(x1.w, n));
-}
-
-// Token inputs of the lane from the raw layer inputs.
-__device__ __forceinline__ TokenIn layer_token(const LayerArgs &L, int b,
-                                               int vi, int hh, int cg, int kh,
-                                               int vh, int M, int m, int p,
-                                               int h) {
-  TokenIn t;
-  const int cq = hh * kDim + 8 * p;
-  const int ck = kh * kDim + hh * kDim + 8 * p;
-  const int cv = 2 * kh * kDim + vi * kDim + 8 * cg + 4 * h;
-  t.q0 = conv4(L, b, M, m, cq);
-  t.q1 = conv4(L, b, M, m, cq + 4);
-  t.k0 = conv4(L, b, M, m, ck);
-  t.k1 = conv4(L, b, M, m, ck + 4);
-  t.v = conv4(L, b, M, m, cv);
-  unit_norm(t.q0, t.q1, L.eps);
-  unit_norm(t.k0, t.k1, L.eps);
-  const size_t gi = ((size_t)b * M + m) * vh + vi;
-  const float xa = __fadd_rn(__ldg(L.a + gi), __ldg(L.dt_bias + vi));
-  float sp;
-  if (xa > 20.0f)
-    sp = xa;
-  else if (xa < -20.0f)
-    sp = expf(xa);
-  else
-    sp = log1pf(expf(xa));
-  t.g = __fmul_rn(-expf(__ldg(L.A_log + vi)), sp);
-  t.beta = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-__ldg(L.b + gi))));
-  return t;
-}
-
-// History after the launch: the last three rows of the window sequence.
-// q and k channels of a key head are written by the lanes h == 0 of the
-// unit with vi % rep == 0 and cg == 0; every lane writes its v channels.
-__device__ __forceinline__ void layer_history(const LayerArgs &L, int b,
-                                              int vi, int hh, int cg, int kh,
-                                              int rep, int M, int p, int h) {
-  const int cv = 2 * kh * kDim + vi * kDim + 8 * cg + 4 * h;
-  const bool qk_writer = (vi % rep == 0) && cg == 0 && h == 0;
-#pragma unroll
-  for (int j = 0; j < kConvK - 1; ++j) {
-    const float *src = seq_row(L, b, M, M + j);
-    float *dst = L.hist_out + ((size_t)b * (kConvK - 1) + j) * L.conv_dim;
-    *reinterpret_cast<float4 *>(dst + cv) = __ldg(reinterpret_cast<const float4 *>(src + cv));
-    if (qk_writer) {
-      const int cq = hh * kDim + 8 * p;
-      const int ck = kh * kDim + hh * kDim + 8 * p;
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        *reinterpret_cast<float4 *>(dst + cq + 4 * e) =
-            __ldg(reinterpret_cast<const float4 *>(src + cq + 4 * e));
-        *reinterpret_cast<float4 *>(dst + ck + 4 * e) =
-            __ldg(reinterpret_cast<const float4 *>(src + ck + 4 * e));
-      }
-    }
-  }
-}
-
 // Start the copy of unit u's 4 KB into the stage at smem address `stage`.
 __device__ __forceinline__ void issue_unit(const float *S_in, size_t u,
                                            uint32_t stage, int p, int h) {
@@ -384,15 +245,14 @@ __device__ __forceinline__ void issue_unit(const float *S_in, size_t u,
     cp_async16(stage + stage_off(p, h, j), src + j * kDim);
 }
 
-template <bool kCkpt, bool kLayer>
+template <bool kCkpt>
 __global__ void __launch_bounds__(kWarpsPerCta * 32, kCtasPerSm)
     gdn_steps_kernel(const float *S_in, float *S_out,
                      float *__restrict__ ckpt, const float *__restrict__ q,
                      const float *__restrict__ k, const float *__restrict__ v,
                      const float *__restrict__ g,
                      const float *__restrict__ beta, float *__restrict__ o,
-                     int vh, int kh, int rep, int M, size_t nheads,
-                     const LayerArgs L) {
+                     int vh, int kh, int rep, int M, size_t nheads) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -432,7 +292,6 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, kCtasPerSm)
     int b, vi, hh, cg;
     size_t head;
     unit_coords(i, b, vi, hh, cg, head);
-    if (kLayer) return layer_token(L, b, vi, hh, cg, kh, vh, M, m, p, h);
     const size_t bm = (size_t)b * M + m;
     return load_token(q, k, v, g, beta, (bm * kh + hh) * kDim + 8 * p,
                       (bm * vh + vi) * kDim + 8 * cg + 4 * h, bm * vh + vi);
@@ -479,7 +338,6 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, kCtasPerSm)
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j) st_stream(S_out + hoff + eoff + j * kDim, s[j]);
-    if (kLayer) layer_history(L, b, vi, hh, cg, kh, rep, M, p, h);
   }
   cp_async_wait<0>();
 }
@@ -512,32 +370,6 @@ __global__ void rollback_seq_kernel(float4 *__restrict__ S,
   for (size_t i = threadIdx.x; i < n4; i += blockDim.x) dst[i] = __ldg(src + i);
 }
 
-// One CTA per sequence: history after m_dev[b] tokens of a launch = rows
-// m .. m+2 of [hist_snap rows, x rows].
-__global__ void hist_rollback_kernel(float4 *__restrict__ hist,
-                                     const float *__restrict__ hist_snap,
-                                     const float *__restrict__ x,
-                                     const int *__restrict__ m_dev,
-                                     int *__restrict__ err, int M,
-                                     int conv_dim) {
-  const int b = blockIdx.x;
-  const int m = __ldg(m_dev + b);
-  if (m < 0 || m > M) {
-    if (err && threadIdx.x == 0) *err = 1;
-    return;
-  }
-  const int n4 = conv_dim / 4;
-  for (int j = 0; j < kConvK - 1; ++j) {
-    const int i = m + j;
-    const float *src = i < kConvK - 1
-                           ? hist_snap + ((size_t)b * (kConvK - 1) + i) * conv_dim
-                           : x + ((size_t)b * M + (i - (kConvK - 1))) * conv_dim;
-    float4 *dst = hist + ((size_t)b * (kConvK - 1) + j) * n4;
-    for (int c = threadIdx.x; c < n4; c += blockDim.x)
-      dst[c] = __ldg(reinterpret_cast<const float4 *>(src) + c);
-  }
-}
-
 int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -551,65 +383,34 @@ int sm_count() {
 
 }  // namespace
 
-template <bool kCkpt, bool kLayer>
-static cudaError_t launch_steps_t(const float *S_in, float *S_out, float *ckpt,
-                                  const float *q, const float *k,
-                                  const float *v, const float *g,
-                                  const float *beta, float *o, int B, int kh,
-                                  int vh, int M, const LayerArgs &L,
-                                  cudaStream_t stream) {
+cudaError_t launch_steps(const float *S_in, float *S_out, float *ckpt,
+                         const float *q, const float *k, const float *v,
+                         const float *g, const float *beta, float *o, int B,
+                         int kh, int vh, int M, cudaStream_t stream) {
   const size_t nheads = (size_t)B * vh;
   const size_t nunits = nheads * kUnitsPerHead;
   if (nunits == 0) return cudaSuccess;
   size_t ctas = (nunits + kWarpsPerCta - 1) / kWarpsPerCta;
   const size_t cap = (size_t)sm_count() * kCtasPerSm;
   if (ctas > cap) ctas = cap;
-  cudaError_t e = cudaFuncSetAttribute(
-      gdn_steps_kernel<kCkpt, kLayer>,
-      cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemPerCta);
-  if (e != cudaSuccess) return e;
-  gdn_steps_kernel<kCkpt, kLayer>
-      <<<(unsigned)ctas, kWarpsPerCta * 32, kSmemPerCta, stream>>>(
-          S_in, S_out, ckpt, q, k, v, g, beta, o, vh, kh, vh / kh, M, nheads,
-          L);
+  const dim3 grid((unsigned)ctas), block(kWarpsPerCta * 32);
+  cudaError_t e;
+  if (ckpt) {
+    e = cudaFuncSetAttribute(gdn_steps_kernel<true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemPerCta);
+    if (e != cudaSuccess) return e;
+    gdn_steps_kernel<true><<<grid, block, kSmemPerCta, stream>>>(
+        S_in, S_out, ckpt, q, k, v, g, beta, o, vh, kh, vh / kh, M, nheads);
+  } else {
+    e = cudaFuncSetAttribute(gdn_steps_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemPerCta);
+    if (e != cudaSuccess) return e;
+    gdn_steps_kernel<false><<<grid, block, kSmemPerCta, stream>>>(
+        S_in, S_out, nullptr, q, k, v, g, beta, o, vh, kh, vh / kh, M, nheads);
+  }
   return cudaGetLastError();
-}
-
-cudaError_t launch_steps(const float *S_in, float *S_out, float *ckpt,
-                         const float *q, const float *k, const float *v,
-                         const float *g, const float *beta, float *o, int B,
-                         int kh, int vh, int M, cudaStream_t stream) {
-  const LayerArgs none{};
-  return ckpt ? launch_steps_t<true, false>(S_in, S_out, ckpt, q, k, v, g, beta,
-                                            o, B, kh, vh, M, none, stream)
-              : launch_steps_t<false, false>(S_in, S_out, nullptr, q, k, v, g,
-                                             beta, o, B, kh, vh, M, none, stream);
-}
-
-cudaError_t launch_layer_steps(const float *S_in, float *S_out, float *ckpt,
-                               const float *hist_in, float *hist_out,
-                               const float *x, const float *conv_w,
-                               const float *a, const float *b,
-                               const float *A_log, const float *dt_bias,
-                               float eps, float *o, int B, int kh, int vh,
-                               int M, cudaStream_t stream) {
-  LayerArgs L;
-  L.x = x;
-  L.conv_w = conv_w;
-  L.hist_in = hist_in;
-  L.hist_out = hist_out;
-  L.a = a;
-  L.b = b;
-  L.A_log = A_log;
-  L.dt_bias = dt_bias;
-  L.eps = eps;
-  L.conv_dim = 2 * kh * kDim + vh * kDim;
-  return ckpt ? launch_steps_t<true, true>(S_in, S_out, ckpt, nullptr, nullptr,
-                                           nullptr, nullptr, nullptr, o, B, kh,
-                                           vh, M, L, stream)
-              : launch_steps_t<false, true>(S_in, S_out, nullptr, nullptr,
-                                            nullptr, nullptr, nullptr, nullptr,
-                                            o, B, kh, vh, M, L, stream);
 }
 
 cudaError_t launch_copy(float *dst, const float *src, size_t n,
@@ -622,17 +423,6 @@ cudaError_t launch_copy(float *dst, const float *src, size_t n,
   copy_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
       reinterpret_cast<float4 *>(dst), reinterpret_cast<const float4 *>(src),
       n4);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_hist_rollback(float *hist, const float *hist_snap,
-                                 const float *x, const int *m_dev, int *err_dev,
-                                 int B, int M, int conv_dim,
-                                 cudaStream_t stream) {
-  if (B == 0) return cudaSuccess;
-  hist_rollback_kernel<<<(unsigned)B, 256, 0, stream>>>(
-      reinterpret_cast<float4 *>(hist), hist_snap, x, m_dev, err_dev, M,
-      conv_dim);
   return cudaGetLastError();
 }
 

@@ -17,16 +17,16 @@ cudaError_t launch_steps(const float *S_in, float *S_out, float *ckpt,
                          const float *g, const float *beta, float *o, int B,
                          int kh, int vh, int M, cudaStream_t stream);
 
-// The same kernel with the layer core (conv1d + SiLU with a width-4
-// history, q/k normalisation, gates) computing its token inputs from raw
-// projections.  hist_in and hist_out must not overlap.
-cudaError_t launch_layer_steps(const float *S_in, float *S_out, float *ckpt,
-                               const float *hist_in, float *hist_out,
-                               const float *x, const float *conv_w,
-                               const float *a, const float *b,
-                               const float *A_log, const float *dt_bias,
-                               float eps, float *o, int B, int kh, int vh,
-                               int M, cudaStream_t stream);
+// Layer prologue (conv1d + SiLU with a width-4 history, q/k normalisation,
+// gates) writing the token inputs q, k, v, g, beta of M tokens.  hist_in and
+// hist_out must not overlap.
+cudaError_t launch_layer_prologue(const float *hist_in, float *hist_out,
+                                  const float *x, const float *conv_w,
+                                  const float *a, const float *b,
+                                  const float *A_log, const float *dt_bias,
+                                  float eps, float *q, float *k, float *v,
+                                  float *g, float *beta, int B, int kh, int vh,
+                                  int M, cudaStream_t stream);
 
 // Per-sequence conv-history rollback (see gdn_layer_hist_rollback).
 cudaError_t launch_hist_rollback(float *hist, const float *hist_snap,

@@ -194,21 +194,20 @@ int gdn_prefill(const gdn_shape *shape, int T, float *S, const float *q,
 int gdn_prefill_timeouts(unsigned int *count);
 
 /*
- * gdn_layer_step_m - the per-token layer core around the recurrence, fused
- * into the M-token kernel: for every token, a depthwise causal convolution
- * of width ck over the raw mixed q|k|v projection with a rolling history of
- * the previous ck-1 inputs (oldest first), SiLU, q and k divided by
- * sqrt(sum of squares + eps) per key head, the gates
+ * gdn_layer_prologue_m - the per-token layer core that produces the inputs
+ * of the update from raw projections, for M tokens: a depthwise causal
+ * convolution of width ck over the raw mixed q|k|v projection with a
+ * rolling history of the previous ck-1 inputs (oldest first), SiLU, q and k
+ * scaled to unit L2 norm per key head (x / sqrt(|x|^2 + eps)), and the gates
  *     beta = 1 / (1 + exp(-b)),
  *     g    = -exp(A_log) * softplus(a + dt_bias)
  *            (softplus(x) = x above 20, exp(x) below -20,
- *             log1p(exp(x)) otherwise),
- * then the update above.  These are steps 2-5 of figure 1 of "24 · GDN
- * linear attention to GPU" (conv + SiLU and gates listed in its section 3;
- * the q/k normalisation formula is not printed there: x / sqrt(|x|^2 + eps)
- * is this library's reading).
+ *             log1p(exp(x)) otherwise).
+ * These are steps 2-4 of figure 1 of "24 · GDN linear attention to GPU"
+ * (conv + SiLU and the gates are listed in its section 3; the article names
+ * the q/k normalisation without its formula, and the form above is this
+ * library's reading).  One streaming kernel: one warp per 128-channel row.
  *   ck       must be 4 (GDN_ESHAPE otherwise); conv_dim = 2*kh*kd + vh*vd
- *   S_in, S_out, ckpt, o     as gdn_step_m
  *   hist_in  [B][ck-1][conv_dim]  in: the previous ck-1 raw inputs
  *   hist_out [B][ck-1][conv_dim]  out: the last ck-1 raw inputs after
  *            token M-1; must not overlap hist_in (use two buffers in turn)
@@ -217,15 +216,37 @@ int gdn_prefill_timeouts(unsigned int *count);
  *   conv_w   [conv_dim][ck]
  *   a, b     [B][M][vh];   A_log, dt_bias [vh]
  *   eps      >= 0 (GDN_EINVAL otherwise)
- * Output m and ckpt[m] are bit-identical to the m-th of M successive calls
- * with M = 1 that pass the history forward.
+ *   q, k     [B][M][kh][kd] out;  v [B][M][vh][vd] out;  g, beta [B][M][vh] out
+ *            (exactly the inputs gdn_step_m takes)
+ */
+int gdn_layer_prologue_m(const gdn_shape *shape, int M, int ck, float eps,
+                         const float *hist_in, float *hist_out,
+                         const float *x, const float *conv_w, const float *a,
+                         const float *b, const float *A_log,
+                         const float *dt_bias, float *q, float *k, float *v,
+                         float *g, float *beta, gdn_stream_t stream);
+
+/*
+ * gdn_layer_workspace - bytes of device workspace gdn_layer_step_m needs to
+ * hold the M tokens' q, k, v, g and beta between its two kernels (0 on
+ * invalid arguments).
+ */
+size_t gdn_layer_workspace(const gdn_shape *shape, int M);
+
+/*
+ * gdn_layer_step_m - gdn_layer_prologue_m followed by gdn_step_m on the same
+ * stream, with the intermediate q, k, v, g, beta in the caller's workspace
+ * (at least gdn_layer_workspace() bytes, 16-byte aligned, device memory;
+ * GDN_ERANGE if smaller).  Arguments as in those two calls.  Output m and
+ * ckpt[m] are bit-identical to the m-th of M successive calls with M = 1
+ * that pass the history forward.
  */
 int gdn_layer_step_m(const gdn_shape *shape, int M, int ck, float eps,
                      const float *S_in, float *S_out, float *ckpt,
                      const float *hist_in, float *hist_out, const float *x,
                      const float *conv_w, const float *a, const float *b,
                      const float *A_log, const float *dt_bias, float *o,
-                     gdn_stream_t stream);
+                     void *workspace, size_t ws_bytes, gdn_stream_t stream);
 
 /*
  * gdn_layer_hist_rollback - the convolution history after m_dev[b] of the

@@ -1,6 +1,7 @@
-"""The fused layer core (conv1d + SiLU with rolling history, q/k
-normalisation, gates, recurrence) against the layer oracle, its exactness
-across launch splits, and the history rollback.
+"""The layer core (conv1d + SiLU with rolling history, q/k normalisation,
+gates) in front of the recurrence, against the layer oracle and against
+fp64 closed forms of each step, its exactness across launch splits, and the
+history rollback.
 
 Tolerances as in test_gpu_parity.py: normwise per (sequence, token) over
 all value heads for o, per (sequence, value head) for the state; 1e-5 for
@@ -44,8 +45,10 @@ def run_layer(L, S=None, hist=None, x=None, a=None, b=None, ckpt=False):
     hist_out = torch.empty_like(hist_in)
     ck = empty(M, B, vh, kd, vd) if ckpt else None
     o = empty(B, M, vh, vd)
+    ws = torch.empty(gdn.gdn_layer_workspace(B, L.kh, vh, M), dtype=torch.uint8,
+                     device="cuda")
     gdn.gdn_layer_step_m(S_in, S_out, ck, hist_in, hist_out, x, dev(L.conv_w),
-                         a, b, dev(L.A_log), dev(L.dt_bias), o, L.kh)
+                         a, b, dev(L.A_log), dev(L.dt_bias), o, L.kh, ws)
     return S_out, hist_out, o, ck
 
 
@@ -62,6 +65,32 @@ def test_layer_vs_oracle(oracle_mod, B, M, kh, vh):
     tol = TOL_STEP if M == 1 else TOL_MULTI
     assert es < tol and eo < tol
     assert np.array_equal(host(hist), hist_ref)
+
+
+def test_prologue_outputs_closed_forms():
+    """The prologue's q, k, v, g, beta against fp64 closed forms of each
+    step (causal convolution over [history, inputs], SiLU, per-head unit
+    norm, softplus and sigmoid gates)."""
+    import oracle_pins
+    L = gdn_inputs.make_layer_inputs(905, B=3, T=4)
+    B, vh = 3, 48
+    M = L.T
+    q = empty(B, M, L.kh, 128)
+    k = torch.empty_like(q)
+    v = empty(B, M, vh, 128)
+    g = empty(B, M, vh)
+    beta = torch.empty_like(g)
+    hist_out = torch.empty_like(dev(L.hist))
+    gdn.gdn_layer_prologue_m(dev(L.hist), hist_out, dev(L.x), dev(L.conv_w),
+                             dev(L.a), dev(L.b), dev(L.A_log),
+                             dev(L.dt_bias), q, k, v, g, beta, L.kh)
+    q64, k64, v64, g64, b64, h64 = oracle_pins._layer_inputs64(
+        L.hist, L.x, L.conv_w, L.a, L.b, L.A_log, L.dt_bias, L.kh, 128, vh,
+        128)
+    for got, ref in ((q, q64), (k, k64), (v, v64)):
+        assert max_rel(host(got), ref, axes=(-2, -1)) < 2e-6
+    assert max_rel(host(g), g64) < 2e-6 and max_rel(host(beta), b64) < 2e-6
+    assert np.array_equal(host(hist_out), h64.astype(np.float32))
 
 
 def test_layer_decode_full_size(oracle_mod):
@@ -140,14 +169,20 @@ def test_layer_refusals():
     st = torch.cuda.current_stream().cuda_stream
     P = lambda t: t.data_ptr()
 
-    def call(ck=4, eps=1e-6, h_out=None):
+    need = gdn.gdn_layer_workspace(B, L.kh, vh, 2)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+
+    def call(ck=4, eps=1e-6, h_out=None, ws_bytes=need, ws_ptr=None):
         return lib.gdn_layer_step_m(
             ctypes.byref(sh), 2, ck, eps, P(S), P(S), None, P(hist),
             P(hist2 if h_out is None else h_out), P(x), P(w), P(a), P(b),
-            P(Al), P(dt), P(o), st)
+            P(Al), P(dt), P(o), P(ws) if ws_ptr is None else ws_ptr,
+            ws_bytes, st)
 
     assert call() == gdn.GDN_OK
     assert call(ck=3) == gdn.GDN_ESHAPE
     assert call(eps=-1.0) == gdn.GDN_EINVAL
     assert call(h_out=hist) == gdn.GDN_EALIAS   # in-place history refused
+    assert call(ws_bytes=need - 16) == gdn.GDN_ERANGE
+    assert call(ws_ptr=P(S)) == gdn.GDN_EALIAS  # workspace over the state
     torch.cuda.synchronize()
