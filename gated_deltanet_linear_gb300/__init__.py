@@ -28,19 +28,23 @@ __all__ = [
     "GDN_PREC_FP32", "GDN_PREC_BF16X3", "GDN_PREC_BF16", "GDN_MAX_TOKENS",
     "gdn_prefill_timeouts", "gdn_layer_prologue_m", "gdn_layer_workspace",
     "gdn_layer_step_m", "gdn_layer_hist_rollback",
+    "gdn_layer_step_m_noalloc", "GDN_NOALLOC_SCRATCH_BYTES",
 ]
 
 GDN_OK, GDN_EINVAL, GDN_ESHAPE, GDN_EALIGN = 0, -1, -2, -3
 GDN_ECUDA, GDN_ERANGE, GDN_EPTR, GDN_EALIAS = -4, -5, -6, -7
+GDN_ESCRATCH = -8
 GDN_PREC_FP32, GDN_PREC_BF16X3, GDN_PREC_BF16 = 0, 1, 2
 GDN_MAX_TOKENS = 1 << 20
+GDN_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 # Every symbol include/gdn.h declares.
 EXPORTS = ("gdn_step", "gdn_step_m", "gdn_mark", "gdn_rollback",
            "gdn_rollback_seq", "gdn_prefill_workspace", "gdn_prefill",
            "gdn_prefill_timeouts", "gdn_layer_prologue_m",
            "gdn_layer_workspace", "gdn_layer_step_m",
-           "gdn_layer_hist_rollback", "gdn_strerror", "gdn_version")
+           "gdn_layer_hist_rollback", "gdn_layer_step_m_noalloc",
+           "gdn_strerror", "gdn_version")
 
 
 class GDNError(RuntimeError):
@@ -94,6 +98,9 @@ def load():
     lib.gdn_layer_step_m.argtypes = [cp, ip, ip, ctypes.c_float] + [vp] * 13 + \
         [ctypes.c_size_t, vp]
     lib.gdn_layer_step_m.restype = ctypes.c_int
+    lib.gdn_layer_step_m_noalloc.argtypes = [cp, ip, ip, ctypes.c_float] + \
+        [vp] * 12 + [vp]
+    lib.gdn_layer_step_m_noalloc.restype = ctypes.c_int
     lib.gdn_layer_hist_rollback.argtypes = [cp, ip, ip] + [vp] * 6
     lib.gdn_layer_hist_rollback.restype = ctypes.c_int
     lib.gdn_prefill_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint)]
@@ -305,6 +312,35 @@ def gdn_layer_step_m(S_in, S_out, ckpt, hist_in, hist_out, x, conv_w, a, b,
         ctypes.byref(sh), M, ck, float(eps), *args, workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), _stream(stream)),
         "gdn_layer_step_m")
+
+
+def gdn_layer_step_m_noalloc(S_in, S_out, ckpt, hist_in, hist_out, x, conv_w,
+                             a, b, A_log, dt_bias, o, kh, eps=1e-6,
+                             stream=None):
+    """gdn_layer_step_m for callers that cannot allocate device memory: the
+    intermediate q, k, v, g, beta go to the library's own static scratch of
+    GDN_NOALLOC_SCRATCH_BYTES (shared by every call on the device; calls that
+    overlap on the GPU race).  Larger requests raise GDNError with
+    GDN_ESCRATCH."""
+    if S_in.dim() != 4:
+        raise ValueError("S must be [B][vh][kd][vd]")
+    B, vh, kd, vd = S_in.shape
+    sh = Shape(B, int(kh), vh, kd, vd)
+    M = int(x.shape[1])
+    ck = int(conv_w.shape[1])
+    conv_dim = 2 * int(kh) * kd + vh * vd
+    n = B * vh * kd * vd
+    args = (_t(S_in, "S_in", n), _t(S_out, "S_out", n),
+            _t(ckpt, "ckpt", M * n),
+            _t(hist_in, "hist_in", B * (ck - 1) * conv_dim),
+            _t(hist_out, "hist_out", B * (ck - 1) * conv_dim),
+            _t(x, "x", B * M * conv_dim), _t(conv_w, "conv_w", conv_dim * ck),
+            _t(a, "a", B * M * vh), _t(b, "b", B * M * vh),
+            _t(A_log, "A_log", vh), _t(dt_bias, "dt_bias", vh),
+            _t(o, "o", B * M * vh * vd))
+    _check(load().gdn_layer_step_m_noalloc(
+        ctypes.byref(sh), M, ck, float(eps), *args, _stream(stream)),
+        "gdn_layer_step_m_noalloc")
 
 
 def gdn_layer_hist_rollback(hist, M, m_dev, hist_snap, x, kh, kd=128, vd=128,

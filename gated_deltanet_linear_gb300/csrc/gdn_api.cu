@@ -409,6 +409,9 @@ const char *gdn_strerror(int status) {
     case GDN_ERANGE: return "count out of range (M, m, T, chunk, precision or workspace)";
     case GDN_EPTR: return "pointer is not device memory of the current device";
     case GDN_EALIAS: return "buffers overlap where they must not";
+    case GDN_ESCRATCH:
+      return "request needs more than the static scratch of "
+             "gdn_layer_step_m_noalloc (GDN_NOALLOC_SCRATCH_BYTES)";
     default: return "unknown status";
   }
 }

@@ -30,7 +30,9 @@
  *     otherwise).  NULL where a buffer is required gives GDN_EINVAL.
  *   - Ownership: the caller allocates and frees everything.  The library
  *     never allocates device memory and never synchronises; every call only
- *     enqueues work on `stream` and returns.
+ *     enqueues work on `stream` and returns.  (The one exception is the
+ *     static scratch array of gdn_layer_step_m_noalloc, created with the
+ *     library's device code.)
  *   - Aliasing: outputs must not overlap inputs or each other, except where
  *     a call states otherwise (GDN_EALIAS).
  *   - Errors: arguments are validated on the host before anything is
@@ -72,7 +74,9 @@ enum {
     GDN_ECUDA = -4,  /* a CUDA runtime call or kernel launch failed        */
     GDN_ERANGE = -5, /* M, m, T, chunk or workspace size out of range      */
     GDN_EPTR = -6,   /* a pointer is not device memory of this device      */
-    GDN_EALIAS = -7  /* buffers overlap where they must not                */
+    GDN_EALIAS = -7, /* buffers overlap where they must not                */
+    GDN_ESCRATCH = -8 /* request larger than the static scratch of
+                         gdn_layer_step_m_noalloc                          */
 };
 
 /* Largest M / T accepted by one call. */
@@ -261,6 +265,45 @@ int gdn_layer_hist_rollback(const gdn_shape *shape, int M, int ck,
                             const int *m_dev, const float *hist_snap,
                             const float *x, float *hist, int *err_dev,
                             gdn_stream_t stream);
+
+/* Bytes of the static scratch array behind gdn_layer_step_m_noalloc. */
+#define GDN_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * gdn_layer_step_m_noalloc - gdn_layer_step_m without a workspace argument,
+ * for callers that cannot allocate device memory (a host handed only the
+ * layer's tensors by a runtime whose allocator it cannot reach, or a decode
+ * loop that must not call cudaMalloc, which can synchronise the device and
+ * fail under memory pressure, between steps).  The article has no
+ * counterpart: this is an interface variant, not a step of the method.
+ *
+ * The intermediate q, k, v, g and beta go to a file-scope device array of
+ * GDN_NOALLOC_SCRATCH_BYTES (16 MiB), which every GPU that loads the
+ * library's device code holds until the process exits.  The call allocates
+ * nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ *   - Limit: a request whose gdn_layer_workspace() exceeds
+ *     GDN_NOALLOC_SCRATCH_BYTES returns GDN_ESCRATCH and launches nothing
+ *     (at kh = 16, vh = 48, kd = vd = 128, 41,344 bytes per sequence and
+ *     token: B * M > 405).
+ *   - Set-up: the first call on a device, with that device current, looks
+ *     up the array's device address (cudaGetSymbolAddress) and keeps it;
+ *     make that first call before any stream capture begins.
+ *   - Sharing: all calls on a device share the one array, which keeps the
+ *     last call's contents.  Nothing in it needs to start at zero (every
+ *     byte read is written first in the same call), so nothing is cleared.
+ *     Calls whose work overlaps on the GPU (different streams with no
+ *     ordering between them) race on the array: order them on one stream or
+ *     with events.
+ * Other arguments, results and status codes are those of gdn_layer_step_m,
+ * and results are bit-identical to it on the same inputs.
+ */
+int gdn_layer_step_m_noalloc(const gdn_shape *shape, int M, int ck, float eps,
+                             const float *S_in, float *S_out, float *ckpt,
+                             const float *hist_in, float *hist_out,
+                             const float *x, const float *conv_w,
+                             const float *a, const float *b,
+                             const float *A_log, const float *dt_bias,
+                             float *o, gdn_stream_t stream);
 
 /* Static description of a status code (never NULL). */
 const char *gdn_strerror(int status);
