@@ -14,7 +14,8 @@ Contents
              linear recurrence, and the chunk-parallel form.
   gdn_ref.c also holds the layer core around the recurrence (conv1d + SiLU
              with rolling history, q/k normalisation, gate computation),
-             ``run_layer``.
+             ``run_layer``, and the gated RMSNorm on its output,
+             ``run_gate_norm``.
 
 Pins (each checked by tests that do not use the oracle's own code):
   run_f32     pinned by closed forms (alpha = 1 & beta = 0 identity, beta = 1
@@ -28,6 +29,10 @@ Pins (each checked by tests that do not use the oracle's own code):
               SiLU/softplus/sigmoid values, unit norms, the +-20 softplus
               branches, history shift) and by equality with run_f32 when the
               layer steps are bypassed by construction.
+  run_gate_norm pinned by closed forms: unit RMS of y / (w silu(z)), a
+              +-1 row with silu(ln 3) = 0.75 ln 3, the eps placement on a
+              constant row, per-channel weights, scale invariance and odd
+              symmetry in o.
 """
 
 from __future__ import annotations
@@ -80,6 +85,9 @@ def _load():
         lib.gdn_oracle_layer.argtypes = [ctypes.c_int] * 7 + [ctypes.c_float] + [fp] * 10
         lib.gdn_oracle_layer.restype = ctypes.c_int
         lib.gdn_oracle_set_threads.argtypes = [ctypes.c_int]
+        lib.gdn_oracle_gate_norm.argtypes = [ctypes.c_int] * 4 + \
+            [ctypes.c_float] + [fp] * 4
+        lib.gdn_oracle_gate_norm.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -150,6 +158,22 @@ def run_layer(S, hist, x, conv_w, a, b, A_log, dt_bias, kh, eps=1e-6,
     if rc != 0:
         raise RuntimeError(f"gdn_oracle_layer failed ({rc})")
     return (S, hist, o, ck_) if ckpt else (S, hist, o)
+
+
+def run_gate_norm(o, z, w, eps=1e-6):
+    """Gated RMSNorm of the recurrence output per (sequence, token, value
+    head): o, z [B][T][vh][vd], w [vd].  Returns y, same shape as o."""
+    lib = _load()
+    o, z, w = map(_f32c, (o, z, w))
+    if o.ndim != 4 or z.shape != o.shape or w.shape != (o.shape[3],):
+        raise ValueError("inconsistent gate-norm shapes")
+    B, T, vh, vd = o.shape
+    y = np.zeros_like(o)
+    rc = lib.gdn_oracle_gate_norm(B, T, vh, vd, float(eps), _ptr(o), _ptr(z),
+                                  _ptr(w), _ptr(y))
+    if rc != 0:
+        raise RuntimeError(f"gdn_oracle_gate_norm failed ({rc})")
+    return y
 
 
 def run_inputs(inp, ckpt: bool = False):

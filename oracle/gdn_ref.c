@@ -251,3 +251,44 @@ int gdn_oracle_layer(int B, int T, int kh, int vh, int kd, int vd, int ck,
     free(xc); free(qn); free(kn); free(gg); free(bb); free(ot);
     return rc;
 }
+
+/* ------------------------------------------------------------------------
+ * Gated RMSNorm on the recurrence output ("Kestrel_VLLM - 24 · GDN linear
+ * attention to GPU", figure 1 step 6, and section 4, which runs it one value
+ * head at a time).  The article names the step without its formula; this is
+ * the plain reading of an RMS normalisation with a per-channel weight and a
+ * SiLU output gate:
+ *   for every (sequence b, token t, value head h), over its vd channels c:
+ *     ms   = (sum_c o[c]^2) / vd
+ *     r    = 1 / sqrt(ms + eps)
+ *     y[c] = ((o[c] * r) * w[c]) * (z[c] / (1 + exp(-z[c])))
+ *   o, z, y [B][T][vh][vd];  w [vd] (shared by all heads);  eps >= 0.
+ * fp32, separately rounded, left-to-right sum.  y may be o (in place).
+ * Returns 0, or -1 on a bad shape.
+ */
+int gdn_oracle_gate_norm(int B, int T, int vh, int vd, float eps,
+                         const float *o, const float *z, const float *w,
+                         float *y) {
+    if (B < 0 || T < 0 || vh <= 0 || vd <= 0 || !(eps >= 0.0f))
+        return -1;
+    const size_t rows = (size_t)B * (size_t)T * (size_t)vh;
+    for (size_t r = 0; r < rows; r++) {
+        const float *orow = o + r * (size_t)vd;
+        const float *zrow = z + r * (size_t)vd;
+        float *yrow = y + r * (size_t)vd;
+        float ss = 0.0f;
+        for (int c = 0; c < vd; c++) {
+            const float p = orow[c] * orow[c];
+            ss = ss + p;
+        }
+        const float ms = ss / (float)vd;
+        const float rinv = 1.0f / sqrtf(ms + eps);
+        for (int c = 0; c < vd; c++) {
+            const float gate = zrow[c] / (1.0f + expf(-zrow[c]));
+            const float n = orow[c] * rinv;
+            const float nw = n * w[c];
+            yrow[c] = nw * gate;
+        }
+    }
+    return 0;
+}

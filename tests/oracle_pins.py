@@ -276,3 +276,69 @@ def layer_pin_gate_values(run_layer, run_f32):
 
 LAYER_PINS = [layer_pin_closed_forms, layer_pin_identity_conv,
               layer_pin_softplus_branches, layer_pin_gate_values]
+
+
+# ---------------------------------------------------------------------------
+# Gated RMSNorm on the recurrence output (one value head's vd channels at a
+# time).  Each pin takes run_gate_norm(o, z, w, eps) -> y.  The values are
+# closed forms: a row of +-1 has RMS exactly 1, and at z = ln 3 the sigmoid
+# is exactly 3/4, so the SiLU gate is 0.75 ln 3.
+
+_SILU_LN3 = 0.75 * np.log(3.0)
+
+
+def _pm_ones(B, T, vh, vd, seed):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return np.where(rng.standard_normal((B, T, vh, vd)) < 0, -1.0, 1.0)
+
+
+def gate_norm_pin_unit_row(run_gate_norm):
+    """o = +-1 (RMS 1), z = ln 3, w = 1, eps = 0: y = +-0.75 ln 3."""
+    o = _pm_ones(2, 3, 4, 128, 41)
+    z = np.full_like(o, np.log(3.0))
+    y = run_gate_norm(o, z, np.ones(128), eps=0.0)
+    assert np.allclose(y, o * _SILU_LN3, rtol=2e-6, atol=0)
+
+
+def gate_norm_pin_per_channel(run_gate_norm):
+    """Per-channel weight and gate: w[c] = 2^(c mod 5 - 2) and z[c] cycling
+    through ln 3, -ln 3, 0 (SiLU 0.75 ln 3, -0.25 ln 3, 0) on a +-1 row."""
+    vd = 128
+    o = _pm_ones(1, 2, 3, vd, 42)
+    c = np.arange(vd)
+    w = 2.0 ** (c % 5 - 2)
+    zc = np.array([np.log(3.0), -np.log(3.0), 0.0])[c % 3]
+    sc = np.array([_SILU_LN3, -0.25 * np.log(3.0), 0.0])[c % 3]
+    y = run_gate_norm(o, np.broadcast_to(zc, o.shape), w, eps=0.0)
+    assert np.allclose(y, o * w * sc, rtol=2e-6, atol=1e-30)
+
+
+def gate_norm_pin_eps_placement(run_gate_norm):
+    """A constant row o = 0.01 with eps = 1e-4: RMS sqrt(1e-4 + 1e-4), so
+    o * r = 1/sqrt 2; an all-zero row gives y = 0."""
+    o = np.full((1, 1, 2, 128), 0.01)
+    o[0, 0, 1] = 0.0
+    z = np.full_like(o, np.log(3.0))
+    y = run_gate_norm(o, z, np.ones(128), eps=1e-4)
+    assert np.allclose(y[0, 0, 0], _SILU_LN3 / np.sqrt(2.0), rtol=2e-6)
+    assert np.all(y[0, 0, 1] == 0.0)
+
+
+def gate_norm_pin_row_scaling(run_gate_norm):
+    """eps = 0: scaling a whole (sequence, token, head) row by a power of two
+    (a different one per row) or negating it changes y by nothing or by its
+    sign, bit for bit; each row is normalised on its own."""
+    rng = np.random.Generator(np.random.PCG64(43))
+    o = rng.standard_normal((2, 2, 3, 128)).astype(np.float32)
+    z = rng.standard_normal(o.shape).astype(np.float32)
+    w = rng.uniform(0.5, 2.0, 128).astype(np.float32)
+    y = run_gate_norm(o, z, w, eps=0.0)
+    scale = np.float32(2.0) ** np.arange(-6, 6).reshape(2, 2, 3, 1)
+    ys = run_gate_norm(o * scale, z, w, eps=0.0)
+    yn = run_gate_norm(-o, z, w, eps=0.0)
+    assert np.array_equal(ys, y)
+    assert np.array_equal(yn, -y)
+
+
+GATE_NORM_PINS = [gate_norm_pin_unit_row, gate_norm_pin_per_channel,
+                  gate_norm_pin_eps_placement, gate_norm_pin_row_scaling]
