@@ -494,6 +494,25 @@ def main():
             "bytes_per_launch": lbytes,
             "note": "raw projections in: layer prologue (conv1d+SiLU with "
                     "history, q/k norm, gates) then the update, two launches"}
+        # the same, followed by the gated RMSNorm in place on o
+        _, zn, wn = gdn_inputs.make_gate_norm_inputs(
+            gdn_inputs.SEED_BASE + 101, 64, 1, 48)
+        lz, lwn = tens(zn), tens(wn)
+
+        def lnstep(i):
+            lstep(i)
+            gdn.gdn_gated_rmsnorm_m(lo, lz, lwn, lo, stream=stream)
+        for i in range(5):
+            lnstep(i)
+        lnms = time_launches(torch, lnstep, n, stream)
+        lnbytes = lbytes + 3 * 64 * 48 * D * 4
+        parts["layer_norm_decode_b64"] = {
+            "ms": lnms, "head_steps_per_s": 64 * 48 / (lnms * 1e-3),
+            "gbs": lnbytes / (lnms * 1e-3) / 1e9,
+            "frac_of_measured_hbm": lnbytes / (lnms * 1e-3) / 1e9 / hbm_peak,
+            "bytes_per_launch": lnbytes,
+            "note": "raw projections in, normalised output out: layer "
+                    "prologue, update, gated RMSNorm in place; three launches"}
         del SL, hL
         torch.cuda.empty_cache()
         prefill_parts(torch, gdn, tens, stream, peaks, parts)

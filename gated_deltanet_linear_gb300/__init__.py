@@ -29,6 +29,7 @@ __all__ = [
     "gdn_prefill_timeouts", "gdn_layer_prologue_m", "gdn_layer_workspace",
     "gdn_layer_step_m", "gdn_layer_hist_rollback",
     "gdn_layer_step_m_noalloc", "GDN_NOALLOC_SCRATCH_BYTES",
+    "gdn_gated_rmsnorm_m",
 ]
 
 GDN_OK, GDN_EINVAL, GDN_ESHAPE, GDN_EALIGN = 0, -1, -2, -3
@@ -43,8 +44,8 @@ EXPORTS = ("gdn_step", "gdn_step_m", "gdn_mark", "gdn_rollback",
            "gdn_rollback_seq", "gdn_prefill_workspace", "gdn_prefill",
            "gdn_prefill_timeouts", "gdn_layer_prologue_m",
            "gdn_layer_workspace", "gdn_layer_step_m",
-           "gdn_layer_hist_rollback", "gdn_layer_step_m_noalloc",
-           "gdn_strerror", "gdn_version")
+           "gdn_layer_hist_rollback", "gdn_gated_rmsnorm_m",
+           "gdn_layer_step_m_noalloc", "gdn_strerror", "gdn_version")
 
 
 class GDNError(RuntimeError):
@@ -98,6 +99,8 @@ def load():
     lib.gdn_layer_step_m.argtypes = [cp, ip, ip, ctypes.c_float] + [vp] * 13 + \
         [ctypes.c_size_t, vp]
     lib.gdn_layer_step_m.restype = ctypes.c_int
+    lib.gdn_gated_rmsnorm_m.argtypes = [cp, ip, ctypes.c_float] + [vp] * 5
+    lib.gdn_gated_rmsnorm_m.restype = ctypes.c_int
     lib.gdn_layer_step_m_noalloc.argtypes = [cp, ip, ip, ctypes.c_float] + \
         [vp] * 12 + [vp]
     lib.gdn_layer_step_m_noalloc.restype = ctypes.c_int
@@ -312,6 +315,20 @@ def gdn_layer_step_m(S_in, S_out, ckpt, hist_in, hist_out, x, conv_w, a, b,
         ctypes.byref(sh), M, ck, float(eps), *args, workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), _stream(stream)),
         "gdn_layer_step_m")
+
+
+def gdn_gated_rmsnorm_m(o, z, w, y, eps=1e-6, stream=None):
+    """Gated RMSNorm of o [B][M][vh][vd] with gate z (same shape) and
+    per-channel weight w [vd] into y (y may be o)."""
+    if o.dim() != 4:
+        raise ValueError("o must be [B][M][vh][vd]")
+    B, M, vh, vd = o.shape
+    sh = Shape(B, 1, vh, 128, vd)
+    n = o.numel()
+    _check(load().gdn_gated_rmsnorm_m(
+        ctypes.byref(sh), M, float(eps), _t(o, "o", n), _t(z, "z", n),
+        _t(w, "w", vd), _t(y, "y", n), _stream(stream)),
+        "gdn_gated_rmsnorm_m")
 
 
 def gdn_layer_step_m_noalloc(S_in, S_out, ckpt, hist_in, hist_out, x, conv_w,

@@ -399,6 +399,27 @@ int gdn_layer_hist_rollback(const gdn_shape *s, int M, int ck,
                                              (cudaStream_t)stream));
 }
 
+int gdn_gated_rmsnorm_m(const gdn_shape *s, int M, float eps, const float *o,
+                        const float *z, const float *w, float *y,
+                        gdn_stream_t stream) {
+  int r = check_shape(s);
+  if (r) return r;
+  if (M < 1 || M > GDN_MAX_TOKENS) return GDN_ERANGE;
+  if (!(eps >= 0.0f) || eps > 3.0e38f) return GDN_EINVAL;
+  if (s->B == 0) return GDN_OK;
+  const size_t rows = (size_t)s->B * M * s->vh;
+  const size_t ob = rows * s->vd * 4;
+  Buf b[] = {{o, ob}, {z, ob}, {w, (size_t)s->vd * 4}, {y, ob}};
+  r = check_bufs(b, 4);
+  if (r) return r;
+  // y may be o exactly (in place); otherwise no output overlap
+  if (y != o && overlaps(b[3], b[0])) return GDN_EALIAS;
+  if (overlaps(b[3], b[1]) || overlaps(b[3], b[2])) return GDN_EALIAS;
+  cudaGetLastError();
+  return status_of(gdn::launch_gate_norm(o, z, w, y, eps, rows,
+                                         (cudaStream_t)stream));
+}
+
 const char *gdn_strerror(int status) {
   switch (status) {
     case GDN_OK: return "success";

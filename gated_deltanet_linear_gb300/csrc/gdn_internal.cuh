@@ -28,6 +28,12 @@ cudaError_t launch_layer_prologue(const float *hist_in, float *hist_out,
                                   float *g, float *beta, int B, int kh, int vh,
                                   int M, cudaStream_t stream);
 
+// Gated RMSNorm of `rows` rows of 128 channels (see gdn_gated_rmsnorm_m);
+// y may equal o.
+cudaError_t launch_gate_norm(const float *o, const float *z, const float *w,
+                             float *y, float eps, size_t rows,
+                             cudaStream_t stream);
+
 // Per-sequence conv-history rollback (see gdn_layer_hist_rollback).
 cudaError_t launch_hist_rollback(float *hist, const float *hist_snap,
                                  const float *x, const int *m_dev, int *err_dev,

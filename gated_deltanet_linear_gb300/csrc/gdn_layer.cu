@@ -126,6 +126,39 @@ __global__ void __launch_bounds__(128)
   }
 }
 
+// Gated RMSNorm on the update's output, one warp per (sequence, token, value
+// head) row of 128 channels ("24 · GDN linear attention to GPU", figure 1
+// step 6; the article runs it one value head at a time and prints no
+// formula):  y = w * o / sqrt(mean(o^2) + eps) * silu(z).  Lane l owns
+// channels 4l .. 4l+3; the sum of squares is a fixed xor tree, so every lane
+// holds the same bits.  o is read with ordinary loads because y may be o.
+__global__ void __launch_bounds__(256)
+    gate_norm_kernel(const float *o, const float *__restrict__ z,
+                     const float *__restrict__ w, float *y, float eps,
+                     size_t rows) {
+  const int lane = threadIdx.x & 31;
+  const size_t row = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (row >= rows) return;
+  const size_t off = row * kDim + 4 * lane;
+  const float4 ov = *reinterpret_cast<const float4 *>(o + off);
+  const float4 zv = __ldg(reinterpret_cast<const float4 *>(z + off));
+  const float4 wv = __ldg(reinterpret_cast<const float4 *>(w + 4 * lane));
+  float ss = __fmul_rn(ov.x, ov.x);
+  ss = __fmaf_rn(ov.y, ov.y, ss);
+  ss = __fmaf_rn(ov.z, ov.z, ss);
+  ss = __fmaf_rn(ov.w, ov.w, ss);
+#pragma unroll
+  for (int d = 16; d; d >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(kFull, ss, d));
+  // mean over the 128 channels: the scale by 2^-7 is exact
+  const float r = __frcp_rn(__fsqrt_rn(__fadd_rn(__fmul_rn(ss, 0.0078125f), eps)));
+  const float *oe = &ov.x, *ze = &zv.x, *we = &wv.x;
+  float out[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    out[e] = __fmul_rn(__fmul_rn(__fmul_rn(oe[e], r), we[e]), silu(ze[e]));
+  *reinterpret_cast<float4 *>(y + off) = make_float4(out[0], out[1], out[2], out[3]);
+}
+
 // One CTA per sequence: history after m_dev[b] tokens of a launch = rows
 // m .. m+2 of [hist_snap rows, x rows].
 __global__ void hist_rollback_kernel(float4 *__restrict__ hist,
@@ -186,6 +219,16 @@ cudaError_t launch_layer_prologue(const float *hist_in, float *hist_out,
   const size_t blocks = (warps + 3) / 4;
   if (blocks > 0x7fffffffull) return cudaErrorInvalidConfiguration;
   layer_prologue_kernel<<<(unsigned)blocks, 128, 0, stream>>>(P);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gate_norm(const float *o, const float *z, const float *w,
+                             float *y, float eps, size_t rows,
+                             cudaStream_t stream) {
+  if (rows == 0) return cudaSuccess;
+  const size_t blocks = (rows + 7) / 8;
+  if (blocks > 0x7fffffffull) return cudaErrorInvalidConfiguration;
+  gate_norm_kernel<<<(unsigned)blocks, 256, 0, stream>>>(o, z, w, y, eps, rows);
   return cudaGetLastError();
 }
 

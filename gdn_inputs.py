@@ -183,3 +183,20 @@ def make_layer_inputs(seed: int, B: int, T: int, kh: int = 16, vh: int = 48,
     dt_bias = (dt + np.log(-np.expm1(-dt))).astype(np.float32)
     return LayerInputs(S=S, hist=hist, x=x, conv_w=conv_w, a=a, b=b,
                        A_log=A_log, dt_bias=dt_bias, kh=kh, T=T)
+
+
+def make_gate_norm_inputs(seed: int, B: int, T: int, vh: int = 48,
+                          vd: int = 128):
+    """Inputs of the gated RMSNorm on the update's output, drawn in this
+    order from one PCG64 generator:
+      o = N(0, 1) * s per (b, t, head) row, s = exp(U(log 1e-3, log 10))
+          (rows of very different scale, as outputs of different heads are);
+      z ~ N(0, 1) (the gate projection);
+      w = 1 + 0.1 N(0, 1) per channel (around the usual all-ones start).
+    Returns (o, z, w) as fp32 arrays [B][T][vh][vd], [B][T][vh][vd], [vd]."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    s = np.exp(rng.uniform(np.log(1e-3), np.log(10.0), (B, T, vh, 1)))
+    o = (rng.standard_normal((B, T, vh, vd)) * s).astype(np.float32)
+    z = rng.standard_normal((B, T, vh, vd)).astype(np.float32)
+    w = (1.0 + 0.1 * rng.standard_normal(vd)).astype(np.float32)
+    return o, z, w

@@ -266,6 +266,24 @@ int gdn_layer_hist_rollback(const gdn_shape *shape, int M, int ck,
                             const float *x, float *hist, int *err_dev,
                             gdn_stream_t stream);
 
+/*
+ * gdn_gated_rmsnorm_m - the gated RMS normalisation of the update's output,
+ * per (sequence, token, value head) row of vd channels:
+ *     y = w * o / sqrt(mean(o^2) + eps) * silu(z),   silu(z) = z / (1 + exp(-z)).
+ * Step 6 of figure 1 of "24 · GDN linear attention to GPU", run there one
+ * value head at a time; the article prints no formula, and the form above
+ * (weight per channel, SiLU output gate) is this library's reading.
+ *   o, z, y  [B][M][vh][vd]  (o as written by gdn_step_m / gdn_layer_step_m;
+ *            z the gate projection); y may be o (in place), otherwise y must
+ *            not overlap o; y must not overlap z or w
+ *   w        [vd], shared by all heads
+ *   eps      >= 0 (GDN_EINVAL otherwise);  1 <= M <= GDN_MAX_TOKENS
+ * One streaming kernel, one warp per row.
+ */
+int gdn_gated_rmsnorm_m(const gdn_shape *shape, int M, float eps,
+                        const float *o, const float *z, const float *w,
+                        float *y, gdn_stream_t stream);
+
 /* Bytes of the static scratch array behind gdn_layer_step_m_noalloc. */
 #define GDN_NOALLOC_SCRATCH_BYTES (16u << 20)
 
