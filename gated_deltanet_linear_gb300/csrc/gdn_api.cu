@@ -366,9 +366,11 @@ int gdn_layer_step_m(const gdn_shape *s, int M, int ck, float eps,
       hist_in, hist_out, x, conv_w, a, b, A_log, dt_bias, eps, q, k, v, g,
       beta, s->B, s->kh, s->vh, M, (cudaStream_t)stream);
   if (e != cudaSuccess) return GDN_ECUDA;
+  // the update overlaps the prologue's tail: it loads the state, which the
+  // prologue never writes, before it waits for q, k, v, g, beta
   return status_of(gdn::launch_steps(S_in, S_out, ckpt, q, k, v, g, beta, o,
                                      s->B, s->kh, s->vh, M,
-                                     (cudaStream_t)stream));
+                                     (cudaStream_t)stream, true));
 }
 
 int gdn_layer_hist_rollback(const gdn_shape *s, int M, int ck,

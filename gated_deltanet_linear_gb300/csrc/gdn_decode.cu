@@ -33,6 +33,14 @@
 // 32-byte sectors of global memory.  Results go straight from registers to
 // global memory with 128-bit stores that skip L1.
 //
+// Launch overlap.  Behind the layer prologue the kernel is launched as a
+// programmatic dependent: it may start while the prologue still runs, puts
+// its first state units in flight (the prologue never writes the state),
+// and waits for the prologue's results (griddepcontrol.wait) before its
+// first read of the token inputs.  In an ordinary launch the wait returns at
+// once.  The kernel also lets its own dependents launch early; they wait
+// for its completion in the same way before reading its outputs.
+//
 // Determinism.  Every product and sum is an explicit round-to-nearest
 // intrinsic and the reduction tree is fixed, so a token gives the same bits
 // whether it is the only token of a launch or one of M: gdn_step_m(M) is
@@ -266,6 +274,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, kCtasPerSm)
   const size_t gw = (size_t)blockIdx.x * kWarpsPerCta + warp;
   const size_t nw = (size_t)gridDim.x * kWarpsPerCta;
   const size_t mine = gw < nunits ? (nunits - gw + nw - 1) / nw : 0;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // Prologue: the first kStages - 1 units in flight (empty groups keep the
   // group count uniform).
@@ -297,6 +306,8 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, kCtasPerSm)
                       (bm * vh + vi) * kDim + 8 * cg + 4 * h, bm * vh + vi);
   };
 
+  // the token inputs may come from the kernel this one overlaps with
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   TokenIn cur;
   if (mine > 0) cur = token_at(0, 0);
   for (size_t i = 0; i < mine; ++i) {
@@ -383,10 +394,30 @@ int sm_count() {
 
 }  // namespace
 
+// Launch with the programmatic-dependent attribute when `overlap` is set.
+template <typename... Params, typename... Args>
+cudaError_t launch_maybe_overlapped(void (*kernel)(Params...), dim3 grid,
+                                    dim3 block, size_t smem,
+                                    cudaStream_t stream, bool overlap,
+                                    Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 cudaError_t launch_steps(const float *S_in, float *S_out, float *ckpt,
                          const float *q, const float *k, const float *v,
                          const float *g, const float *beta, float *o, int B,
-                         int kh, int vh, int M, cudaStream_t stream) {
+                         int kh, int vh, int M, cudaStream_t stream,
+                         bool overlap) {
   const size_t nheads = (size_t)B * vh;
   const size_t nunits = nheads * kUnitsPerHead;
   if (nunits == 0) return cudaSuccess;
@@ -400,17 +431,21 @@ cudaError_t launch_steps(const float *S_in, float *S_out, float *ckpt,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemPerCta);
     if (e != cudaSuccess) return e;
-    gdn_steps_kernel<true><<<grid, block, kSmemPerCta, stream>>>(
-        S_in, S_out, ckpt, q, k, v, g, beta, o, vh, kh, vh / kh, M, nheads);
+    e = launch_maybe_overlapped(gdn_steps_kernel<true>, grid, block,
+                                kSmemPerCta, stream, overlap, S_in, S_out,
+                                ckpt, q, k, v, g, beta, o, vh, kh, vh / kh, M,
+                                nheads);
   } else {
     e = cudaFuncSetAttribute(gdn_steps_kernel<false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemPerCta);
     if (e != cudaSuccess) return e;
-    gdn_steps_kernel<false><<<grid, block, kSmemPerCta, stream>>>(
-        S_in, S_out, nullptr, q, k, v, g, beta, o, vh, kh, vh / kh, M, nheads);
+    e = launch_maybe_overlapped(gdn_steps_kernel<false>, grid, block,
+                                kSmemPerCta, stream, overlap, S_in, S_out,
+                                (float *)nullptr, q, k, v, g, beta, o, vh, kh,
+                                vh / kh, M, nheads);
   }
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_copy(float *dst, const float *src, size_t n,

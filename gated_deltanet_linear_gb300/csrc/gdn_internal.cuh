@@ -11,11 +11,14 @@ constexpr int kDim = 128;  // kd == vd: the only head size the kernels serve
 
 // Token-serial update of every head over M tokens (gdn_step, gdn_step_m and
 // the fp32 prefill path).  Pointers and layouts as in gdn.h; S_out may equal
-// S_in.  ckpt may be nullptr.
+// S_in.  ckpt may be nullptr.  overlap: launch as a programmatic dependent of
+// the previous kernel on the stream, which then must not write S_in (the
+// kernel starts loading the state before it waits for that kernel).
 cudaError_t launch_steps(const float *S_in, float *S_out, float *ckpt,
                          const float *q, const float *k, const float *v,
                          const float *g, const float *beta, float *o, int B,
-                         int kh, int vh, int M, cudaStream_t stream);
+                         int kh, int vh, int M, cudaStream_t stream,
+                         bool overlap = false);
 
 // Layer prologue (conv1d + SiLU with a width-4 history, q/k normalisation,
 // gates) writing the token inputs q, k, v, g, beta of M tokens.  hist_in and

@@ -59,6 +59,9 @@ __device__ __forceinline__ float silu(float x) {
 // of every value head.  Lane l owns channels 4l .. 4l+3 of its row.
 __global__ void __launch_bounds__(128)
     layer_prologue_kernel(const PrologueArgs P) {
+  // the state kernel that follows may start now: it loads the state (which
+  // this kernel never writes) and waits for these results before reading them
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const size_t gw = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int rows = 2 * P.kh + P.vh + 1;
@@ -132,10 +135,13 @@ __global__ void __launch_bounds__(128)
 // formula):  y = w * o / sqrt(mean(o^2) + eps) * silu(z).  Lane l owns
 // channels 4l .. 4l+3; the sum of squares is a fixed xor tree, so every lane
 // holds the same bits.  o is read with ordinary loads because y may be o.
+// Launched as a programmatic dependent of the previous kernel on the stream,
+// it waits for that kernel's results before touching any memory.
 __global__ void __launch_bounds__(256)
     gate_norm_kernel(const float *o, const float *__restrict__ z,
                      const float *__restrict__ w, float *y, float eps,
                      size_t rows) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const size_t row = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (row >= rows) return;
@@ -228,8 +234,16 @@ cudaError_t launch_gate_norm(const float *o, const float *z, const float *w,
   if (rows == 0) return cudaSuccess;
   const size_t blocks = (rows + 7) / 8;
   if (blocks > 0x7fffffffull) return cudaErrorInvalidConfiguration;
-  gate_norm_kernel<<<(unsigned)blocks, 256, 0, stream>>>(o, z, w, y, eps, rows);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gate_norm_kernel, o, z, w, y, eps, rows);
 }
 
 cudaError_t launch_hist_rollback(float *hist, const float *hist_snap,
