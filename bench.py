@@ -281,6 +281,62 @@ def tens_fn(torch, dev):
     return lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
 
+def layer_parts(torch, gdn, tens, stream, hbm_peak, parts, steps,
+                warmup=5):
+    """The layer core on 64 sequences x 48 heads, one token: prologue +
+    update (gdn_layer_step_m), then the same followed by the gated RMSNorm."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    L = gdn_inputs.make_layer_inputs(gdn_inputs.SEED_BASE + 100, B=64, T=1)
+    SL = [tens(L.S) for _ in range(NSETS)]
+    hL = [tens(L.hist), tens(L.hist)]
+    lx, lw, la, lb = (tens(t) for t in (L.x, L.conv_w, L.a, L.b))
+    lA, ldt = tens(L.A_log), tens(L.dt_bias)
+    lo = torch.empty(64, 1, 48, D, device=dev)
+
+    lws = torch.empty(gdn.gdn_layer_workspace(64, 16, 48, 1),
+                      dtype=torch.uint8, device=dev)
+
+    def lstep(i):
+        s_ = SL[i % NSETS]
+        gdn.gdn_layer_step_m(s_, s_, None, hL[i % 2], hL[(i + 1) % 2], lx,
+                             lw, la, lb, lA, ldt, lo, L.kh, lws,
+                             stream=stream)
+    for i in range(warmup):
+        lstep(i)
+    n = max(20, min(200, steps))
+    lms = time_launches(torch, lstep, n, stream)
+    conv_dim = 2 * 16 * D + 48 * D
+    lbytes = decode_bytes(64, 16, 48) + 64 * 4 * (conv_dim + 6 * conv_dim)
+    parts["layer_decode_b64"] = {
+        "ms": lms, "head_steps_per_s": 64 * 48 / (lms * 1e-3),
+        "gbs": lbytes / (lms * 1e-3) / 1e9,
+        "frac_of_measured_hbm": lbytes / (lms * 1e-3) / 1e9 / hbm_peak,
+        "bytes_per_launch": lbytes,
+        "note": "raw projections in: layer prologue (conv1d+SiLU with "
+                "history, q/k norm, gates) then the update, two launches"}
+    # the same, followed by the gated RMSNorm in place on o
+    _, zn, wn = gdn_inputs.make_gate_norm_inputs(
+        gdn_inputs.SEED_BASE + 101, 64, 1, 48)
+    lz, lwn = tens(zn), tens(wn)
+
+    def lnstep(i):
+        lstep(i)
+        gdn.gdn_gated_rmsnorm_m(lo, lz, lwn, lo, stream=stream)
+    for i in range(warmup):
+        lnstep(i)
+    lnms = time_launches(torch, lnstep, n, stream)
+    lnbytes = lbytes + 3 * 64 * 48 * D * 4
+    parts["layer_norm_decode_b64"] = {
+        "ms": lnms, "head_steps_per_s": 64 * 48 / (lnms * 1e-3),
+        "gbs": lnbytes / (lnms * 1e-3) / 1e9,
+        "frac_of_measured_hbm": lnbytes / (lnms * 1e-3) / 1e9 / hbm_peak,
+        "bytes_per_launch": lnbytes,
+        "note": "raw projections in, normalised output out: layer "
+                "prologue, update, gated RMSNorm in place; three launches"}
+    del SL, hL
+    torch.cuda.empty_cache()
+
+
 def prefill_parts(torch, gdn, tens, stream, peaks, parts):
     """Time the 8 x 4096-token prefill in its three precisions."""
     pin_ = gdn_inputs.make_workload("prefill_b8_t4096")
@@ -337,8 +393,9 @@ def main():
                     help="skip the verify / prefill sub-measurements")
     ap.add_argument("--no-cpu", action="store_true",
                     help="skip the CPU-baseline leg")
-    ap.add_argument("--only", choices=["prefill"], default=None,
-                    help="time only the prefill parts (used for profiling)")
+    ap.add_argument("--only", choices=["prefill", "layer"], default=None,
+                    help="time only the prefill or the layer parts (used "
+                         "for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -378,6 +435,12 @@ def main():
         prefill_parts(torch, gdn, tens_fn(torch, dev), stream, peaks, parts)
         print(json.dumps({"only": "prefill", "parts": parts}), flush=True)
         return 0
+    if args.only == "layer":
+        parts = {}
+        layer_parts(torch, gdn, tens_fn(torch, dev), stream, hbm_peak, parts,
+                    args.steps, max(5, args.warmup))
+        print(json.dumps({"only": "layer", "parts": parts}), flush=True)
+        return 0
 
     # ---- headline workload: batched decode step
     inp = gdn_inputs.make_workload("decode_b64")
@@ -407,17 +470,24 @@ def main():
     ms, _, value = aggregate(ms_local, heads_per_step, dist, dev)
     achieved_gbs = bytes_step / (ms_local * 1e-3) / 1e9
 
-    # ---- end to end through the public API with host buffers
-    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
-    h_in = [pin(x) for x in (inp.q, inp.k, inp.v, inp.g, inp.beta)]
-    d_in = [torch.empty_like(x, device=dev) for x in h_in]
+    # ---- end to end through the public API with host buffers: the step's
+    # inputs q | k | v | g | beta sit back to back in one pinned host buffer
+    # and go over in one copy; o comes back in one copy
+    parts_in = (inp.q, inp.k, inp.v, inp.g, inp.beta)
+    sizes = [x.size for x in parts_in]           # each a multiple of 4 floats
+    h_pack = torch.empty(sum(sizes), dtype=torch.float32).pin_memory()
+    d_pack = torch.empty(sum(sizes), dtype=torch.float32, device=dev)
+    d_in, off = [], 0
+    for x, n_ in zip(parts_in, sizes):
+        h_pack[off:off + n_] = torch.from_numpy(np.ascontiguousarray(x).ravel())
+        d_in.append(d_pack[off:off + n_].view(x.shape))
+        off += n_
     h_o = torch.empty(tuple(o.shape), dtype=torch.float32).pin_memory()
-    h2d = sum(x.numel() * 4 for x in h_in)
+    h2d = h_pack.numel() * 4
     d2h = h_o.numel() * 4
 
     def e2e_step(i):
-        for hx, dx in zip(h_in, d_in):
-            dx.copy_(hx, non_blocking=True)
+        d_pack.copy_(h_pack, non_blocking=True)
         gdn.gdn_step(states[i % NSETS], *d_in, o, stream=stream)
         h_o.copy_(o, non_blocking=True)
 
@@ -430,14 +500,35 @@ def main():
     e2e = {"value": e2e_value, "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "ms_per_step": ms_e2e,
-           "note": "q, k, v, g, beta copied from pinned host memory and o "
-                   "copied back every step; the recurrent state stays "
-                   "resident on the device"}
+           "note": "q, k, v, g, beta copied from one pinned host buffer "
+                   "(one copy) and o copied back (one copy) every step, "
+                   "serially with the step's kernel; the recurrent state "
+                   "stays resident on the device"}
 
     # ---- parts: verify launches and prefill (rank 0 only, N = 1 shapes)
     parts = {}
     launches = args.steps  # headline timed region: one kernel per step
     if not args.no_parts and rank == 0:
+        # reference point: a plain copy of the same 201 MB state (gdn_mark),
+        # same rotation of state sets, i.e. the same bytes as the headline
+        # step without its arithmetic and token inputs
+        snaps = [torch.empty_like(states[0]) for _ in range(NSETS)]
+
+        def cstep(i):
+            gdn.gdn_mark(states[i % NSETS], snaps[(i + 1) % NSETS], kh,
+                         stream=stream)
+        for i in range(5):
+            cstep(i)
+        cms = time_launches(torch, cstep, max(20, min(200, args.steps)), stream)
+        cbytes = 2 * states[0].numel() * 4
+        parts["state_copy_b64"] = {
+            "ms": cms, "gbs": cbytes / (cms * 1e-3) / 1e9,
+            "frac_of_measured_hbm": cbytes / (cms * 1e-3) / 1e9 / hbm_peak,
+            "bytes_per_launch": cbytes,
+            "note": "gdn_mark copy of the headline state (201.3 MB read + "
+                    "201.3 MB written): the practical ceiling for this size"}
+        del snaps
+        torch.cuda.empty_cache()
         del states
         torch.cuda.empty_cache()
         vin = gdn_inputs.make_workload("verify_b32")
@@ -465,56 +556,7 @@ def main():
                     "bytes_per_launch": nb}
         del Sv, ck
         torch.cuda.empty_cache()
-        # the fused layer core (conv1d + SiLU + q/k norm + gates + update)
-        L = gdn_inputs.make_layer_inputs(gdn_inputs.SEED_BASE + 100, B=64, T=1)
-        SL = [tens(L.S) for _ in range(NSETS)]
-        hL = [tens(L.hist), tens(L.hist)]
-        lx, lw, la, lb = (tens(t) for t in (L.x, L.conv_w, L.a, L.b))
-        lA, ldt = tens(L.A_log), tens(L.dt_bias)
-        lo = torch.empty(64, 1, 48, D, device=dev)
-
-        lws = torch.empty(gdn.gdn_layer_workspace(64, 16, 48, 1),
-                          dtype=torch.uint8, device=dev)
-
-        def lstep(i):
-            s_ = SL[i % NSETS]
-            gdn.gdn_layer_step_m(s_, s_, None, hL[i % 2], hL[(i + 1) % 2], lx,
-                                 lw, la, lb, lA, ldt, lo, L.kh, lws,
-                                 stream=stream)
-        for i in range(5):
-            lstep(i)
-        n = max(20, min(200, args.steps))
-        lms = time_launches(torch, lstep, n, stream)
-        conv_dim = 2 * 16 * D + 48 * D
-        lbytes = decode_bytes(64, 16, 48) + 64 * 4 * (conv_dim + 6 * conv_dim)
-        parts["layer_decode_b64"] = {
-            "ms": lms, "head_steps_per_s": 64 * 48 / (lms * 1e-3),
-            "gbs": lbytes / (lms * 1e-3) / 1e9,
-            "frac_of_measured_hbm": lbytes / (lms * 1e-3) / 1e9 / hbm_peak,
-            "bytes_per_launch": lbytes,
-            "note": "raw projections in: layer prologue (conv1d+SiLU with "
-                    "history, q/k norm, gates) then the update, two launches"}
-        # the same, followed by the gated RMSNorm in place on o
-        _, zn, wn = gdn_inputs.make_gate_norm_inputs(
-            gdn_inputs.SEED_BASE + 101, 64, 1, 48)
-        lz, lwn = tens(zn), tens(wn)
-
-        def lnstep(i):
-            lstep(i)
-            gdn.gdn_gated_rmsnorm_m(lo, lz, lwn, lo, stream=stream)
-        for i in range(5):
-            lnstep(i)
-        lnms = time_launches(torch, lnstep, n, stream)
-        lnbytes = lbytes + 3 * 64 * 48 * D * 4
-        parts["layer_norm_decode_b64"] = {
-            "ms": lnms, "head_steps_per_s": 64 * 48 / (lnms * 1e-3),
-            "gbs": lnbytes / (lnms * 1e-3) / 1e9,
-            "frac_of_measured_hbm": lnbytes / (lnms * 1e-3) / 1e9 / hbm_peak,
-            "bytes_per_launch": lnbytes,
-            "note": "raw projections in, normalised output out: layer "
-                    "prologue, update, gated RMSNorm in place; three launches"}
-        del SL, hL
-        torch.cuda.empty_cache()
+        layer_parts(torch, gdn, tens, stream, hbm_peak, parts, args.steps)
         prefill_parts(torch, gdn, tens, stream, peaks, parts)
 
     sampler.stop()
