@@ -348,11 +348,11 @@ def prefill_parts(torch, gdn, tens, stream, peaks, parts):
     toks = pin_.B * pin_.T
     flops = 7 * D * D * toks * pin_.vh
     # executed tensor-core flops of the chunked form per 64-token chunk
-    # and head: [K;Q]K^T 2*128*64*128, W^T and U^T 2*(2*128*64*64),
-    # S^T[W^T|(gQ)^T] 2*128*128*128, Delta^T P^T 2*128*64*64,
-    # Delta^T K~ 2*128*128*64
-    tc_flops = (2 * 128 * 64 * 128 + 4 * 128 * 64 * 64 +
-                2 * 128 * 128 * 128 + 2 * 128 * 64 * 64 +
+    # and head: [K;Q]K^T 2*128*64*128; S^T K^T and S^T Q^T 2*(2*128*64*128);
+    # U^T and Y (T diag(beta gamma))^T 2*(2*128*64*64); Delta^T P^T
+    # 2*128*64*64; Delta^T K~ 2*128*128*64
+    tc_flops = (2 * 128 * 64 * 128 + 4 * 128 * 64 * 128 +
+                4 * 128 * 64 * 64 + 2 * 128 * 64 * 64 +
                 2 * 128 * 128 * 64) * (pin_.T // 64) * pin_.B * pin_.vh
     for prec, name, reps in ((gdn.GDN_PREC_FP32, "fp32", 3),
                              (gdn.GDN_PREC_BF16X3, "bf16x3", 10),
@@ -360,7 +360,8 @@ def prefill_parts(torch, gdn, tens, stream, peaks, parts):
         def pstep(i, prec=prec):
             gdn.gdn_prefill(Sp, pq, pk, pv, pg, pb, po, precision=prec,
                             stream=stream)
-        pstep(0)
+        for i in range(3):
+            pstep(i)
         pms = time_launches(torch, pstep, reps, stream)
         entry = {
             "ms": pms, "tokens_per_s": toks / (pms * 1e-3),
@@ -430,16 +431,21 @@ def main():
         torch.cuda.synchronize()
 
 
-    if args.only == "prefill":
+    if args.only is not None:
         parts = {}
-        prefill_parts(torch, gdn, tens_fn(torch, dev), stream, peaks, parts)
-        print(json.dumps({"only": "prefill", "parts": parts}), flush=True)
-        return 0
-    if args.only == "layer":
-        parts = {}
-        layer_parts(torch, gdn, tens_fn(torch, dev), stream, hbm_peak, parts,
-                    args.steps, max(5, args.warmup))
-        print(json.dumps({"only": "layer", "parts": parts}), flush=True)
+        sampler = ClockSampler()
+        sampler.start()
+        time.sleep(0.3)
+        t0 = time.time()
+        if args.only == "prefill":
+            prefill_parts(torch, gdn, tens_fn(torch, dev), stream, peaks, parts)
+        else:
+            layer_parts(torch, gdn, tens_fn(torch, dev), stream, hbm_peak,
+                        parts, args.steps, max(5, args.warmup))
+        t1 = time.time()
+        sampler.stop()
+        print(json.dumps({"only": args.only, "parts": parts,
+                          "clocks": sampler.summary(t0, t1, None)}), flush=True)
         return 0
 
     # ---- headline workload: batched decode step

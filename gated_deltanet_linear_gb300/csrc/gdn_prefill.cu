@@ -15,19 +15,25 @@
 //
 // One CTA per (sequence, value head) walks the chunks in order; the fp32
 // state is kept transposed (S^T: one TMEM lane per value column dv, one
-// column per key row dk) in tensor memory for the whole sequence.  Per
-// chunk (D = M x N accumulator in TMEM, lanes = M):
+// column per key row dk) in tensor memory for the whole sequence.  Since
+// (W S)^T = S^T W^T = (S^T K^T) (T diag(beta gamma))^T, the two products
+// with the chunk-start state, Y = S^T K^T and (Q S)^T = S^T Q^T, need only
+// that state and the chunk's inputs: they are issued early and run under
+// the SIMT work on A and its inverse.  Per chunk (D = M x N accumulator in
+// TMEM, lanes = M):
 //   MMA-a  G,H  [t'][s]  = [K; Q] K^T                       (A, B K-major)
-//   SIMT   A from G; T = (I + A)^-1, blocked 16 x 16, fp32
-//   MMA-w  W^T  [dk][t]  = K^T (T diag(beta gamma))^T       (A = K, MN-major)
+//   SIMT   S^T operand from TMEM (under MMA-a)
+//   MMA-s  Y    [dv][t]  = S^T K^T;  (Q S)^T [dv][t] = S^T Q^T
+//   SIMT   o of the previous chunk;  A and P from G, H;
+//          T = (I + A)^-1, blocked 16 x 16, fp32 (under MMA-s)
 //   MMA-u  U^T  [dv][t]  = V^T (T diag(beta))^T             (A = V, MN-major)
-//   MMA-1  Delta^T = U^T - S^T W^T (negated A, accumulated onto U^T);
-//          (Q S)^T [dv][t] = S^T Q^T                        (B = W^T, MN-major)
-//   SIMT   Delta^T also scaled by w;  S^T *= gamma_63;  P (built with A)
+//   SIMT   Y operand from TMEM (under MMA-u)
+//   MMA-d  Delta^T = U^T - Y (T diag(beta gamma))^T   (negated A onto U^T)
+//   SIMT   Delta^T and Delta^T diag(w) operands;  S^T *= gamma_63
 //   MMA-3  (P Delta)^T = Delta^T P^T
 //   MMA-4  S^T += (Delta^T diag(w)) K                        (B = K, MN-major)
-//   SIMT   O^T = diag(gamma) (Q S)^T + (P Delta)^T  -> o, emitted while the
-//          next chunk's first product runs
+//   SIMT   O^T = diag(gamma) (Q S)^T + (P Delta)^T  -> o, emitted in the
+//          next chunk while its first products run
 // Every operand a thread writes is a row it owns (a row of an input, or a
 // TMEM lane of an earlier result), stored 8 elements at a time; transposes
 // happen in the MMA descriptors (MN-major operands), never in memory.  The
@@ -57,39 +63,45 @@ using namespace tc;
 
 constexpr int kC = 64;       // chunk length
 constexpr int kD = kDim;     // 128
-constexpr int kThreads = 256;
+constexpr int kSimt = 256;              // 8 SIMT warps
+constexpr int kIssuer = kSimt / 32;     // warp that issues the products
+constexpr int kLoader = kIssuer + 1;    // warp that copies the next K, Q
+constexpr int kThreads = kSimt + 64;
 
 // Operand tiles: R rows x C bf16 columns, 128-byte-swizzled blocks of 64
 // columns (see gdn_tc.cuh), hi tile followed by lo tile (R * C * 2 bytes
 // each).  Regions (byte offsets from a 1024-aligned base) are reused by
 // phase:
 //   Ra 64 KB: [K; Q] (128 x 128), the whole chunk
-//   Rb 32 KB: V (64 x 128)            -> Delta^T (128 x 64)
+//   Rb 32 KB: V (64 x 128)            -> Y (128 x 64) -> Delta^T (128 x 64)
 //   Rc 32 KB: A, T scratch (fp32)     -> T diag(bg), T diag(b) (64 x 64 each)
-//                                     -> W^T (128 x 64) -> Delta^T diag(w)
-//   Rd 64 KB: S^T (128 x 128)         -> P (64 x 64)
-constexpr uint32_t RA = 0, RB = 65536, RC = 98304, RD = 131072;
+//                                     -> Delta^T diag(w) (128 x 64)
+//   Rd 64 KB: S^T (128 x 128)         -> fp32 [K; Q] of the next chunk
+//   Rp 16 KB: P (64 x 64)
+constexpr uint32_t RA = 0, RB = 65536, RC = 98304, RD = 131072, RP = 196608;
 constexpr uint32_t OFF_KQ = RA;             // 128 x 128
 constexpr uint32_t OFF_V = RB;              // 64 x 128
-constexpr uint32_t OFF_DT = RB;             // 128 x 64 (after MMA-u)
+constexpr uint32_t OFF_Y = RB;              // 128 x 64 (after MMA-u)
+constexpr uint32_t OFF_DT = RB;             // 128 x 64 (after MMA-d)
 constexpr uint32_t OFF_SCR = RC;            // fp32 A [64][64] + T [64][64]
 constexpr uint32_t OFF_TB = RC;             // 64 x 64: T diag(beta gamma)
 constexpr uint32_t OFF_TB2 = RC + 16384;    // 64 x 64: T diag(beta)
-constexpr uint32_t OFF_WT = RC;             // 128 x 64 (after MMA-w/u)
-constexpr uint32_t OFF_DTW = RC;            // 128 x 64 (after MMA-1)
+constexpr uint32_t OFF_DTW = RC;            // 128 x 64 (after MMA-d)
 constexpr uint32_t OFF_ST = RD;             // 128 x 128
-constexpr uint32_t OFF_P = RD;              // 64 x 64 (after MMA-1)
-constexpr uint32_t OFF_VEC = RD + 65536;    // Gamma, gamma, w, beta, gamma x 2
-constexpr uint32_t OFF_BAR = OFF_VEC + 2048;
-constexpr uint32_t kSmemUsed = OFF_BAR + 64;
+constexpr uint32_t OFF_P = RP;              // 64 x 64
+constexpr uint32_t OFF_VEC = RP + 16384;    // Gamma, gamma, w, beta, gamma x 2
+constexpr uint32_t OFF_STAGE = RD;          // fp32 [K; Q] of the next chunk (64 KB)
+constexpr uint32_t OFF_BAR = OFF_VEC + 2048;  // 12 mbarriers
+constexpr uint32_t OFF_SLOT = OFF_BAR + 96;   // TMEM address
+constexpr uint32_t kSmemUsed = OFF_BAR + 128;
 constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;  // room to align the base
 
 // TMEM columns (512 allocated).
 constexpr uint32_t T_SACC = 0;    // S^T: lanes dv, 128 columns dk
-constexpr uint32_t T_GH = 128;    // G (lanes 0-63), H then P (lanes 64-127): 64 columns
-constexpr uint32_t T_W = 192;     // W^T: lanes dk, columns t
+constexpr uint32_t T_GH = 128;    // G (lanes 0-63), H (lanes 64-127): 64 columns
+constexpr uint32_t T_Y = 192;     // Y = S^T K^T: lanes dv, columns t
 constexpr uint32_t T_U = 256;     // U^T, then Delta^T = U^T - (W S)^T: lanes dv
-constexpr uint32_t T_QS = 384;    // (Q S)^T: lanes dv, columns t
+constexpr uint32_t T_QS = 320;    // (Q S)^T, two buffers (chunk parity): lanes dv
 constexpr uint32_t T_PD = 448;    // (P Delta)^T: lanes dv, columns t
 
 constexpr uint32_t kWaitLimit = 1u << 24;
@@ -148,24 +160,38 @@ struct Operand {
   bool mn;        // MN-major use
 };
 
-// D[M][N] (+)= A B^T over K = 16 * ksteps, issued by one thread.
-template <bool kLo>
+// Descriptor of K step 0 of the hi (lo = false) or lo tile of an operand.
+__device__ __forceinline__ uint64_t opdesc(const Operand &o, bool lo) {
+  const uint32_t base = o.base + (lo ? (uint32_t)(o.R * o.C * 2) : 0u);
+  return o.mn ? mnmajor(base, o.R, 0) : kmajor(base, o.R, 0);
+}
+
+// Start-address step of K step ks, in the descriptor's 16-byte units.  The
+// start address is the descriptor's low field (shared address >> 4, 14
+// bits; every tile lies below 256 KB), so the descriptor of K step ks is
+// the K-step-0 descriptor plus this constant.
+__device__ __forceinline__ uint32_t kstep16(const Operand &o, int ks) {
+  return o.mn ? (uint32_t)ks * (2048u >> 4)
+              : (uint32_t)(((ks >> 2) * o.R * 128 + (ks & 3) * 32) >> 4);
+}
+
+// D[M][N] (+)= A B^T over K = 16 * KSTEPS, issued by one thread.  The
+// descriptors are formed once and stepped by constants, so the issuing
+// thread spends its time on the MMAs rather than on descriptor arithmetic.
+template <bool kLo, int KSTEPS>
 __device__ __forceinline__ void gemm(uint32_t d, const Operand &a,
                                      const Operand &b, int M, int N,
-                                     int ksteps, bool accumulate,
-                                     bool negate_a = false) {
+                                     bool accumulate, bool negate_a = false) {
   const uint32_t id = idesc_bf16(M, N, a.mn, b.mn) | (negate_a ? (1u << 13) : 0u);
-  const uint32_t a_lo = a.base + (uint32_t)(a.R * a.C * 2);
-  const uint32_t b_lo = b.base + (uint32_t)(b.R * b.C * 2);
-  for (int ks = 0; ks < ksteps; ++ks) {
-    const uint64_t ah = a.mn ? mnmajor(a.base, a.R, ks) : kmajor(a.base, a.R, ks);
-    const uint64_t bh = b.mn ? mnmajor(b.base, b.R, ks) : kmajor(b.base, b.R, ks);
-    mma_bf16(d, ah, bh, id, (accumulate || ks > 0) ? 1u : 0u);
+  const uint64_t ah = opdesc(a, false), bh = opdesc(b, false);
+  const uint64_t al = kLo ? opdesc(a, true) : 0, bl = kLo ? opdesc(b, true) : 0;
+#pragma unroll
+  for (int ks = 0; ks < KSTEPS; ++ks) {
+    const uint64_t ao = kstep16(a, ks), bo = kstep16(b, ks);
+    mma_bf16(d, ah + ao, bh + bo, id, (accumulate || ks > 0) ? 1u : 0u);
     if (kLo) {
-      const uint64_t bl = b.mn ? mnmajor(b_lo, b.R, ks) : kmajor(b_lo, b.R, ks);
-      const uint64_t al = a.mn ? mnmajor(a_lo, a.R, ks) : kmajor(a_lo, a.R, ks);
-      mma_bf16(d, ah, bl, id, 1u);
-      mma_bf16(d, al, bh, id, 1u);
+      mma_bf16(d, ah + ao, bl + bo, id, 1u);
+      mma_bf16(d, al + ao, bh + bo, id, 1u);
     }
   }
 }
@@ -174,6 +200,60 @@ __device__ __forceinline__ void cta_sync_tc() {
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
+}
+
+// Barrier among the kSimt threads of the SIMT warps only (named barrier 1);
+// the issuing warp never takes part.
+__device__ __forceinline__ void simt_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kSimt) : "memory");
+}
+
+// simt_sync that also returns whether `p` holds on every SIMT thread.
+__device__ __forceinline__ bool simt_and(bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred a, b;\n\t"
+      "setp.ne.u32 a, %1, 0;\n\t"
+      "bar.red.and.pred b, 1, %2, a;\n\t"
+      "selp.u32 %0, 1, 0, b;\n\t}\n"
+      : "=r"(r)
+      : "r"((uint32_t)p), "n"(kSimt)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(mbar)
+               : "memory");
+}
+
+// A SIMT thread's part of "operands ready": its shared-memory writes made
+// visible to the tensor cores, its TMEM accesses ordered, then one arrival
+// (the barrier completes after all kSimt arrivals).
+__device__ __forceinline__ void signal_ready(uint32_t mbar) {
+  fence_proxy_async();
+  fence_before_sync();
+  mbar_arrive(mbar);
+}
+
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
+// global -> shared by the copy engine; its bytes count against the
+// mbarrier's expected transaction count.
+__device__ __forceinline__ void bulk_copy(uint32_t smem, const void *gmem,
+                                          uint32_t bytes, uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1], %2, [%3];" ::"r"(smem),
+      "l"(gmem), "r"(bytes), "r"(mbar)
+      : "memory");
+}
+
+// The one arrival of a phase, announcing `bytes` of bulk copies.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t mbar,
+                                                      uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar),
+               "r"(bytes)
+               : "memory");
 }
 
 // fp32 scratch for the triangular solve: A and T, 64 x 64 each, rows of 64
@@ -212,7 +292,7 @@ __device__ __forceinline__ void put_row4(float *X, int r, int c, float4 v) {
 // conquer: invert the four 16 x 16 diagonal blocks, merge them into 32 x 32
 // inverses, then into the 64 x 64 inverse, using
 //   [[E1, 0], [A21, E2]]^-1 = [[E1^-1, 0], [-E2^-1 A21 E1^-1, E2^-1]].
-// All 256 threads.  Reads the lower triangle of Asc; its upper triangle
+// The kSimt SIMT threads.  Reads the lower triangle of Asc; its upper triangle
 // (zero, never read as A) holds the intermediate products.  Writes Tsc.
 __device__ __forceinline__ void tri_inverse(float *Asc, float *Tsc, int tid) {
   // 1. Diagonal blocks by forward substitution: column j of block i on 4
@@ -238,7 +318,7 @@ __device__ __forceinline__ void tri_inverse(float *Asc, float *Tsc, int tid) {
     // zero the strictly-upper part of this column
     for (int r = q4; r < r0; r += 4) Tsc[sidx(r, r0 + jj)] = 0.f;
   }
-  __syncthreads();
+  simt_sync();
   // 2. 16 -> 32: blocks (1,0) and (3,2).  Thread: block pair p, row r,
   //    columns 4 c4 .. 4 c4 + 3.  X = A_{i,i-1} E_{i-1} goes to the upper
   //    block (i-1, i) of the A scratch.
@@ -248,7 +328,7 @@ __device__ __forceinline__ void tri_inverse(float *Asc, float *Tsc, int tid) {
     put_row4(Asc, 16 * j + r, 16 * i + c4,
              row_times(Asc, 16 * i + r, 16 * j, Tsc, 16 * j, 16 * j + c4, 16));
   }
-  __syncthreads();
+  simt_sync();
   if (tid < 128) {
     const int pr = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
     const int i = 2 * pr + 1, j = i - 1;
@@ -269,20 +349,20 @@ __device__ __forceinline__ void tri_inverse(float *Asc, float *Tsc, int tid) {
     }
     put_row4(Tsc, 16 * i + r, 16 * j + c4, make_float4(-y.x, -y.y, -y.z, -y.w));
   }
-  __syncthreads();
+  simt_sync();
   // 3. 32 -> 64: X = A[32:64, 0:32] T[0:32, 0:32] goes to A scratch
   //    [0:32, 32:64]; then T[32:64, 0:32] = -T[32:64, 32:64] X.
   {
     const int r = tid >> 3, c4 = (tid & 7) * 4;
     put_row4(Asc, r, 32 + c4, row_times(Asc, 32 + r, 0, Tsc, 0, c4, 32));
   }
-  __syncthreads();
+  simt_sync();
   {
     const int r = tid >> 3, c4 = (tid & 7) * 4;
     const float4 y = row_times(Tsc, 32 + r, 32, Asc, 0, 32 + c4, 32);
     put_row4(Tsc, 32 + r, c4, make_float4(-y.x, -y.y, -y.z, -y.w));
   }
-  __syncthreads();
+  simt_sync();
 }
 
 template <bool kLo>
@@ -301,15 +381,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   float *wv = Gam + 128;
   float *bet = Gam + 192;
   float *gam_o = Gam + 256;       // [2][64]: gamma of the chunk whose o is pending
+  const float *stage = reinterpret_cast<const float *>(gb + OFF_STAGE);
+  // mbarriers: products done (one commit each), operands ready (kSimt
+  // arrivals each), and the final drain
   const uint32_t bar0 = sb + OFF_BAR;
-  volatile uint32_t *slot = reinterpret_cast<volatile uint32_t *>(gb + OFF_BAR + 32);
+  const uint32_t done_a = bar0, done_s = bar0 + 8, done_d = bar0 + 16,
+                 done_4 = bar0 + 24;
+  const uint32_t rdy_a = bar0 + 32, rdy_s = bar0 + 40, rdy_t = bar0 + 48,
+                 rdy_y = bar0 + 56, rdy_d = bar0 + 64;
+  const uint32_t drain = bar0 + 72;
+  const uint32_t staged = bar0 + 80;  // next K, Q rows in the staging tile
+  const uint32_t done_u = bar0 + 88;
+  volatile uint32_t *slot = reinterpret_cast<volatile uint32_t *>(gb + OFF_SLOT);
   float *Asc = reinterpret_cast<float *>(gb + OFF_SCR);
   float *Tsc = Asc + 64 * 64;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int quad = warp & 3;      // TMEM lane quadrant of this warp
-  const int half = warp >> 2;     // which half of the columns this warp moves
+  const int half = (warp >> 2) & 1;  // which half of the columns this warp moves
   const int myrow = 32 * quad + lane;
   const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
 
@@ -318,296 +408,344 @@ __global__ void __launch_bounds__(kThreads, 1)
   const size_t head_off = (size_t)head * kD * kD;
   const int nchunks = (T + kC - 1) / kC;
 
-  const Operand opKQ{sb + OFF_KQ, 128, 128, false};   // MMA-a A
-  const Operand opKb{sb + OFF_KQ, 128, 128, false};   // MMA-a B (rows 0-63)
-  const Operand opKmn{sb + OFF_KQ, 128, 128, true};   // MMA-w A (rows 0-63)
-  const Operand opVmn{sb + OFF_V, 64, 128, true};     // MMA-u A
-  const Operand opTB{sb + OFF_TB, 64, 64, false};     // MMA-w B
-  const Operand opTB2{sb + OFF_TB2, 64, 64, false};   // MMA-u B
-  const Operand opST{sb + OFF_ST, 128, 128, false};   // MMA-1 A
-  const Operand opWT{sb + OFF_WT, 128, 64, true};     // MMA-1 B (W part)
-  const Operand opQb{sb + OFF_KQ + 64 * 128, 128, 128, false};  // MMA-1 B (Q rows)
-  const Operand opDT{sb + OFF_DT, 128, 64, false};    // MMA-3 A
-  const Operand opP{sb + OFF_P, 64, 64, false};       // MMA-3 B
-  const Operand opDTW{sb + OFF_DTW, 128, 64, false};  // MMA-4 A
-  const Operand opKnB{sb + OFF_KQ, 128, 128, true};   // MMA-4 B (K rows)
-
-  if (warp == 0) tmem_alloc(sb + OFF_BAR + 32, 512);
-  if (tid == 0)
+  if (warp == 0) tmem_alloc(sb + OFF_SLOT, 512);
+  if (tid == 0) {
     for (int i = 0; i < 4; ++i) mbar_init(bar0 + 8 * i, 1);
-  cta_sync_tc();
-  const uint32_t tmem = *slot;
-  const uint32_t tl = tmem + lane_base;
-
-  // Inputs of one chunk held in registers: rows (tid >> 4) + 16 i of
-  // [K; Q; V] (i = 0..11), columns (tid & 15) * 8 .. + 7; and, on warp 0,
-  // the gates of tokens lane and lane + 32.
-  float4 pre[24];
-  float pg[2], pb[2];
-  auto prefetch = [&](int c) {
-    const int t0 = c * kC;
-    const int n = min(kC, T - t0);
-    const size_t qk_base = ((size_t)b * T + t0) * kh + hh;
-    const size_t v_base = ((size_t)b * T + t0) * vh + vi;
-    const int c0 = (tid & 15) * 8;
-#pragma unroll
-    for (int i = 0; i < 12; ++i) {
-      const int row = (tid >> 4) + 16 * i;
-      const int t = row & (kC - 1);
-      const float *src = i < 4 ? k : (i < 8 ? q : v);
-      if (t < n) {
-        const size_t base = i < 8 ? (qk_base + (size_t)t * kh) * kD
-                                  : (v_base + (size_t)t * vh) * kD;
-        pre[2 * i] = __ldg(reinterpret_cast<const float4 *>(src + base + c0));
-        pre[2 * i + 1] = __ldg(reinterpret_cast<const float4 *>(src + base + c0 + 4));
-      } else {
-        pre[2 * i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        pre[2 * i + 1] = pre[2 * i];
-      }
-    }
-    if (warp == 0) {
-      pg[0] = lane < n ? __ldg(g + v_base + (size_t)lane * vh) : 0.f;
-      pg[1] = lane + 32 < n ? __ldg(g + v_base + (size_t)(lane + 32) * vh) : 0.f;
-      pb[0] = lane < n ? __ldg(beta + v_base + (size_t)lane * vh) : 0.f;
-      pb[1] = lane + 32 < n ? __ldg(beta + v_base + (size_t)(lane + 32) * vh) : 0.f;
-    }
-  };
-  prefetch(0);
-
-  // State in: S[dk][dv] -> TMEM lane dv, column dk.
-  {
-    const float *Sh = S + head_off;
-    for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
-      float r[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) r[j] = __ldg(Sh + (size_t)(c0 + j) * kD + myrow);
-      tmem_st16(tl + T_SACC + c0, r);
-    }
+    for (int i = 4; i < 9; ++i) mbar_init(bar0 + 8 * i, kSimt);
+    mbar_init(drain, 1);
+    mbar_init(staged, 1);
+    mbar_init(done_u, 1);
   }
   cta_sync_tc();
+  const uint32_t tmem = *slot;
 
-  // o for chunk cc = diag(gamma) (Q S)^T + (P Delta)^T, read from TMEM.
-  auto emit_o = [&](int cc) {
-    const int nn = min(kC, T - cc * kC);
-    const size_t vb = ((size_t)b * T + (size_t)cc * kC) * vh + vi;
-    const float *gm = gam_o + (cc & 1) * 64;
-    for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
-      float r[16], pd[16];
-      tmem_ld16(tl + T_QS + c0, r);
-      tmem_ld16(tl + T_PD + c0, pd);
-#pragma unroll
-      for (int jj = 0; jj < 16; ++jj) {
-        const int t = c0 + jj;
-        if (t < nn) o[(vb + (size_t)t * vh) * kD + myrow] = fmaf(gm[t], r[jj], pd[jj]);
+  if (warp == kLoader) {
+    // ------------------------------------------------ the copying warp
+    // K and Q rows of chunk c, fp32, into the staging tile [128 rows: K then
+    // Q][128] as soon as it is free: before the loop for chunk 0, else once
+    // MMA-s of chunk c-1 has consumed the S^T operand that shares its region
+    // (about two thirds of a chunk ahead of use).
+    // Each row is 512 contiguous bytes: one bulk copy; rows past T are
+    // zeroed with ordinary stores before the phase's single arrival.
+    int issued = -1;
+    for (int c = 0; c < nchunks; ++c) {
+      if (c > 0 && !mbar_wait(done_s, (uint32_t)((c - 1) & 1), kWaitLimit)) break;
+      const int t0 = c * kC;
+      const int n = min(kC, T - t0);
+      const size_t qk_base = ((size_t)b * T + t0) * kh + hh;
+      if (n < kC) {
+        for (int j = lane; j < 2 * (kC - n) * 32; j += 32) {
+          const int rr = j >> 5, ch = j & 31;
+          const int row = (rr < kC - n ? 0 : kC) + n + (rr % (kC - n));
+          *reinterpret_cast<float4 *>(gb + OFF_STAGE + row * 512 + ch * 16) =
+              make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        __syncwarp();
       }
+      if (lane == 0) mbar_arrive_expect_tx(staged, (uint32_t)(2 * n * 512));
+      __syncwarp();
+      for (int row = lane; row < 2 * kC; row += 32) {
+        const int t = row & (kC - 1);
+        if (t < n)
+          bulk_copy(sb + OFF_STAGE + (uint32_t)(row * 512),
+                    (row < kC ? k : q) + (qk_base + (size_t)t * kh) * kD, 512u,
+                    staged);
+      }
+      issued = c;
     }
-  };
+    // nothing may still be copying into shared memory when the CTA ends
+    if (issued >= 0) mbar_wait(staged, (uint32_t)(issued & 1), kWaitLimit);
+  } else if (warp == kIssuer) {
+    // ------------------------------------------------ the issuing warp
+    // One thread issues every product of every chunk as soon as the SIMT
+    // warps report its operands ready; tcgen05.mma issue waits while the
+    // tensor pipe is busy, and here that wait holds up no SIMT work.
+    if (lane == 0) {
+      const Operand opKQ{sb + OFF_KQ, 128, 128, false};   // MMA-a A
+      const Operand opKb{sb + OFF_KQ, 128, 128, false};   // MMA-a, MMA-s B (rows 0-63)
+      const Operand opVmn{sb + OFF_V, 64, 128, true};     // MMA-u A
+      const Operand opTB{sb + OFF_TB, 64, 64, false};     // MMA-d B
+      const Operand opTB2{sb + OFF_TB2, 64, 64, false};   // MMA-u B
+      const Operand opST{sb + OFF_ST, 128, 128, false};   // MMA-s A
+      const Operand opY{sb + OFF_Y, 128, 64, false};      // MMA-d A
+      const Operand opQb{sb + OFF_KQ + 64 * 128, 128, 128, false};  // MMA-s B (Q rows)
+      const Operand opDT{sb + OFF_DT, 128, 64, false};    // MMA-3 A
+      const Operand opP{sb + OFF_P, 64, 64, false};       // MMA-3 B
+      const Operand opDTW{sb + OFF_DTW, 128, 64, false};  // MMA-4 A
+      const Operand opKnB{sb + OFF_KQ, 128, 128, true};   // MMA-4 B (K rows)
+      uint32_t ph = 0;
+      for (int c = 0; c < nchunks; ++c) {
+        if (!mbar_wait(rdy_a, ph, kWaitLimit)) break;
+        fence_after_sync();
+        gemm<kLo, kD / 16>(tmem + T_GH, opKQ, opKb, 128, kC, false);
+        commit(done_a);
+        if (!mbar_wait(rdy_s, ph, kWaitLimit)) break;
+        fence_after_sync();
+        gemm<kLo, kD / 16>(tmem + T_Y, opST, opKb, 128, kC, false);
+        gemm<kLo, kD / 16>(tmem + T_QS + 64u * (uint32_t)(c & 1), opST, opQb,
+                           128, kC, false);
+        commit(done_s);
+        if (!mbar_wait(rdy_t, ph, kWaitLimit)) break;
+        fence_after_sync();
+        gemm<kLo, kC / 16>(tmem + T_U, opVmn, opTB2, 128, kC, false);
+        commit(done_u);  // V's region then takes the Y operand
+        if (!mbar_wait(rdy_y, ph, kWaitLimit)) break;
+        fence_after_sync();
+        gemm<kLo, kC / 16>(tmem + T_U, opY, opTB, 128, kC, true, true);
+        commit(done_d);
+        if (!mbar_wait(rdy_d, ph, kWaitLimit)) break;
+        fence_after_sync();
+        gemm<kLo, kC / 16>(tmem + T_PD, opDT, opP, 128, kC, false);
+        gemm<kLo, kC / 16>(tmem + T_SACC, opDTW, opKnB, 128, kD, true);
+        commit(done_4);
+        ph ^= 1u;
+      }
+      commit(drain);  // arrives once every product issued above is done
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ the SIMT warps
+    const uint32_t tl = tmem + lane_base;
 
-  uint32_t parity = 0;
-  bool failed = false;
-  for (int c = 0; c < nchunks; ++c) {
-    // ------------------------------------------ phase 0: inputs, S^T operand
-    if (warp == 0) {
-      bet[lane] = pb[0];
-      bet[lane + 32] = pb[1];
-      float sa = pg[0], sc = pg[1];
+    // Next chunk's V rows (tid >> 4) + 16 i, i = 0..3, columns
+    // (tid & 15) * 8 .. + 7 in registers; on warp 0, the gates of tokens
+    // lane and lane + 32.  (K and Q come through the staging tile.)
+    float4 pv[8];
+    float pg[2], pb[2];
+    auto prefetch = [&](int c) {
+      const int t0 = c * kC;
+      const int n = min(kC, T - t0);
+      const size_t v_base = ((size_t)b * T + t0) * vh + vi;
+      const int c0 = (tid & 15) * 8;
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const float ya = __shfl_up_sync(0xffffffffu, sa, off);
-        const float yc = __shfl_up_sync(0xffffffffu, sc, off);
-        if (lane >= off) {
-          sa += ya;
-          sc += yc;
+      for (int i = 0; i < 4; ++i) {
+        const int t = (tid >> 4) + 16 * i;
+        if (t < n) {
+          const float *src = v + (v_base + (size_t)t * vh) * kD + c0;
+          pv[2 * i] = __ldg(reinterpret_cast<const float4 *>(src));
+          pv[2 * i + 1] = __ldg(reinterpret_cast<const float4 *>(src + 4));
+        } else {
+          pv[2 * i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          pv[2 * i + 1] = pv[2 * i];
         }
       }
-      sc += __shfl_sync(0xffffffffu, sa, 31);
-      const float last = __shfl_sync(0xffffffffu, sc, 31);
-      Gam[lane] = sa;
-      Gam[lane + 32] = sc;
-      gam[lane] = expf(sa);
-      gam[lane + 32] = expf(sc);
-      gam_o[(c & 1) * 64 + lane] = gam[lane];
-      gam_o[(c & 1) * 64 + lane + 32] = gam[lane + 32];
-      wv[lane] = expf(last - sa);
-      wv[lane + 32] = expf(last - sc);
-    }
-    // [K; Q] rows and V rows from the prefetched registers.
-#pragma unroll
-    for (int i = 0; i < 12; ++i) {
-      const int row = (tid >> 4) + 16 * i, c0 = (tid & 15) * 8;
-      const float x[8] = {pre[2 * i].x, pre[2 * i].y, pre[2 * i].z, pre[2 * i].w,
-                          pre[2 * i + 1].x, pre[2 * i + 1].y, pre[2 * i + 1].z,
-                          pre[2 * i + 1].w};
-      if (i < 8)
-        put8<kLo>(gb, OFF_KQ, 128, 128, row, c0, x);
-      else
-        put8<kLo>(gb, OFF_V, 64, 128, row & (kC - 1), c0, x);
-    }
-    // S^T operand (rows dv, columns dk) from the TMEM master copy.
-    for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
-      float r[16];
-      tmem_ld16(tl + T_SACC + c0, r);
-      put8<kLo>(gb, OFF_ST, 128, 128, myrow, c0, r);
-      put8<kLo>(gb, OFF_ST, 128, 128, myrow, c0 + 8, r + 8);
-    }
-    fence_proxy_async();
-    cta_sync_tc();
+      if (warp == 0) {
+        pg[0] = lane < n ? __ldg(g + v_base + (size_t)lane * vh) : 0.f;
+        pg[1] = lane + 32 < n ? __ldg(g + v_base + (size_t)(lane + 32) * vh) : 0.f;
+        pb[0] = lane < n ? __ldg(beta + v_base + (size_t)lane * vh) : 0.f;
+        pb[1] = lane + 32 < n ? __ldg(beta + v_base + (size_t)(lane + 32) * vh) : 0.f;
+      }
+    };
+    prefetch(0);
 
-    // --------------------------------------- phase 1: G, H = [K;Q] K^T
-    if (tid == 0) {
-      gemm<kLo>(tmem + T_GH, opKQ, opKb, 128, kC, kD / 16, false);
-      commit(bar0);
-    }
-    if (c > 0) emit_o(c - 1);  // the previous chunk's output, under this product
-    if (!__syncthreads_and(mbar_wait(bar0, parity, kWaitLimit))) { failed = true; break; }
-    fence_after_sync();
-
-    // -------------------------- phase 2: A, T = (I + A)^-1, T diag operands
-    if (quad < 2) {  // lanes 0-63 hold G rows t
-      const int t = myrow;
-      const float bt = bet[t], Gt = Gam[t];
-      for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
+    // State in: S[dk][dv] -> TMEM lane dv, column dk.
+    {
+      const float *Sh = S + head_off;
+      for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
         float r[16];
-        tmem_ld16(tl + T_GH + c0, r);
 #pragma unroll
-        for (int j4 = 0; j4 < 4; ++j4) {
-          float4 a4;
-          float *a = &a4.x;
+        for (int j = 0; j < 16; ++j) r[j] = __ldg(Sh + (size_t)(c0 + j) * kD + myrow);
+        tmem_st16(tl + T_SACC + c0, r);
+      }
+    }
+
+    // o for chunk cc = diag(gamma) (Q S)^T + (P Delta)^T, read from TMEM.
+    auto emit_o = [&](int cc) {
+      const int nn = min(kC, T - cc * kC);
+      const size_t vb = ((size_t)b * T + (size_t)cc * kC) * vh + vi;
+      const float *gm = gam_o + (cc & 1) * 64;
+      const uint32_t qs = T_QS + 64u * (uint32_t)(cc & 1);
+      for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
+        float r[16], pd[16];
+        tmem_ld16(tl + qs + c0, r);
+        tmem_ld16(tl + T_PD + c0, pd);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int s = c0 + 4 * j4 + e;
-            a[e] = s < t ? bt * expf(Gt - Gam[s]) * r[4 * j4 + e] : 0.f;
+        for (int jj = 0; jj < 16; ++jj) {
+          const int t = c0 + jj;
+          if (t < nn) o[(vb + (size_t)t * vh) * kD + myrow] = fmaf(gm[t], r[jj], pd[jj]);
+        }
+      }
+    };
+
+    uint32_t parity = 0;
+    bool failed = false;
+    for (int c = 0; c < nchunks; ++c) {
+      // ---------------------------------------------------- phase 0: inputs
+      if (warp == 0) {
+        bet[lane] = pb[0];
+        bet[lane + 32] = pb[1];
+        float sa = pg[0], sc = pg[1];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const float ya = __shfl_up_sync(0xffffffffu, sa, off);
+          const float yc = __shfl_up_sync(0xffffffffu, sc, off);
+          if (lane >= off) {
+            sa += ya;
+            sc += yc;
           }
-          *reinterpret_cast<float4 *>(Asc + sidx(t, c0 + 4 * j4)) = a4;
+        }
+        sc += __shfl_sync(0xffffffffu, sa, 31);
+        const float last = __shfl_sync(0xffffffffu, sc, 31);
+        Gam[lane] = sa;
+        Gam[lane + 32] = sc;
+        gam[lane] = expf(sa);
+        gam[lane + 32] = expf(sc);
+        gam_o[(c & 1) * 64 + lane] = gam[lane];
+        gam_o[(c & 1) * 64 + lane + 32] = gam[lane + 32];
+        wv[lane] = expf(last - sa);
+        wv[lane + 32] = expf(last - sc);
+      }
+      // this chunk's K and Q rows are in the staging tile (and the gates above
+      // are visible: the wait is also a SIMT barrier)
+      if (!simt_and(mbar_wait(staged, parity, kWaitLimit))) { failed = true; break; }
+      // [K; Q] operand rows from the staging tile, V rows from registers.
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int row = (tid >> 4) + 16 * i, c0 = (tid & 15) * 8;
+        const float4 x0 = *reinterpret_cast<const float4 *>(stage + row * 128 + c0);
+        const float4 x1 = *reinterpret_cast<const float4 *>(stage + row * 128 + c0 + 4);
+        const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        put8<kLo>(gb, OFF_KQ, 128, 128, row, c0, x);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int row = (tid >> 4) + 16 * i, c0 = (tid & 15) * 8;
+        const float x[8] = {pv[2 * i].x, pv[2 * i].y, pv[2 * i].z, pv[2 * i].w,
+                            pv[2 * i + 1].x, pv[2 * i + 1].y, pv[2 * i + 1].z,
+                            pv[2 * i + 1].w};
+        put8<kLo>(gb, OFF_V, 64, 128, row, c0, x);
+      }
+      signal_ready(rdy_a);  // -> MMA-a: G, H = [K; Q] K^T
+      simt_sync();          // the staging tile is read; its region is reused
+
+      // ------------- phase 1: S^T operand (rows dv, columns dk) from TMEM
+      for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
+        float r[16];
+        tmem_ld16(tl + T_SACC + c0, r);
+        put8<kLo>(gb, OFF_ST, 128, 128, myrow, c0, r);
+        put8<kLo>(gb, OFF_ST, 128, 128, myrow, c0 + 8, r + 8);
+      }
+      signal_ready(rdy_s);  // -> MMA-s: Y = S^T K^T, (Q S)^T = S^T Q^T
+      if (c > 0) emit_o(c - 1);  // the previous chunk's output
+      if (!simt_and(mbar_wait(done_a, parity, kWaitLimit))) { failed = true; break; }
+      fence_after_sync();
+
+      // ----------------- phase 2: A and P, T = (I + A)^-1, T diag operands
+      if (quad < 2) {  // lanes 0-63 hold G rows t
+        const int t = myrow;
+        const float bt = bet[t], Gt = Gam[t];
+        for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
+          float r[16];
+          tmem_ld16(tl + T_GH + c0, r);
+#pragma unroll
+          for (int j4 = 0; j4 < 4; ++j4) {
+            float4 a4;
+            float *a = &a4.x;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int s = c0 + 4 * j4 + e;
+              a[e] = s < t ? bt * expf(Gt - Gam[s]) * r[4 * j4 + e] : 0.f;
+            }
+            *reinterpret_cast<float4 *>(Asc + sidx(t, c0 + 4 * j4)) = a4;
+          }
+        }
+      } else {  // lanes 64-127 hold H rows t: P straight to its operand
+        const int t = myrow - kC;
+        const float Gt = Gam[t];
+        for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
+          float r[16];
+          tmem_ld16(tl + T_GH + c0, r);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int s = c0 + e;
+            r[e] = s <= t ? expf(Gt - Gam[s]) * r[e] : 0.f;
+          }
+          put8<kLo>(gb, OFF_P, kC, kC, t, c0, r);
+          put8<kLo>(gb, OFF_P, kC, kC, t, c0 + 8, r + 8);
         }
       }
-    }
-    if (quad >= 2) {  // lanes 64-127 hold H rows t: P in place of H
-      const int t = myrow - kC;
-      const float Gt = Gam[t];
+      simt_sync();
+      tri_inverse(Asc, Tsc, tid);
+      {
+        // each thread takes one row-half of T: row t = tid >> 2, 16 columns
+        const int t = tid >> 2, cq = (tid & 3) * 16;
+        float tr[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) tr[e] = Tsc[sidx(t, cq + e)];
+        simt_sync();  // everyone holds its T values; scratch may be reused
+        float x1[8], x2[8];
+#pragma unroll
+        for (int h8 = 0; h8 < 2; ++h8) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int s = cq + 8 * h8 + e;
+            x1[e] = tr[8 * h8 + e] * bet[s] * gam[s];
+            x2[e] = tr[8 * h8 + e] * bet[s];
+          }
+          put8<kLo>(gb, OFF_TB, kC, kC, t, cq + 8 * h8, x1);
+          put8<kLo>(gb, OFF_TB2, kC, kC, t, cq + 8 * h8, x2);
+        }
+      }
+      signal_ready(rdy_t);  // -> MMA-u: U^T = V^T (T diag(beta))^T
+
+      // -------------------------------- phase 3: Y operand (lane dv, cols t)
+      if (!simt_and(mbar_wait(done_s, parity, kWaitLimit) &&
+                    mbar_wait(done_u, parity, kWaitLimit))) { failed = true; break; }
+      fence_after_sync();
       for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
         float r[16];
-        tmem_ld16(tl + T_GH + c0, r);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int s = c0 + e;
-          r[e] = s <= t ? expf(Gt - Gam[s]) * r[e] : 0.f;
-        }
-        tmem_st16(tl + T_GH + c0, r);
+        tmem_ld16(tl + T_Y + c0, r);
+        put8<kLo>(gb, OFF_Y, 128, kC, myrow, c0, r);
+        put8<kLo>(gb, OFF_Y, 128, kC, myrow, c0 + 8, r + 8);
       }
-    }
-    __syncthreads();
-    tri_inverse(Asc, Tsc, tid);
-    {
-      // each thread takes one row-half of T: row t = tid >> 2, 16 columns
-      const int t = tid >> 2, cq = (tid & 3) * 16;
-      float tr[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) tr[e] = Tsc[sidx(t, cq + e)];
-      __syncthreads();  // everyone holds its T values; scratch may be reused
-      float x1[8], x2[8];
-#pragma unroll
-      for (int h8 = 0; h8 < 2; ++h8) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int s = cq + 8 * h8 + e;
-          x1[e] = tr[8 * h8 + e] * bet[s] * gam[s];
-          x2[e] = tr[8 * h8 + e] * bet[s];
-        }
-        put8<kLo>(gb, OFF_TB, kC, kC, t, cq + 8 * h8, x1);
-        put8<kLo>(gb, OFF_TB2, kC, kC, t, cq + 8 * h8, x2);
-      }
-    }
-    fence_proxy_async();
-    cta_sync_tc();
+      signal_ready(rdy_y);  // -> MMA-d: Delta^T = U^T - Y (T diag(beta gamma))^T
+      if (!simt_and(mbar_wait(done_d, parity, kWaitLimit))) { failed = true; break; }
+      fence_after_sync();
+      if (c + 1 < nchunks) prefetch(c + 1);  // lands under the work below
 
-    // ------------------------------------------------ phase 3: W^T, U^T
-    if (tid == 0) {
-      gemm<kLo>(tmem + T_W, opKmn, opTB, 128, kC, kC / 16, false);
-      gemm<kLo>(tmem + T_U, opVmn, opTB2, 128, kC, kC / 16, false);
-      commit(bar0 + 8);
-    }
-    if (!__syncthreads_and(mbar_wait(bar0 + 8, parity, kWaitLimit))) { failed = true; break; }
-    fence_after_sync();
-
-    // ------------------------------------------- phase 4: W^T operand
-    for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
-      float r[16];
-      tmem_ld16(tl + T_W + c0, r);  // lane dk, columns t
-      put8<kLo>(gb, OFF_WT, 128, kC, myrow, c0, r);
-      put8<kLo>(gb, OFF_WT, 128, kC, myrow, c0 + 8, r + 8);
-    }
-    fence_proxy_async();
-    cta_sync_tc();
-
-    // ----------------------------- phase 5: (W S)^T, (Q S)^T = S^T [W^T | Q^T]
-    if (tid == 0) {
-      gemm<kLo>(tmem + T_U, opST, opWT, 128, kC, kD / 16, true, true);
-      gemm<kLo>(tmem + T_QS, opST, opQb, 128, kC, kD / 16, false);
-      commit(bar0 + 16);
-    }
-    if (!__syncthreads_and(mbar_wait(bar0 + 16, parity, kWaitLimit))) { failed = true; break; }
-    fence_after_sync();
-
-    // ---- phase 6: Delta^T = U^T - (W S)^T, Delta^T diag(w); P; S^T *= gamma_63
-    for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
-      float u[16];
-      tmem_ld16(tl + T_U + c0, u);  // Delta^T = U^T - (W S)^T
-      put8<kLo>(gb, OFF_DT, 128, kC, myrow, c0, u);
-      put8<kLo>(gb, OFF_DT, 128, kC, myrow, c0 + 8, u + 8);
-#pragma unroll
-      for (int e = 0; e < 16; ++e) u[e] *= wv[c0 + e];
-      put8<kLo>(gb, OFF_DTW, 128, kC, myrow, c0, u);
-      put8<kLo>(gb, OFF_DTW, 128, kC, myrow, c0 + 8, u + 8);
-    }
-    if (quad >= 2) {  // lanes 64-127 hold P rows t (built in phase 2)
-      const int t = myrow - kC;
+      // ------ phase 4: Delta^T, Delta^T diag(w) operands; S^T *= gamma_63
       for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
-        float r[16];
-        tmem_ld16(tl + T_GH + c0, r);
-        put8<kLo>(gb, OFF_P, kC, kC, t, c0, r);
-        put8<kLo>(gb, OFF_P, kC, kC, t, c0 + 8, r + 8);
+        float u[16];
+        tmem_ld16(tl + T_U + c0, u);
+        put8<kLo>(gb, OFF_DT, 128, kC, myrow, c0, u);
+        put8<kLo>(gb, OFF_DT, 128, kC, myrow, c0 + 8, u + 8);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) u[e] *= wv[c0 + e];
+        put8<kLo>(gb, OFF_DTW, 128, kC, myrow, c0, u);
+        put8<kLo>(gb, OFF_DTW, 128, kC, myrow, c0 + 8, u + 8);
       }
+      {
+        const float gC = gam[kC - 1];
+        for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
+          float r[16];
+          tmem_ld16(tl + T_SACC + c0, r);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) r[j] *= gC;
+          tmem_st16(tl + T_SACC + c0, r);
+        }
+      }
+      signal_ready(rdy_d);  // -> MMA-3: (P Delta)^T;  MMA-4: S^T += ...
+      if (!simt_and(mbar_wait(done_4, parity, kWaitLimit))) { failed = true; break; }
+      fence_after_sync();
+      parity ^= 1u;
     }
-    {
-      const float gC = gam[kC - 1];
+
+    if (!failed) {
+      emit_o(nchunks - 1);
+      float *Sh = S + head_off;
       for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
         float r[16];
         tmem_ld16(tl + T_SACC + c0, r);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) r[j] *= gC;
-        tmem_st16(tl + T_SACC + c0, r);
+        for (int j = 0; j < 16; ++j) Sh[(size_t)(c0 + j) * kD + myrow] = r[j];
       }
+    } else if (tid == 0) {
+      atomicAdd(&g_prefill_timeouts, 1u);
     }
-    fence_proxy_async();
-    cta_sync_tc();
-
-    // ---------- phase 7: (P Delta)^T = Delta^T P^T; S^T += Delta^T diag(w) K
-    if (tid == 0) {
-      gemm<kLo>(tmem + T_PD, opDT, opP, 128, kC, kC / 16, false);
-      gemm<kLo>(tmem + T_SACC, opDTW, opKnB, 128, kD, kC / 16, true);
-      commit(bar0 + 24);
-    }
-    if (c + 1 < nchunks) prefetch(c + 1);  // overlaps the products above
-    if (!__syncthreads_and(mbar_wait(bar0 + 24, parity, kWaitLimit))) { failed = true; break; }
-    fence_after_sync();
-
-    cta_sync_tc();
-    parity ^= 1u;
   }
-
-  if (!failed) {
-    emit_o(nchunks - 1);
-    float *Sh = S + head_off;
-    for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
-      float r[16];
-      tmem_ld16(tl + T_SACC + c0, r);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) Sh[(size_t)(c0 + j) * kD + myrow] = r[j];
-    }
-  } else if (tid == 0) {
-    atomicAdd(&g_prefill_timeouts, 1u);
-  }
+  // every product issued has finished (bounded: after a timeout the issuer
+  // stops early and its drain commit still arrives)
+  mbar_wait(drain, 0, kWaitLimit);
   cta_sync_tc();
   if (warp == 0) tmem_dealloc(tmem, 512);
 }

@@ -180,7 +180,11 @@ size_t gdn_prefill_workspace(const gdn_shape *shape, int T, int chunk,
  *   GPU", section 4; the articles themselves never use it ("34 · batched M
  *   rows", section 3.6).  Needs no workspace (gdn_prefill_workspace returns
  *   0; pass NULL, 0).  Results agree with the token-serial definition to
- *   the stated relative error, not bitwise.
+ *   the stated relative error, not bitwise.  The chunked form works with
+ *   differences of cumulative sums of g, so every g must be finite there
+ *   (a decay that empties the state is any g below about -104, where
+ *   exp(g) is 0 in fp32; g = -inf would give NaN).  The token-serial path
+ *   also accepts g = -inf.
  * 1 <= T <= GDN_MAX_TOKENS.  Other precision values give GDN_ERANGE.
  */
 int gdn_prefill(const gdn_shape *shape, int T, float *S, const float *q,
