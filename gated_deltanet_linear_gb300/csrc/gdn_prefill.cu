@@ -89,10 +89,10 @@ constexpr uint32_t OFF_TB2 = RC + 16384;    // 64 x 64: T diag(beta)
 constexpr uint32_t OFF_DTW = RC;            // 128 x 64 (after MMA-d)
 constexpr uint32_t OFF_ST = RD;             // 128 x 128
 constexpr uint32_t OFF_P = RP;              // 64 x 64
-constexpr uint32_t OFF_VEC = RP + 16384;    // Gamma, gamma, w, beta, gamma x 2
+constexpr uint32_t OFF_VEC = RP + 16384;    // Gamma, gamma, w, beta, gamma x 2, ea, eb
 constexpr uint32_t OFF_STAGE = RD;          // fp32 [K; Q] of the next chunk (64 KB)
 constexpr uint32_t OFF_BAR = OFF_VEC + 2048;  // 12 mbarriers
-constexpr uint32_t OFF_SLOT = OFF_BAR + 96;   // TMEM address
+constexpr uint32_t OFF_SLOT = OFF_BAR + 96;   // TMEM address; +104: int flag
 constexpr uint32_t kSmemUsed = OFF_BAR + 128;
 constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;  // room to align the base
 
@@ -381,6 +381,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   float *wv = Gam + 128;
   float *bet = Gam + 192;
   float *gam_o = Gam + 256;       // [2][64]: gamma of the chunk whose o is pending
+  // exp(Gamma_t - Gamma_s) = ea[t] eb[s] about the middle of the chunk's
+  // range of Gamma; used when that range is at most 160 (*fac != 0), where
+  // every factor is a normal fp32 number
+  float *ea = Gam + 384;
+  float *eb = Gam + 448;
+  volatile int *fac = reinterpret_cast<volatile int *>(gb + OFF_BAR + 104);
   const float *stage = reinterpret_cast<const float *>(gb + OFF_STAGE);
   // mbarriers: products done (one commit each), operands ready (kSimt
   // arrivals each), and the final drain
@@ -594,11 +600,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         gam_o[(c & 1) * 64 + lane + 32] = gam[lane + 32];
         wv[lane] = expf(last - sa);
         wv[lane + 32] = expf(last - sc);
+        float gmax = fmaxf(sa, sc), gmin = fminf(sa, sc);
+#pragma unroll
+        for (int off = 16; off; off >>= 1) {
+          gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, off));
+          gmin = fminf(gmin, __shfl_xor_sync(0xffffffffu, gmin, off));
+        }
+        const float ref = 0.5f * (gmax + gmin);
+        ea[lane] = expf(sa - ref);
+        ea[lane + 32] = expf(sc - ref);
+        eb[lane] = expf(ref - sa);
+        eb[lane + 32] = expf(ref - sc);
+        if (lane == 0) *fac = (gmax - gmin <= 160.f) ? 1 : 0;
       }
       // this chunk's K and Q rows are in the staging tile (and the gates above
       // are visible: the wait is also a SIMT barrier)
       if (!simt_and(mbar_wait(staged, parity, kWaitLimit))) { failed = true; break; }
-      // [K; Q] operand rows from the staging tile, V rows from registers.
+      // [K; Q] operand rows from the staging tile.
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int row = (tid >> 4) + 16 * i, c0 = (tid & 15) * 8;
@@ -607,6 +625,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
         put8<kLo>(gb, OFF_KQ, 128, 128, row, c0, x);
       }
+      signal_ready(rdy_a);  // -> MMA-a: G, H = [K; Q] K^T
+      // V operand rows from registers (needed from MMA-u on)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int row = (tid >> 4) + 16 * i, c0 = (tid & 15) * 8;
@@ -615,7 +635,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                             pv[2 * i + 1].w};
         put8<kLo>(gb, OFF_V, 64, 128, row, c0, x);
       }
-      signal_ready(rdy_a);  // -> MMA-a: G, H = [K; Q] K^T
       simt_sync();          // the staging tile is read; its region is reused
 
       // ------------- phase 1: S^T operand (rows dv, columns dk) from TMEM
@@ -631,9 +650,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_after_sync();
 
       // ----------------- phase 2: A and P, T = (I + A)^-1, T diag operands
+      const bool factored = *fac != 0;
       if (quad < 2) {  // lanes 0-63 hold G rows t
         const int t = myrow;
-        const float bt = bet[t], Gt = Gam[t];
+        const float bt = bet[t], Gt = Gam[t], bea = bt * ea[t];
         for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
           float r[16];
           tmem_ld16(tl + T_GH + c0, r);
@@ -641,24 +661,40 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j4 = 0; j4 < 4; ++j4) {
             float4 a4;
             float *a = &a4.x;
+            if (factored) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int s = c0 + 4 * j4 + e;
-              a[e] = s < t ? bt * expf(Gt - Gam[s]) * r[4 * j4 + e] : 0.f;
+              for (int e = 0; e < 4; ++e) {
+                const int s = c0 + 4 * j4 + e;
+                a[e] = s < t ? bea * eb[s] * r[4 * j4 + e] : 0.f;
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int s = c0 + 4 * j4 + e;
+                a[e] = s < t ? bt * expf(Gt - Gam[s]) * r[4 * j4 + e] : 0.f;
+              }
             }
             *reinterpret_cast<float4 *>(Asc + sidx(t, c0 + 4 * j4)) = a4;
           }
         }
       } else {  // lanes 64-127 hold H rows t: P straight to its operand
         const int t = myrow - kC;
-        const float Gt = Gam[t];
+        const float Gt = Gam[t], et = ea[t];
         for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
           float r[16];
           tmem_ld16(tl + T_GH + c0, r);
+          if (factored) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int s = c0 + e;
-            r[e] = s <= t ? expf(Gt - Gam[s]) * r[e] : 0.f;
+            for (int e = 0; e < 16; ++e) {
+              const int s = c0 + e;
+              r[e] = s <= t ? et * eb[s] * r[e] : 0.f;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int s = c0 + e;
+              r[e] = s <= t ? expf(Gt - Gam[s]) * r[e] : 0.f;
+            }
           }
           put8<kLo>(gb, OFF_P, kC, kC, t, c0, r);
           put8<kLo>(gb, OFF_P, kC, kC, t, c0 + 8, r + 8);

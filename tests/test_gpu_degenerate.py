@@ -95,3 +95,21 @@ def test_reset_inside_chunks(oracle_mod, precision):
     print(f"reset chunks {precision}: state {es:.3e} o {eo:.3e}")
     assert es < TOL_CHUNK[precision] and eo < TOL_CHUNK[precision]
     assert gdn.gdn_prefill_timeouts() == 0
+
+
+@pytest.mark.parametrize("precision", [gdn.GDN_PREC_BF16X3, gdn.GDN_PREC_BF16])
+@pytest.mark.parametrize("g_const", [-2.4, -2.6])
+def test_strong_uniform_decay_chunked(oracle_mod, precision, g_const):
+    """A constant decay whose range over a 64-token chunk (63 |g|) is just
+    under (151) and just over (164) the 160 up to which the kernel splits
+    exp(Gamma_t - Gamma_s) into two per-token factors; either side must
+    match the oracle."""
+    inp = gdn_inputs.make_inputs(1205, B=2, T=130)
+    inp.g[:] = g_const
+    S, o = _prefill(inp, precision)
+    S_ref, o_ref = oracle_mod.run_inputs(inp)
+    es = max_rel(S, S_ref, axes=(-2, -1))
+    eo = max_rel(o, o_ref, axes=(-2, -1))
+    print(f"decay {g_const} {precision}: state {es:.3e} o {eo:.3e}")
+    assert es < TOL_CHUNK[precision] and eo < TOL_CHUNK[precision]
+    assert gdn.gdn_prefill_timeouts() == 0
