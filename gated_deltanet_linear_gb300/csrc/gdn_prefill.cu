@@ -100,7 +100,8 @@ constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;  // room to align the base
 constexpr uint32_t T_SACC = 0;    // S^T: lanes dv, 128 columns dk
 constexpr uint32_t T_GH = 128;    // G (lanes 0-63), H (lanes 64-127): 64 columns
 constexpr uint32_t T_Y = 192;     // Y = S^T K^T: lanes dv, columns t
-constexpr uint32_t T_U = 256;     // U^T, then Delta^T = U^T - (W S)^T: lanes dv
+constexpr uint32_t T_U = 256;     // second half-K of G, H; then U^T, then
+                                  // Delta^T = U^T - (W S)^T: lanes dv
 constexpr uint32_t T_QS = 320;    // (Q S)^T, two buffers (chunk parity): lanes dv
 constexpr uint32_t T_PD = 448;    // (P Delta)^T: lanes dv, columns t
 
@@ -175,24 +176,53 @@ __device__ __forceinline__ uint32_t kstep16(const Operand &o, int ks) {
               : (uint32_t)(((ks >> 2) * o.R * 128 + (ks & 3) * 32) >> 4);
 }
 
-// D[M][N] (+)= A B^T over K = 16 * KSTEPS, issued by one thread.  The
-// descriptors are formed once and stepped by constants, so the issuing
+// One product D[M][N] (+)= A B^T, K = 16 per step, issued by one thread.
+// The descriptors are formed once and stepped by constants, so the issuing
 // thread spends its time on the MMAs rather than on descriptor arithmetic.
-template <bool kLo, int KSTEPS>
-__device__ __forceinline__ void gemm(uint32_t d, const Operand &a,
-                                     const Operand &b, int M, int N,
-                                     bool accumulate, bool negate_a = false) {
-  const uint32_t id = idesc_bf16(M, N, a.mn, b.mn) | (negate_a ? (1u << 13) : 0u);
-  const uint64_t ah = opdesc(a, false), bh = opdesc(b, false);
-  const uint64_t al = kLo ? opdesc(a, true) : 0, bl = kLo ? opdesc(b, true) : 0;
-#pragma unroll
-  for (int ks = 0; ks < KSTEPS; ++ks) {
-    const uint64_t ao = kstep16(a, ks), bo = kstep16(b, ks);
-    mma_bf16(d, ah + ao, bh + bo, id, (accumulate || ks > 0) ? 1u : 0u);
+template <bool kLo>
+struct Gemm {
+  uint32_t d, id;
+  uint64_t ah, bh, al, bl;
+  const Operand *a, *b;
+  bool accumulate;
+  __device__ __forceinline__ Gemm(uint32_t d_, const Operand &a_,
+                                  const Operand &b_, int M, int N,
+                                  bool accumulate_, bool negate_a = false)
+      : d(d_),
+        id(idesc_bf16(M, N, a_.mn, b_.mn) | (negate_a ? (1u << 13) : 0u)),
+        ah(opdesc(a_, false)), bh(opdesc(b_, false)),
+        al(kLo ? opdesc(a_, true) : 0), bl(kLo ? opdesc(b_, true) : 0),
+        a(&a_), b(&b_), accumulate(accumulate_) {}
+  // K step ks of the operands, accumulated onto D unless it is the first
+  // step written (`first`) of a product that does not accumulate.
+  __device__ __forceinline__ void step(int ks, bool first) const {
+    const uint64_t ao = kstep16(*a, ks), bo = kstep16(*b, ks);
+    mma_bf16(d, ah + ao, bh + bo, id, (accumulate || !first) ? 1u : 0u);
     if (kLo) {
       mma_bf16(d, ah + ao, bl + bo, id, 1u);
       mma_bf16(d, al + ao, bh + bo, id, 1u);
     }
+  }
+};
+
+template <bool kLo, int KSTEPS>
+__device__ __forceinline__ void gemm(uint32_t d, const Operand &a,
+                                     const Operand &b, int M, int N,
+                                     bool accumulate, bool negate_a = false) {
+  const Gemm<kLo> g(d, a, b, M, N, accumulate, negate_a);
+#pragma unroll
+  for (int ks = 0; ks < KSTEPS; ++ks) g.step(ks, ks == 0);
+}
+
+// Two independent products (different accumulators), their K steps
+// interleaved so that one product's dependent chain runs while the other's
+// waits.
+template <bool kLo, int KSTEPS>
+__device__ __forceinline__ void gemm2(const Gemm<kLo> &x, const Gemm<kLo> &y) {
+#pragma unroll
+  for (int ks = 0; ks < KSTEPS; ++ks) {
+    x.step(ks, ks == 0);
+    y.step(ks, ks == 0);
   }
 }
 
@@ -483,13 +513,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < nchunks; ++c) {
         if (!mbar_wait(rdy_a, ph, kWaitLimit)) break;
         fence_after_sync();
-        gemm<kLo, kD / 16>(tmem + T_GH, opKQ, opKb, 128, kC, false);
+        {
+          // [K;Q] K^T as two half-K products in two accumulators (T_U is
+          // free until MMA-u); the A/P build adds them
+          const Gemm<kLo> lo_(tmem + T_GH, opKQ, opKb, 128, kC, false);
+          const Gemm<kLo> hi_(tmem + T_U, opKQ, opKb, 128, kC, false);
+#pragma unroll
+          for (int ks = 0; ks < kD / 32; ++ks) {
+            lo_.step(ks, ks == 0);
+            hi_.step(ks + kD / 32, ks == 0);
+          }
+        }
         commit(done_a);
         if (!mbar_wait(rdy_s, ph, kWaitLimit)) break;
         fence_after_sync();
-        gemm<kLo, kD / 16>(tmem + T_Y, opST, opKb, 128, kC, false);
-        gemm<kLo, kD / 16>(tmem + T_QS + 64u * (uint32_t)(c & 1), opST, opQb,
-                           128, kC, false);
+        gemm2<kLo, kD / 16>(
+            Gemm<kLo>(tmem + T_Y, opST, opKb, 128, kC, false),
+            Gemm<kLo>(tmem + T_QS + 64u * (uint32_t)(c & 1), opST, opQb, 128,
+                      kC, false));
         commit(done_s);
         if (!mbar_wait(rdy_t, ph, kWaitLimit)) break;
         fence_after_sync();
@@ -501,8 +542,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         commit(done_d);
         if (!mbar_wait(rdy_d, ph, kWaitLimit)) break;
         fence_after_sync();
-        gemm<kLo, kC / 16>(tmem + T_PD, opDT, opP, 128, kC, false);
-        gemm<kLo, kC / 16>(tmem + T_SACC, opDTW, opKnB, 128, kD, true);
+        gemm2<kLo, kC / 16>(Gemm<kLo>(tmem + T_PD, opDT, opP, 128, kC, false),
+                            Gemm<kLo>(tmem + T_SACC, opDTW, opKnB, 128, kD, true));
         commit(done_4);
         ph ^= 1u;
       }
@@ -655,8 +696,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = myrow;
         const float bt = bet[t], Gt = Gam[t], bea = bt * ea[t];
         for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
-          float r[16];
+          float r[16], r2[16];
           tmem_ld16(tl + T_GH + c0, r);
+          tmem_ld16(tl + T_U + c0, r2);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) r[e] += r2[e];
 #pragma unroll
           for (int j4 = 0; j4 < 4; ++j4) {
             float4 a4;
@@ -681,8 +725,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = myrow - kC;
         const float Gt = Gam[t], et = ea[t];
         for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
-          float r[16];
+          float r[16], r2[16];
           tmem_ld16(tl + T_GH + c0, r);
+          tmem_ld16(tl + T_U + c0, r2);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) r[e] += r2[e];
           if (factored) {
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
