@@ -658,11 +658,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // are visible: the wait is also a SIMT barrier)
       if (!simt_and(mbar_wait(staged, parity, kWaitLimit))) { failed = true; break; }
       // [K; Q] operand rows from the staging tile.
+      // Lanes 4-7 of each quarter warp read their two 16-byte halves in the
+      // other order, so each of the two loads covers all eight 16-byte bank
+      // groups of the quarter warp once.
+      const int swap = (tid >> 2) & 1;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int row = (tid >> 4) + 16 * i, c0 = (tid & 15) * 8;
-        const float4 x0 = *reinterpret_cast<const float4 *>(stage + row * 128 + c0);
-        const float4 x1 = *reinterpret_cast<const float4 *>(stage + row * 128 + c0 + 4);
+        const float4 ya = *reinterpret_cast<const float4 *>(stage + row * 128 + c0 + 4 * swap);
+        const float4 yb = *reinterpret_cast<const float4 *>(stage + row * 128 + c0 + 4 - 4 * swap);
+        const float4 x0 = swap ? yb : ya, x1 = swap ? ya : yb;
         const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
         put8<kLo>(gb, OFF_KQ, 128, 128, row, c0, x);
       }
@@ -754,7 +759,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = tid >> 2, cq = (tid & 3) * 16;
         float tr[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) tr[e] = Tsc[sidx(t, cq + e)];
+        for (int e4 = 0; e4 < 16; e4 += 4) {
+          const float4 v4 = *reinterpret_cast<const float4 *>(Tsc + sidx(t, cq + e4));
+          tr[e4] = v4.x;
+          tr[e4 + 1] = v4.y;
+          tr[e4 + 2] = v4.z;
+          tr[e4 + 3] = v4.w;
+        }
         simt_sync();  // everyone holds its T values; scratch may be reused
         float x1[8], x2[8];
 #pragma unroll
