@@ -602,7 +602,7 @@ def main():
                      "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved_gbs / hbm_peak,
                      "traffic": traffic, "peak_kind": peak_kind,
-                     "kernel": "gdn_steps_kernel<false>"},
+                     "kernel": "gdn_steps_kernel<false, true>"},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,
