@@ -281,6 +281,39 @@ def tens_fn(torch, dev):
     return lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
 
+def verify_parts(torch, gdn, tens, stream, hbm_peak, parts, steps,
+                 warmup=5):
+    """The M-token verify launches on 32 sequences x 48 heads, M = 2, 4, 8,
+    without and with per-token checkpoints, in that order; each timed over
+    max(20, min(200, steps)) launches after `warmup` untimed ones."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    vin = gdn_inputs.make_workload("verify_b32")
+    Sv = [tens(vin.S) for _ in range(NSETS)]
+    ck = torch.empty((8,) + tuple(vin.S.shape), device=dev)
+    for M in (2, 4, 8):
+        sub = vin.tokens(0, M)
+        vq, vk, vv, vg, vb = (tens(x) for x in
+                              (sub.q, sub.k, sub.v, sub.g, sub.beta))
+        vo = torch.empty(sub.B, M, sub.vh, D, device=dev)
+        for use_ck in (False, True):
+            def vstep(i, M=M, use_ck=use_ck):
+                s = Sv[i % NSETS]
+                gdn.gdn_step_m(s, s, ck[:M] if use_ck else None, vq, vk,
+                               vv, vg, vb, vo, M=M, stream=stream)
+            n = max(20, min(200, steps))
+            for i in range(warmup):
+                vstep(i)
+            vms = time_launches(torch, vstep, n, stream)
+            nb = decode_bytes(sub.B, sub.kh, sub.vh, M, use_ck)
+            parts[f"verify_b32_m{M}{'_ckpt' if use_ck else ''}"] = {
+                "ms": vms, "head_steps_per_s": sub.B * sub.vh * M / (vms * 1e-3),
+                "gbs": nb / (vms * 1e-3) / 1e9,
+                "frac_of_measured_hbm": nb / (vms * 1e-3) / 1e9 / hbm_peak,
+                "bytes_per_launch": nb}
+    del Sv, ck
+    torch.cuda.empty_cache()
+
+
 def layer_parts(torch, gdn, tens, stream, hbm_peak, parts, steps,
                 warmup=5):
     """The layer core on 64 sequences x 48 heads, one token: prologue +
@@ -394,8 +427,9 @@ def main():
                     help="skip the verify / prefill sub-measurements")
     ap.add_argument("--no-cpu", action="store_true",
                     help="skip the CPU-baseline leg")
-    ap.add_argument("--only", choices=["prefill", "layer"], default=None,
-                    help="time only the prefill or the layer parts (used "
+    ap.add_argument("--only", choices=["prefill", "layer", "verify"],
+                    default=None,
+                    help="time only the prefill, layer or verify parts (used "
                          "for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -439,6 +473,9 @@ def main():
         t0 = time.time()
         if args.only == "prefill":
             prefill_parts(torch, gdn, tens_fn(torch, dev), stream, peaks, parts)
+        elif args.only == "verify":
+            verify_parts(torch, gdn, tens_fn(torch, dev), stream, hbm_peak,
+                         parts, args.steps, max(5, args.warmup))
         else:
             layer_parts(torch, gdn, tens_fn(torch, dev), stream, hbm_peak,
                         parts, args.steps, max(5, args.warmup))
@@ -537,31 +574,7 @@ def main():
         torch.cuda.empty_cache()
         del states
         torch.cuda.empty_cache()
-        vin = gdn_inputs.make_workload("verify_b32")
-        Sv = [tens(vin.S) for _ in range(NSETS)]
-        ck = torch.empty((8,) + tuple(vin.S.shape), device=dev)
-        for M in (2, 4, 8):
-            sub = vin.tokens(0, M)
-            vq, vk, vv, vg, vb = (tens(x) for x in
-                                  (sub.q, sub.k, sub.v, sub.g, sub.beta))
-            vo = torch.empty(sub.B, M, sub.vh, D, device=dev)
-            for use_ck in (False, True):
-                def vstep(i, M=M, use_ck=use_ck):
-                    s = Sv[i % NSETS]
-                    gdn.gdn_step_m(s, s, ck[:M] if use_ck else None, vq, vk,
-                                   vv, vg, vb, vo, M=M, stream=stream)
-                n = max(20, min(200, args.steps))
-                for i in range(5):
-                    vstep(i)
-                vms = time_launches(torch, vstep, n, stream)
-                nb = decode_bytes(sub.B, sub.kh, sub.vh, M, use_ck)
-                parts[f"verify_b32_m{M}{'_ckpt' if use_ck else ''}"] = {
-                    "ms": vms, "head_steps_per_s": sub.B * sub.vh * M / (vms * 1e-3),
-                    "gbs": nb / (vms * 1e-3) / 1e9,
-                    "frac_of_measured_hbm": nb / (vms * 1e-3) / 1e9 / hbm_peak,
-                    "bytes_per_launch": nb}
-        del Sv, ck
-        torch.cuda.empty_cache()
+        verify_parts(torch, gdn, tens, stream, hbm_peak, parts, args.steps)
         layer_parts(torch, gdn, tens, stream, hbm_peak, parts, args.steps)
         prefill_parts(torch, gdn, tens, stream, peaks, parts)
 
