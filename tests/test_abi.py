@@ -90,3 +90,40 @@ def test_binding_refuses_cpu_tensors(lib):
     with pytest.raises(ValueError):
         gdn.gdn_step(S, q, q, torch.zeros(1, 1, 3, 128), torch.zeros(1, 1, 3),
                      torch.zeros(1, 1, 3), torch.zeros(1, 1, 3, 128))
+
+
+def test_layer_and_norm_host_refusals(lib):
+    """The layer-core and gated-RMSNorm entry points refuse bad shapes,
+    counts and values on the host, before any CUDA call."""
+    ok = gdn.Shape(2, 16, 48, 128, 128)
+    bad = gdn.Shape(2, 16, 40, 128, 128)         # vh % kh != 0
+    zero = gdn.Shape(0, 16, 48, 128, 128)
+    n = None
+    # gated RMSNorm: shape, count, eps, B == 0, NULL buffers
+    norm = lambda sh, M, eps: lib.gdn_gated_rmsnorm_m(
+        ctypes.byref(sh) if sh is not None else None, M, eps, n, n, n, n, n)
+    assert norm(None, 1, 1e-6) == gdn.GDN_EINVAL
+    assert norm(bad, 1, 1e-6) == gdn.GDN_ESHAPE
+    assert norm(ok, 0, 1e-6) == gdn.GDN_ERANGE
+    assert norm(ok, gdn.GDN_MAX_TOKENS + 1, 1e-6) == gdn.GDN_ERANGE
+    assert norm(ok, 1, -1.0) == gdn.GDN_EINVAL
+    assert norm(ok, 1, float("nan")) == gdn.GDN_EINVAL
+    assert norm(zero, 1, 1e-6) == gdn.GDN_OK
+    assert norm(ok, 1, 1e-6) == gdn.GDN_EINVAL     # NULL buffers
+    # layer step: width-4 convolution only, count, eps, workspace size query
+    step = lambda sh, M, ck, eps: lib.gdn_layer_step_m(
+        ctypes.byref(sh), M, ck, eps, *([n] * 13), 0, n)
+    assert step(ok, 1, 3, 1e-6) == gdn.GDN_ESHAPE
+    assert step(ok, 0, 4, 1e-6) == gdn.GDN_ERANGE
+    assert step(ok, 1, 4, -1.0) == gdn.GDN_EINVAL
+    assert step(zero, 1, 4, 1e-6) == gdn.GDN_OK
+    assert step(bad, 1, 4, 1e-6) == gdn.GDN_ESHAPE
+    assert lib.gdn_layer_workspace(ctypes.byref(ok), 0) == 0
+    per_token = 2 * 16 * 128 * 4 + 48 * 128 * 4 + 2 * 48 * 4
+    assert lib.gdn_layer_workspace(ctypes.byref(ok), 3) == 2 * 3 * per_token
+    # history rollback
+    assert lib.gdn_layer_hist_rollback(ctypes.byref(ok), 4, 3, *([n] * 5),
+                                       n) == gdn.GDN_ESHAPE
+    assert lib.gdn_layer_hist_rollback(ctypes.byref(ok), 0, 4, *([n] * 5),
+                                       n) == gdn.GDN_ERANGE
+    assert gdn.gdn_strerror(gdn.GDN_ESCRATCH) != "unknown status"
