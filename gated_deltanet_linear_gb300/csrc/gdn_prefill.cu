@@ -326,22 +326,29 @@ __device__ __forceinline__ void put_row4(float *X, int r, int c, float4 v) {
 // (zero, never read as A) holds the intermediate products.  Writes Tsc.
 __device__ __forceinline__ void tri_inverse(float *Asc, float *Tsc, int tid) {
   // 1. Diagonal blocks by forward substitution: column j of block i on 4
-  //    lanes, rows split by r mod 4.
+  //    lanes, rows split by r mod 4.  Each lane keeps, for its rows t, the
+  //    running sum p_t of A[t][k] x_k over the x_k known so far; x_k is
+  //    final once p_k has all k terms, and its owner broadcasts it with one
+  //    shuffle, so the serial chain per step is a shuffle and an FMA.  A is
+  //    strictly lower, so terms with k >= t add exact zeros.
   {
     const int col = tid >> 2;          // 0..63: block i = col / 16
     const int q4 = tid & 3;
     const int blk = col >> 4, jj = col & 15, r0 = blk * 16;
+    const int lane = tid & 31;
     float x[4] = {0.f, 0.f, 0.f, 0.f};  // rows r0 + q4 + 4i
+    float p[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int t = 0; t < 16; ++t) {
-      float part = 0.f;
+    for (int k = 0; k < 16; ++k) {
+      float xk = 0.f;
+      if ((k & 3) == q4) {
+        xk = (k == jj ? 1.f : 0.f) - p[k >> 2];
+        x[k >> 2] = xk;
+      }
+      xk = __shfl_sync(0xffffffffu, xk, (lane & ~3) | (k & 3));
 #pragma unroll
       for (int i = 0; i < 4; ++i)
-        part = fmaf(Asc[sidx(r0 + t, r0 + q4 + 4 * i)], x[i], part);
-      part += __shfl_xor_sync(0xffffffffu, part, 1);
-      part += __shfl_xor_sync(0xffffffffu, part, 2);
-      const float xt = (t == jj ? 1.f : 0.f) - part;
-      if ((t & 3) == q4) x[t >> 2] = xt;
+        p[i] = fmaf(Asc[sidx(r0 + q4 + 4 * i, r0 + k)], xk, p[i]);
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) Tsc[sidx(r0 + q4 + 4 * i, r0 + jj)] = x[i];
