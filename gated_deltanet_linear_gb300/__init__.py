@@ -144,6 +144,22 @@ def _t(x, name, numel):
     return x.data_ptr()
 
 
+def _io(x, name, numel):
+    """Pointer of a token input or output: a contiguous fp32 CUDA tensor, or a
+    page-locked (pinned) CPU tensor, which the kernels read or write over the
+    host link."""
+    if isinstance(x, torch.Tensor) and not x.is_cuda:
+        if not x.is_pinned():
+            raise ValueError(f"{name}: a CPU tensor must be pinned "
+                             "(tensor.pin_memory())")
+        if x.dtype != torch.float32 or not x.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous float32 tensor")
+        if x.numel() != numel:
+            raise ValueError(f"{name} has {x.numel()} elements, expected {numel}")
+        return x.data_ptr()
+    return _t(x, name, numel)
+
+
 def _shape(S, q):
     if S.dim() != 4:
         raise ValueError("S must be [B][vh][kd][vd]")
@@ -158,28 +174,30 @@ def _check(status, where):
 
 
 def gdn_step(S, q, k, v, g, beta, o, stream=None):
-    """One token for all heads; S is updated in place, o written."""
+    """One token for all heads; S is updated in place, o written.  The token
+    tensors (q, k, v, g, beta, o) may be CUDA tensors or pinned CPU tensors."""
     sh = _shape(S, q)
     B, kh, vh, kd, vd = sh.B, sh.kh, sh.vh, sh.kd, sh.vd
-    args = (_t(S, "S", B * vh * kd * vd), _t(q, "q", B * kh * kd),
-            _t(k, "k", B * kh * kd), _t(v, "v", B * vh * vd),
-            _t(g, "g", B * vh), _t(beta, "beta", B * vh),
-            _t(o, "o", B * vh * vd))
+    args = (_t(S, "S", B * vh * kd * vd), _io(q, "q", B * kh * kd),
+            _io(k, "k", B * kh * kd), _io(v, "v", B * vh * vd),
+            _io(g, "g", B * vh), _io(beta, "beta", B * vh),
+            _io(o, "o", B * vh * vd))
     _check(load().gdn_step(ctypes.byref(sh), *args, _stream(stream)),
            "gdn_step")
 
 
 def gdn_step_m(S_in, S_out, ckpt, q, k, v, g, beta, o, M=None, stream=None):
-    """M tokens in one launch (M defaults to q.shape[1])."""
+    """M tokens in one launch (M defaults to q.shape[1]).  The token tensors
+    may be CUDA tensors or pinned CPU tensors, as for gdn_step."""
     sh = _shape(S_in, q)
     B, kh, vh, kd, vd = sh.B, sh.kh, sh.vh, sh.kd, sh.vd
     M = int(q.shape[1] if M is None else M)
     n = B * vh * kd * vd
     args = (_t(S_in, "S_in", n), _t(S_out, "S_out", n),
-            _t(ckpt, "ckpt", M * n), _t(q, "q", B * M * kh * kd),
-            _t(k, "k", B * M * kh * kd), _t(v, "v", B * M * vh * vd),
-            _t(g, "g", B * M * vh), _t(beta, "beta", B * M * vh),
-            _t(o, "o", B * M * vh * vd))
+            _t(ckpt, "ckpt", M * n), _io(q, "q", B * M * kh * kd),
+            _io(k, "k", B * M * kh * kd), _io(v, "v", B * M * vh * vd),
+            _io(g, "g", B * M * vh), _io(beta, "beta", B * M * vh),
+            _io(o, "o", B * M * vh * vd))
     _check(load().gdn_step_m(ctypes.byref(sh), M, *args, _stream(stream)),
            "gdn_step_m")
 

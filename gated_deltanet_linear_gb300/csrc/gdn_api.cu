@@ -49,6 +49,22 @@ int check_device_ptr(const void *p) {
   return attr.device == dev ? GDN_OK : GDN_EPTR;
 }
 
+// Token inputs and outputs may also live in page-locked host memory that is
+// mapped into the device's address space at the same address (any
+// cudaHostAlloc / cudaMallocHost block under unified addressing): kernels
+// then read and write it over the host link.  Pageable memory is refused.
+int check_io_ptr(const void *p) {
+  cudaPointerAttributes attr;
+  memset(&attr, 0, sizeof(attr));
+  if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+    cudaGetLastError();
+    return GDN_EPTR;
+  }
+  if (attr.type == cudaMemoryTypeHost)
+    return attr.devicePointer == p ? GDN_OK : GDN_EPTR;
+  return check_device_ptr(p);
+}
+
 int check_shape(const gdn_shape *s) {
   if (!s) return GDN_EINVAL;
   if (s->B < 0 || s->kh <= 0 || s->vh <= 0) return GDN_ESHAPE;
@@ -65,6 +81,20 @@ int check_bufs(const Buf *b, int n) {
   }
   for (int i = 0; i < n; ++i) {
     const int r = check_device_ptr(b[i].p);
+    if (r != GDN_OK) return r;
+  }
+  return GDN_OK;
+}
+
+// check_bufs for token inputs and outputs (device, managed or mapped
+// page-locked host memory).
+int check_io_bufs(const Buf *b, int n) {
+  for (int i = 0; i < n; ++i) {
+    if (!b[i].p) return GDN_EINVAL;
+    if (!aligned16(b[i].p)) return GDN_EALIGN;
+  }
+  for (int i = 0; i < n; ++i) {
+    const int r = check_io_ptr(b[i].p);
     if (r != GDN_OK) return r;
   }
   return GDN_OK;
@@ -93,9 +123,14 @@ int steps_common_check(const gdn_shape *s, int M, const float *S_in,
   Buf in[] = {{S_in, sb}, {q, qkb}, {k, qkb}, {v, vb}, {g, gb}, {beta, gb}};
   Buf out[] = {{S_out, sb}, {o, vb}, {ckpt, sb * (size_t)M}};
   const int nout = ckpt ? 3 : 2;
-  r = check_bufs(in, 6);
+  // the state and the checkpoints in device memory; token inputs and o
+  // also in mapped page-locked host memory
+  Buf dev_bufs[] = {in[0], out[0], out[2]};
+  r = check_bufs(dev_bufs, ckpt ? 3 : 2);
   if (r) return r;
-  r = check_bufs(out, nout);
+  r = check_io_bufs(in + 1, 5);
+  if (r) return r;
+  r = check_io_bufs(out + 1, 1);
   if (r) return r;
   // Outputs never overlap inputs or each other; the one exception is an
   // in-place state (S_out == S_in exactly).

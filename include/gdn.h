@@ -28,6 +28,15 @@
  *     Every array pointer must be 16-byte aligned (GDN_EALIGN otherwise) and
  *     point to device (or managed) memory of the current device (GDN_EPTR
  *     otherwise).  NULL where a buffer is required gives GDN_EINVAL.
+ *     Exception: the token inputs and outputs of gdn_step, gdn_step_m and
+ *     gdn_layer_step_m's o may also be page-locked host memory mapped at
+ *     the same address on the device (cudaHostAlloc / cudaMallocHost under
+ *     unified addressing); the kernel then reads and writes it over the
+ *     host link.  On a GB300 a 64 x 48-head decode step writing o to host
+ *     memory this way took the same time as with device memory, while
+ *     reading q, k, v, g, beta from host memory added ~13 us of latency;
+ *     copy the inputs in, write o out directly.  Pageable memory is refused
+ *     (GDN_EPTR).
  *   - Ownership: the caller allocates and frees everything.  The library
  *     never allocates device memory and never synchronises; every call only
  *     enqueues work on `stream` and returns.  (The one exception is the

@@ -345,11 +345,20 @@ def test_refusals_with_device_memory():
     bad = list(base)
     bad[3] = p(v) + 4
     assert step(*bad) == gdn.GDN_EALIGN
-    # host memory (pageable and pinned)
-    for host_t in (torch.empty(1, 48, 128), torch.empty(1, 48, 128).pin_memory()):
-        bad = list(base)
-        bad[3] = host_t.data_ptr()
-        assert step(*bad) == gdn.GDN_EPTR
+    # pageable host memory is refused; page-locked host memory mapped into
+    # the device's address space is accepted for the token inputs/outputs
+    bad = list(base)
+    pageable = torch.empty(1, 48, 128)
+    bad[3] = pageable.data_ptr()
+    assert step(*bad) == gdn.GDN_EPTR
+    pinned = torch.zeros(1, 48, 128).pin_memory()
+    ok = list(base)
+    ok[3] = pinned.data_ptr()
+    assert step(*ok) == gdn.GDN_OK
+    # ... but never for the state
+    bad = list(base)
+    bad[0] = torch.zeros(1, 48, 128, 128).pin_memory().data_ptr()
+    assert step(*bad) == gdn.GDN_EPTR
     # output overlapping an input
     bad = list(base)
     bad[6] = p(S)
