@@ -7,8 +7,8 @@
 // K elements is stored as K / (128 / elem_bytes) column blocks, each block
 // R rows x 128 bytes, rows consecutive; inside a block, 16-byte chunk c of
 // row r is stored at chunk position c ^ (r & 7).  Blocks start on 1024-byte
-// boundaries.  One MMA consumes 32 bytes of K per row (8 tf32 or 16 bf16
-// elements), so the descriptor start steps by 32 bytes within a block.
+// boundaries.  One MMA consumes 32 bytes of K per row (16 bf16 elements),
+// so the descriptor start steps by 32 bytes within a block.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -31,7 +31,7 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t smem_addr) {
   return d;
 }
 
-enum : uint32_t { kFmtBF16 = 1, kFmtTF32 = 2 };
+enum : uint32_t { kFmtBF16 = 1 };
 
 // Instruction descriptor: fp32 accumulator, A and B of format `fmt`, both
 // K-major, M x N tile.
@@ -41,17 +41,6 @@ __host__ __device__ constexpr uint32_t idesc(uint32_t fmt, int M, int N) {
 }
 
 // ------------------------------------------------------------------ MMA
-
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a,
-                                         uint64_t b, uint32_t id,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(
-          d_tmem),
-      "l"(a), "l"(b), "r"(id), "r"(accumulate));
-}
 
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a,
                                          uint64_t b, uint32_t id,
@@ -186,13 +175,6 @@ __device__ __forceinline__ uint32_t sw128_off(int R, int r, int k, int eb) {
 // Descriptor of K step `ks` (32 bytes of K) of a tile of R rows at `base`.
 __device__ __forceinline__ uint64_t desc_kstep(uint32_t base, int R, int ks) {
   return desc_sw128(base + (uint32_t)((ks >> 2) * R * 128 + (ks & 3) * 32));
-}
-
-// fp32 -> tf32 (round to nearest, ties away), kept in an fp32 container.
-__device__ __forceinline__ float to_tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return __uint_as_float(r);
 }
 
 }  // namespace tc
