@@ -293,13 +293,13 @@ __device__ __forceinline__ int sidx(int r, int c) {
   return r * 64 + ((((c >> 2) ^ (r & 7)) << 2) | (c & 3));
 }
 
-// Y[r][c0..c0+3] = sum_{u < n} X[xr][xc + u] * Z[zr + u][zc + c0 .. +3] over
-// the fp32 scratch layout; returns the four sums.
+// Y[r][c0..c0+3] = sum_{u0 <= u < n} X[xr][xc + u] * Z[zr + u][zc + c0 .. +3]
+// over the fp32 scratch layout (u0, n multiples of 4); returns the four sums.
 __device__ __forceinline__ float4 row_times(const float *X, int xr, int xc,
                                             const float *Z, int zr, int zc,
-                                            int n) {
+                                            int n, int u0 = 0) {
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int u4 = 0; u4 < n; u4 += 4) {
+  for (int u4 = u0; u4 < n; u4 += 4) {
     const float4 a = *reinterpret_cast<const float4 *>(X + sidx(xr, xc + u4));
     const float av[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
@@ -388,15 +388,21 @@ __device__ __forceinline__ void tri_inverse(float *Asc, float *Tsc, int tid) {
   }
   simt_sync();
   // 3. 32 -> 64: X = A[32:64, 0:32] T[0:32, 0:32] goes to A scratch
-  //    [0:32, 32:64]; then T[32:64, 0:32] = -T[32:64, 32:64] X.
+  //    [0:32, 32:64]; then T[32:64, 0:32] = -T[32:64, 32:64] X.  Both T
+  //    factors are exactly lower triangular, so the terms a warp skips are
+  //    exact zeros: warp w takes columns 4w .. 4w+3 of X (rows = lanes) from
+  //    k = 4w on, then rows 4w .. 4w+3 of the result (lanes: row 4w + lane/8,
+  //    columns 4 (lane % 8)) up to k = 4w+3.  The sums keep their order.
   {
-    const int r = tid >> 3, c4 = (tid & 7) * 4;
-    put_row4(Asc, r, 32 + c4, row_times(Asc, 32 + r, 0, Tsc, 0, c4, 32));
+    const int w = tid >> 5, lane = tid & 31, c4 = 4 * w;
+    put_row4(Asc, lane, 32 + c4,
+             row_times(Asc, 32 + lane, 0, Tsc, 0, c4, 32, c4));
   }
   simt_sync();
   {
-    const int r = tid >> 3, c4 = (tid & 7) * 4;
-    const float4 y = row_times(Tsc, 32 + r, 32, Asc, 0, 32 + c4, 32);
+    const int w = tid >> 5, lane = tid & 31;
+    const int r = 4 * w + (lane >> 3), c4 = (lane & 7) * 4;
+    const float4 y = row_times(Tsc, 32 + r, 32, Asc, 0, 32 + c4, 4 * w + 4);
     put_row4(Tsc, 32 + r, c4, make_float4(-y.x, -y.y, -y.z, -y.w));
   }
   simt_sync();
