@@ -252,6 +252,8 @@ int gdn_prefill(const gdn_shape *shape, int T, float *S, const float *q,
   int r = check_shape(shape);
   if (r) return r;
   if (T < 1 || T > GDN_MAX_TOKENS || chunk != 64) return GDN_ERANGE;
+  // the copy engine addresses a sequence's rows of q, k, o with strides below 2^40 bytes
+  if ((unsigned long long)T * (unsigned long long)shape->vh >= (1ull << 31)) return GDN_ERANGE;
   if (shape->B == 0) return GDN_OK;
   const size_t sb = state_floats(shape) * 4;
   const size_t qkb = (size_t)shape->B * T * shape->kh * shape->kd * 4;

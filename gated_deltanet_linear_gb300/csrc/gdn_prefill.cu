@@ -22,14 +22,14 @@
 // the SIMT work on A and its inverse.  Per chunk (D = M x N accumulator in
 // TMEM, lanes = M):
 //   MMA-a  G,H  [t'][s]  = [K; Q] K^T                       (A, B K-major)
-//   SIMT   S^T operand from TMEM (under MMA-a)
+//   SIMT   S^T operand from TMEM, then S^T *= gamma_63 in TMEM (under MMA-a)
 //   MMA-s  Y    [dv][t]  = S^T K^T;  (Q S)^T [dv][t] = S^T Q^T
 //   SIMT   o of the previous chunk;  A and P from G, H;
 //          T = (I + A)^-1, blocked 16 x 16, fp32 (under MMA-s)
 //   MMA-u  U^T  [dv][t]  = V^T (T diag(beta))^T             (A = V, MN-major)
 //   SIMT   Y operand from TMEM (under MMA-u)
 //   MMA-d  Delta^T = U^T - Y (T diag(beta gamma))^T   (negated A onto U^T)
-//   SIMT   Delta^T and Delta^T diag(w) operands;  S^T *= gamma_63
+//   SIMT   Delta^T and Delta^T diag(w) operands
 //   MMA-3  (P Delta)^T = Delta^T P^T
 //   MMA-4  S^T += (Delta^T diag(w)) K                        (B = K, MN-major)
 //   SIMT   O^T = diag(gamma) (Q S)^T + (P Delta)^T  -> o, emitted in the
@@ -37,8 +37,9 @@
 // Every operand a thread writes is a row it owns (a row of an input, or a
 // TMEM lane of an earlier result), stored 8 elements at a time; transposes
 // happen in the MMA descriptors (MN-major operands), never in memory.  The
-// next chunk's K, Q, V rows and gates are loaded into registers while the
-// current chunk's last products run.
+// next chunk's V rows and gates are loaded into registers, and its gate
+// vectors computed, while the current chunk's last products run; its K and
+// Q rows are bulk-copied into a staging tile earlier still.
 //
 // Precision.  Operands are bf16 in shared memory:
 //   split-bf16 ("BF16X3"): x = hi + lo with hi = bf16(x), lo = bf16(x - hi);
@@ -49,6 +50,9 @@
 // fp32.
 
 #include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
 
 #include "gdn_internal.cuh"
 #include "gdn_tc.cuh"
@@ -74,7 +78,10 @@ constexpr int kThreads = kSimt + 64;
 // phase:
 //   Ra 64 KB: [K; Q] (128 x 128), the whole chunk
 //   Rb 32 KB: V (64 x 128)            -> Y (128 x 64) -> Delta^T (128 x 64)
-//   Rc 32 KB: A, T scratch (fp32)     -> T diag(bg), T diag(b) (64 x 64 each)
+//   Rc 32 KB: o of the previous chunk (fp32 [t][dv], 64 x 128, read by
+//             bulk stores before the A build)
+//                                     -> A, T scratch (fp32)
+//                                     -> T diag(bg), T diag(b) (64 x 64 each)
 //                                     -> Delta^T diag(w) (128 x 64)
 //   Rd 64 KB: S^T (128 x 128)         -> fp32 [K; Q] of the next chunk
 //   Rp 16 KB: P (64 x 64)
@@ -83,6 +90,7 @@ constexpr uint32_t OFF_KQ = RA;             // 128 x 128
 constexpr uint32_t OFF_V = RB;              // 64 x 128
 constexpr uint32_t OFF_Y = RB;              // 128 x 64 (after MMA-u)
 constexpr uint32_t OFF_DT = RB;             // 128 x 64 (after MMA-d)
+constexpr uint32_t OFF_OT = RC;             // fp32 o tile [64][128]
 constexpr uint32_t OFF_SCR = RC;            // fp32 A [64][64] + T [64][64]
 constexpr uint32_t OFF_TB = RC;             // 64 x 64: T diag(beta gamma)
 constexpr uint32_t OFF_TB2 = RC + 16384;    // 64 x 64: T diag(beta)
@@ -266,24 +274,50 @@ __device__ __forceinline__ void signal_ready(uint32_t mbar) {
   mbar_arrive(mbar);
 }
 
-// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
-// global -> shared by the copy engine; its bytes count against the
-// mbarrier's expected transaction count.
-__device__ __forceinline__ void bulk_copy(uint32_t smem, const void *gmem,
-                                          uint32_t bytes, uint32_t mbar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
-      "[%0], [%1], %2, [%3];" ::"r"(smem),
-      "l"(gmem), "r"(bytes), "r"(mbar)
-      : "memory");
-}
-
 // The one arrival of a phase, announcing `bytes` of bulk copies.
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t mbar,
                                                       uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar),
                "r"(bytes)
                : "memory");
+}
+
+// Tensor copies of one box of a row tensor map (see rows_map): the 64
+// token rows t0 .. t0+63 of head h of sequence b, 512 bytes each, to or from
+// consecutive 512-byte rows of shared memory.  Rows past the sequence's end
+// read as zeros and are not written.  The load counts its bytes (the whole
+// box) against the mbarrier; the store joins this thread's bulk group.
+__device__ __forceinline__ void tma_load_rows(uint32_t smem, const CUtensorMap *map,
+                                              int h, int t0, int b, uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(h), "r"(t0), "r"(b),
+      "r"(mbar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_store_rows(const CUtensorMap *map, int h,
+                                               int t0, int b, uint32_t smem) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group"
+      " [%0, {%1, %2, %3, %4}], [%5];" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(0), "r"(h), "r"(t0), "r"(b), "r"(smem)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until this thread's bulk stores have read their shared-memory source
+// (the tile may be overwritten), or (`all`) have completed.
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // fp32 scratch for the triangular solve: A and T, 64 x 64 each, rows of 64
@@ -410,11 +444,12 @@ __device__ __forceinline__ void tri_inverse(float *Asc, float *Tsc, int tid) {
 
 template <bool kLo>
 __global__ void __launch_bounds__(kThreads, 1)
-    gdn_chunk_kernel(float *__restrict__ S, const float *__restrict__ q,
-                     const float *__restrict__ k, const float *__restrict__ v,
-                     const float *__restrict__ g,
-                     const float *__restrict__ beta, float *__restrict__ o,
-                     int T, int kh, int vh, int rep) {
+    gdn_chunk_kernel(float *__restrict__ S, const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k,
+                     const float *__restrict__ v, const float *__restrict__ g,
+                     const float *__restrict__ beta,
+                     const __grid_constant__ CUtensorMap tm_o, int T, int kh,
+                     int vh, int rep) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw_s = (uint32_t)__cvta_generic_to_shared(smem_raw);
   const uint32_t sb = (raw_s + 1023u) & ~1023u;
@@ -473,33 +508,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // K and Q rows of chunk c, fp32, into the staging tile [128 rows: K then
     // Q][128] as soon as it is free: before the loop for chunk 0, else once
     // MMA-s of chunk c-1 has consumed the S^T operand that shares its region
-    // (about two thirds of a chunk ahead of use).
-    // Each row is 512 contiguous bytes: one bulk copy; rows past T are
-    // zeroed with ordinary stores before the phase's single arrival.
+    // (about two thirds of a chunk ahead of use).  One tensor copy of 64
+    // rows each; rows past T arrive as zeros.
     int issued = -1;
     for (int c = 0; c < nchunks; ++c) {
       if (c > 0 && !mbar_wait(done_s, (uint32_t)((c - 1) & 1), kWaitLimit)) break;
-      const int t0 = c * kC;
-      const int n = min(kC, T - t0);
-      const size_t qk_base = ((size_t)b * T + t0) * kh + hh;
-      if (n < kC) {
-        for (int j = lane; j < 2 * (kC - n) * 32; j += 32) {
-          const int rr = j >> 5, ch = j & 31;
-          const int row = (rr < kC - n ? 0 : kC) + n + (rr % (kC - n));
-          *reinterpret_cast<float4 *>(gb + OFF_STAGE + row * 512 + ch * 16) =
-              make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(staged, 2u * kC * 512u);
+        tma_load_rows(sb + OFF_STAGE, &tm_k, hh, c * kC, b, staged);
+        tma_load_rows(sb + OFF_STAGE + kC * 512, &tm_q, hh, c * kC, b, staged);
       }
-      if (lane == 0) mbar_arrive_expect_tx(staged, (uint32_t)(2 * n * 512));
       __syncwarp();
-      for (int row = lane; row < 2 * kC; row += 32) {
-        const int t = row & (kC - 1);
-        if (t < n)
-          bulk_copy(sb + OFF_STAGE + (uint32_t)(row * 512),
-                    (row < kC ? k : q) + (qk_base + (size_t)t * kh) * kD, 512u,
-                    staged);
-      }
       issued = c;
     }
     // nothing may still be copying into shared memory when the CTA ends
@@ -609,10 +628,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
 
-    // o for chunk cc = diag(gamma) (Q S)^T + (P Delta)^T, read from TMEM.
+    // o for chunk cc = diag(gamma) (Q S)^T + (P Delta)^T, read from TMEM
+    // into the o tile ([t][dv] rows of 512 bytes, the layout of o), then
+    // written out by one tensor store (store_o) after a SIMT barrier, so the
+    // global stores leave the SIMT warps' path.
+    float *otile = reinterpret_cast<float *>(gb + OFF_OT);
     auto emit_o = [&](int cc) {
-      const int nn = min(kC, T - cc * kC);
-      const size_t vb = ((size_t)b * T + (size_t)cc * kC) * vh + vi;
       const float *gm = gam_o + (cc & 1) * 64;
       const uint32_t qs = T_QS + 64u * (uint32_t)(cc & 1);
       for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
@@ -620,55 +641,70 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld16(tl + qs + c0, r);
         tmem_ld16(tl + T_PD + c0, pd);
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-          const int t = c0 + jj;
-          if (t < nn) o[(vb + (size_t)t * vh) * kD + myrow] = fmaf(gm[t], r[jj], pd[jj]);
+        for (int j4 = 0; j4 < 16; j4 += 4) {
+          const float4 g4 = *reinterpret_cast<const float4 *>(gm + c0 + j4);
+          otile[(c0 + j4) * kD + myrow] = fmaf(g4.x, r[j4], pd[j4]);
+          otile[(c0 + j4 + 1) * kD + myrow] = fmaf(g4.y, r[j4 + 1], pd[j4 + 1]);
+          otile[(c0 + j4 + 2) * kD + myrow] = fmaf(g4.z, r[j4 + 2], pd[j4 + 2]);
+          otile[(c0 + j4 + 3) * kD + myrow] = fmaf(g4.w, r[j4 + 3], pd[j4 + 3]);
         }
       }
+      fence_proxy_async();  // the tile is read by the copy engine
+    };
+    // Thread 0, after the barrier that follows emit_o(cc): one tensor store
+    // of the tile (rows past T are not written).
+    auto store_o = [&](int cc) {
+      tma_store_rows(&tm_o, vi, cc * kC, b, sb + OFF_OT);
+      bulk_commit();
     };
 
+    // Gate vectors of chunk cc from the prefetched g, beta (warp 0): the
+    // cumulative log-decay Gamma, gamma, w, beta, the factors ea, eb.
+    // Run for chunk c + 1 while chunk c's last products finish; the SIMT
+    // barrier that ends that wait makes them visible.
+    auto gates = [&](int cc) {
+      bet[lane] = pb[0];
+      bet[lane + 32] = pb[1];
+      float sa = pg[0], sc = pg[1];
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float ya = __shfl_up_sync(0xffffffffu, sa, off);
+        const float yc = __shfl_up_sync(0xffffffffu, sc, off);
+        if (lane >= off) {
+          sa += ya;
+          sc += yc;
+        }
+      }
+      sc += __shfl_sync(0xffffffffu, sa, 31);
+      const float last = __shfl_sync(0xffffffffu, sc, 31);
+      Gam[lane] = sa;
+      Gam[lane + 32] = sc;
+      gam[lane] = expf(sa);
+      gam[lane + 32] = expf(sc);
+      gam_o[(cc & 1) * 64 + lane] = gam[lane];
+      gam_o[(cc & 1) * 64 + lane + 32] = gam[lane + 32];
+      wv[lane] = expf(last - sa);
+      wv[lane + 32] = expf(last - sc);
+      float gmax = fmaxf(sa, sc), gmin = fminf(sa, sc);
+#pragma unroll
+      for (int off = 16; off; off >>= 1) {
+        gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, off));
+        gmin = fminf(gmin, __shfl_xor_sync(0xffffffffu, gmin, off));
+      }
+      const float ref = 0.5f * (gmax + gmin);
+      ea[lane] = expf(sa - ref);
+      ea[lane + 32] = expf(sc - ref);
+      eb[lane] = expf(ref - sa);
+      eb[lane + 32] = expf(ref - sc);
+      if (lane == 0) *fac = (gmax - gmin <= 160.f) ? 1 : 0;
+    };
+    if (warp == 0) gates(0);
     uint32_t parity = 0;
     bool failed = false;
     for (int c = 0; c < nchunks; ++c) {
       // ---------------------------------------------------- phase 0: inputs
-      if (warp == 0) {
-        bet[lane] = pb[0];
-        bet[lane + 32] = pb[1];
-        float sa = pg[0], sc = pg[1];
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const float ya = __shfl_up_sync(0xffffffffu, sa, off);
-          const float yc = __shfl_up_sync(0xffffffffu, sc, off);
-          if (lane >= off) {
-            sa += ya;
-            sc += yc;
-          }
-        }
-        sc += __shfl_sync(0xffffffffu, sa, 31);
-        const float last = __shfl_sync(0xffffffffu, sc, 31);
-        Gam[lane] = sa;
-        Gam[lane + 32] = sc;
-        gam[lane] = expf(sa);
-        gam[lane + 32] = expf(sc);
-        gam_o[(c & 1) * 64 + lane] = gam[lane];
-        gam_o[(c & 1) * 64 + lane + 32] = gam[lane + 32];
-        wv[lane] = expf(last - sa);
-        wv[lane + 32] = expf(last - sc);
-        float gmax = fmaxf(sa, sc), gmin = fminf(sa, sc);
-#pragma unroll
-        for (int off = 16; off; off >>= 1) {
-          gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, off));
-          gmin = fminf(gmin, __shfl_xor_sync(0xffffffffu, gmin, off));
-        }
-        const float ref = 0.5f * (gmax + gmin);
-        ea[lane] = expf(sa - ref);
-        ea[lane + 32] = expf(sc - ref);
-        eb[lane] = expf(ref - sa);
-        eb[lane + 32] = expf(ref - sc);
-        if (lane == 0) *fac = (gmax - gmin <= 160.f) ? 1 : 0;
-      }
-      // this chunk's K and Q rows are in the staging tile (and the gates above
-      // are visible: the wait is also a SIMT barrier)
+      // this chunk's K and Q rows are in the staging tile (its gates were
+      // written before the SIMT barrier that ended the previous wait)
       if (!simt_and(mbar_wait(staged, parity, kWaitLimit))) { failed = true; break; }
       // [K; Q] operand rows from the staging tile.
       // Lanes 4-7 of each quarter warp read their two 16-byte halves in the
@@ -685,6 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         put8<kLo>(gb, OFF_KQ, 128, 128, row, c0, x);
       }
       signal_ready(rdy_a);  // -> MMA-a: G, H = [K; Q] K^T
+      if (c > 0) emit_o(c - 1);  // the previous chunk's output, into the o tile
       // V operand rows from registers (needed from MMA-u on)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -695,16 +732,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         put8<kLo>(gb, OFF_V, 64, 128, row, c0, x);
       }
       simt_sync();          // the staging tile is read; its region is reused
+      if (c > 0 && tid == 0) store_o(c - 1);
 
-      // ------------- phase 1: S^T operand (rows dv, columns dk) from TMEM
-      for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
-        float r[16];
-        tmem_ld16(tl + T_SACC + c0, r);
-        put8<kLo>(gb, OFF_ST, 128, 128, myrow, c0, r);
-        put8<kLo>(gb, OFF_ST, 128, 128, myrow, c0 + 8, r + 8);
+      // ------------- phase 1: S^T operand (rows dv, columns dk) from TMEM;
+      // the accumulator is then decayed in place, S^T *= gamma_63, ready for
+      // MMA-4 (nothing reads it in between: MMA-s reads the operand)
+      {
+        const float gC = gam[kC - 1];
+        for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
+          float r[16];
+          tmem_ld16(tl + T_SACC + c0, r);
+          put8<kLo>(gb, OFF_ST, 128, 128, myrow, c0, r);
+          put8<kLo>(gb, OFF_ST, 128, 128, myrow, c0 + 8, r + 8);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) r[j] *= gC;
+          tmem_st16(tl + T_SACC + c0, r);
+        }
       }
       signal_ready(rdy_s);  // -> MMA-s: Y = S^T K^T, (Q S)^T = S^T Q^T
-      if (c > 0) emit_o(c - 1);  // the previous chunk's output
+      if (c > 0 && tid == 0) bulk_wait_read();  // the o tile's region is reused
       if (!simt_and(mbar_wait(done_a, parity, kWaitLimit))) { failed = true; break; }
       fence_after_sync();
 
@@ -806,11 +852,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         put8<kLo>(gb, OFF_Y, 128, kC, myrow, c0 + 8, r + 8);
       }
       signal_ready(rdy_y);  // -> MMA-d: Delta^T = U^T - Y (T diag(beta gamma))^T
+      if (c + 1 < nchunks) prefetch(c + 1);  // lands under the work below
       if (!simt_and(mbar_wait(done_d, parity, kWaitLimit))) { failed = true; break; }
       fence_after_sync();
-      if (c + 1 < nchunks) prefetch(c + 1);  // lands under the work below
 
-      // ------ phase 4: Delta^T, Delta^T diag(w) operands; S^T *= gamma_63
+      // ------------- phase 4: Delta^T, Delta^T diag(w) operands
       for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
         float u[16];
         tmem_ld16(tl + T_U + c0, u);
@@ -821,17 +867,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         put8<kLo>(gb, OFF_DTW, 128, kC, myrow, c0, u);
         put8<kLo>(gb, OFF_DTW, 128, kC, myrow, c0 + 8, u + 8);
       }
-      {
-        const float gC = gam[kC - 1];
-        for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
-          float r[16];
-          tmem_ld16(tl + T_SACC + c0, r);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) r[j] *= gC;
-          tmem_st16(tl + T_SACC + c0, r);
-        }
-      }
       signal_ready(rdy_d);  // -> MMA-3: (P Delta)^T;  MMA-4: S^T += ...
+      if (warp == 0 && c + 1 < nchunks) gates(c + 1);
       if (!simt_and(mbar_wait(done_4, parity, kWaitLimit))) { failed = true; break; }
       fence_after_sync();
       parity ^= 1u;
@@ -839,6 +876,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (!failed) {
       emit_o(nchunks - 1);
+      simt_sync();
+      if (tid == 0) store_o(nchunks - 1);
       float *Sh = S + head_off;
       for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
         float r[16];
@@ -849,6 +888,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (tid == 0) {
       atomicAdd(&g_prefill_timeouts, 1u);
     }
+    if (tid == 0) bulk_wait_all();  // no store of o outlives the CTA
   }
   // every product issued has finished (bounded: after a timeout the issuer
   // stops early and its drain commit still arrives)
@@ -861,6 +901,49 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 size_t prefill_workspace_bytes(int, int, int, int, int, int) { return 0; }
 
+namespace {
+
+// cuTensorMapEncodeTiled, from the driver through the runtime (the library
+// does not link the driver library itself); null if it is unavailable.
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Tensor map over a [B][T][heads][128] fp32 array (q, k, v or o) as a 4-d
+// tensor {128, heads, T, B}; one box is the 64 token rows of one head of one
+// sequence.  Rows past T are outside the tensor: zeros when loaded, skipped
+// when stored.
+cudaError_t rows_map(CUtensorMap *map, const float *base, int heads, int T,
+                     int B) {
+  const PFN_cuTensorMapEncodeTiled_v12000 fn = encode_tiled();
+  if (fn == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t row = (cuuint64_t)kD * sizeof(float);
+  const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)heads, (cuuint64_t)T,
+                              (cuuint64_t)B};
+  const cuuint64_t strides[3] = {row, row * (cuuint64_t)heads,
+                                 row * (cuuint64_t)heads * (cuuint64_t)T};
+  const cuuint32_t box[4] = {(cuuint32_t)kD, 1, (cuuint32_t)kC, 1};
+  const cuuint32_t step[4] = {1, 1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
+                        const_cast<float *>(base), dims, strides, box, step,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
 cudaError_t launch_prefill_chunked(float *S, const float *q, const float *k,
                                    const float *v, const float *g,
                                    const float *beta, float *o, int B, int kh,
@@ -869,19 +952,23 @@ cudaError_t launch_prefill_chunked(float *S, const float *q, const float *k,
   const size_t nheads = (size_t)B * vh;
   if (nheads == 0) return cudaSuccess;
   if (nheads > 0x7fffffffull) return cudaErrorInvalidConfiguration;
+  CUtensorMap tm_q, tm_k, tm_o;
   cudaError_t e;
+  if ((e = rows_map(&tm_q, q, kh, T, B)) != cudaSuccess) return e;
+  if ((e = rows_map(&tm_k, k, kh, T, B)) != cudaSuccess) return e;
+  if ((e = rows_map(&tm_o, o, vh, T, B)) != cudaSuccess) return e;
   if (precision == 1) {
     e = cudaFuncSetAttribute(gdn_chunk_kernel<true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
     if (e != cudaSuccess) return e;
     gdn_chunk_kernel<true><<<(unsigned)nheads, kThreads, kSmemAlloc, stream>>>(
-        S, q, k, v, g, beta, o, T, kh, vh, vh / kh);
+        S, tm_q, tm_k, v, g, beta, tm_o, T, kh, vh, vh / kh);
   } else {
     e = cudaFuncSetAttribute(gdn_chunk_kernel<false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
     if (e != cudaSuccess) return e;
     gdn_chunk_kernel<false><<<(unsigned)nheads, kThreads, kSmemAlloc, stream>>>(
-        S, q, k, v, g, beta, o, T, kh, vh, vh / kh);
+        S, tm_q, tm_k, v, g, beta, tm_o, T, kh, vh, vh / kh);
   }
   return cudaGetLastError();
 }

@@ -194,7 +194,10 @@ size_t gdn_prefill_workspace(const gdn_shape *shape, int T, int chunk,
  *   (a decay that empties the state is any g below about -104, where
  *   exp(g) is 0 in fp32; g = -inf would give NaN).  The token-serial path
  *   also accepts g = -inf.
- * 1 <= T <= GDN_MAX_TOKENS.  Other precision values give GDN_ERANGE.
+ * 1 <= T <= GDN_MAX_TOKENS; in the chunked modes also T * vh < 2^31
+ * (the tensor copies that move q, k and o address a sequence's rows with
+ * strides below 2^40 bytes).  Other values, and other precision values,
+ * give GDN_ERANGE.
  */
 int gdn_prefill(const gdn_shape *shape, int T, float *S, const float *q,
                 const float *k, const float *v, const float *g,
