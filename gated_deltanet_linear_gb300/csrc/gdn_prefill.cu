@@ -23,7 +23,7 @@
 // TMEM, lanes = M):
 //   MMA-a  G,H  [t'][s]  = [K; Q] K^T                       (A, B K-major)
 //   SIMT   S^T operand from TMEM, then S^T *= gamma_63 in TMEM (under MMA-a)
-//   MMA-s  Y    [dv][t]  = S^T K^T;  (Q S)^T [dv][t] = S^T Q^T
+//   MMA-s  [Y | (Q S)^T] [dv][t'] = S^T [K; Q]^T      (one N = 128 product)
 //   SIMT   o of the previous chunk;  A and P from G, H;
 //          T = (I + A)^-1, blocked 16 x 16, fp32 (under MMA-s)
 //   MMA-u  U^T  [dv][t]  = V^T (T diag(beta))^T             (A = V, MN-major)
@@ -37,9 +37,10 @@
 // Every operand a thread writes is a row it owns (a row of an input, or a
 // TMEM lane of an earlier result), stored 8 elements at a time; transposes
 // happen in the MMA descriptors (MN-major operands), never in memory.  The
-// next chunk's V rows and gates are loaded into registers, and its gate
-// vectors computed, while the current chunk's last products run; its K and
-// Q rows are bulk-copied into a staging tile earlier still.
+// next chunk's K and Q rows are tensor-copied into a staging tile about two
+// thirds of a chunk ahead; its V rows and gates are loaded into registers,
+// and its Q operand and gate vectors made, while the current chunk's last
+// products run.
 //
 // Precision.  Operands are bf16 in shared memory:
 //   split-bf16 ("BF16X3"): x = hi + lo with hi = bf16(x), lo = bf16(x - hi);
@@ -107,11 +108,13 @@ constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;  // room to align the base
 // TMEM columns (512 allocated).
 constexpr uint32_t T_SACC = 0;    // S^T: lanes dv, 128 columns dk
 constexpr uint32_t T_GH = 128;    // G (lanes 0-63), H (lanes 64-127): 64 columns
-constexpr uint32_t T_Y = 192;     // Y = S^T K^T: lanes dv, columns t
-constexpr uint32_t T_U = 256;     // second half-K of G, H; then U^T, then
+constexpr uint32_t T_U = 192;     // second half-K of G, H; then U^T, then
                                   // Delta^T = U^T - (W S)^T: lanes dv
-constexpr uint32_t T_QS = 320;    // (Q S)^T, two buffers (chunk parity): lanes dv
-constexpr uint32_t T_PD = 448;    // (P Delta)^T: lanes dv, columns t
+// Two buffers of 128 columns (chunk parity), lanes dv, columns t: MMA-s
+// writes [Y | (Q S)^T] in one product (B = [K; Q]); once Y has been read
+// out, MMA-3 writes (P Delta)^T over it, and the next chunk reads
+// [(P Delta)^T | (Q S)^T] for the output.
+constexpr uint32_t T_BUF = 256;
 
 constexpr uint32_t kWaitLimit = 1u << 24;
 
@@ -529,14 +532,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // warps report its operands ready; tcgen05.mma issue waits while the
     // tensor pipe is busy, and here that wait holds up no SIMT work.
     if (lane == 0) {
-      const Operand opKQ{sb + OFF_KQ, 128, 128, false};   // MMA-a A
-      const Operand opKb{sb + OFF_KQ, 128, 128, false};   // MMA-a, MMA-s B (rows 0-63)
+      const Operand opKQ{sb + OFF_KQ, 128, 128, false};   // MMA-a A; MMA-s B ([K; Q])
+      const Operand opKb{sb + OFF_KQ, 128, 128, false};   // MMA-a B (K: rows 0-63)
       const Operand opVmn{sb + OFF_V, 64, 128, true};     // MMA-u A
       const Operand opTB{sb + OFF_TB, 64, 64, false};     // MMA-d B
       const Operand opTB2{sb + OFF_TB2, 64, 64, false};   // MMA-u B
       const Operand opST{sb + OFF_ST, 128, 128, false};   // MMA-s A
       const Operand opY{sb + OFF_Y, 128, 64, false};      // MMA-d A
-      const Operand opQb{sb + OFF_KQ + 64 * 128, 128, 128, false};  // MMA-s B (Q rows)
       const Operand opDT{sb + OFF_DT, 128, 64, false};    // MMA-3 A
       const Operand opP{sb + OFF_P, 64, 64, false};       // MMA-3 B
       const Operand opDTW{sb + OFF_DTW, 128, 64, false};  // MMA-4 A
@@ -559,10 +561,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         commit(done_a);
         if (!mbar_wait(rdy_s, ph, kWaitLimit)) break;
         fence_after_sync();
-        gemm2<kLo, kD / 16>(
-            Gemm<kLo>(tmem + T_Y, opST, opKb, 128, kC, false),
-            Gemm<kLo>(tmem + T_QS + 64u * (uint32_t)(c & 1), opST, opQb, 128,
-                      kC, false));
+        gemm<kLo, kD / 16>(tmem + T_BUF + 128u * (uint32_t)(c & 1), opST, opKQ,
+                           128, 2 * kC, false);
         commit(done_s);
         if (!mbar_wait(rdy_t, ph, kWaitLimit)) break;
         fence_after_sync();
@@ -574,7 +574,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         commit(done_d);
         if (!mbar_wait(rdy_d, ph, kWaitLimit)) break;
         fence_after_sync();
-        gemm2<kLo, kC / 16>(Gemm<kLo>(tmem + T_PD, opDT, opP, 128, kC, false),
+        gemm2<kLo, kC / 16>(Gemm<kLo>(tmem + T_BUF + 128u * (uint32_t)(c & 1), opDT,
+                                      opP, 128, kC, false),
                             Gemm<kLo>(tmem + T_SACC, opDTW, opKnB, 128, kD, true));
         commit(done_4);
         ph ^= 1u;
@@ -635,11 +636,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *otile = reinterpret_cast<float *>(gb + OFF_OT);
     auto emit_o = [&](int cc) {
       const float *gm = gam_o + (cc & 1) * 64;
-      const uint32_t qs = T_QS + 64u * (uint32_t)(cc & 1);
+      const uint32_t pdq = T_BUF + 128u * (uint32_t)(cc & 1);
       for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
         float r[16], pd[16];
-        tmem_ld16(tl + qs + c0, r);
-        tmem_ld16(tl + T_PD + c0, pd);
+        tmem_ld16(tl + pdq + 64 + c0, r);
+        tmem_ld16(tl + pdq + c0, pd);
 #pragma unroll
         for (int j4 = 0; j4 < 16; j4 += 4) {
           const float4 g4 = *reinterpret_cast<const float4 *>(gm + c0 + j4);
@@ -699,20 +700,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) *fac = (gmax - gmin <= 160.f) ? 1 : 0;
     };
     if (warp == 0) gates(0);
-    uint32_t parity = 0;
-    bool failed = false;
-    for (int c = 0; c < nchunks; ++c) {
-      // ---------------------------------------------------- phase 0: inputs
-      // this chunk's K and Q rows are in the staging tile (its gates were
-      // written before the SIMT barrier that ended the previous wait)
-      if (!simt_and(mbar_wait(staged, parity, kWaitLimit))) { failed = true; break; }
-      // [K; Q] operand rows from the staging tile.
-      // Lanes 4-7 of each quarter warp read their two 16-byte halves in the
-      // other order, so each of the two loads covers all eight 16-byte bank
-      // groups of the quarter warp once.
+    // [K; Q] operand rows (tid >> 4) + 16 i, i0 <= i < i1 (K: i < 4), from
+    // the staging tile.  Lanes 4-7 of each quarter warp read their two
+    // 16-byte halves in the other order, so each of the two loads covers all
+    // eight 16-byte bank groups of the quarter warp once.
+    auto kq_rows = [&](int i0, int i1) {
       const int swap = (tid >> 2) & 1;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = i0; i < i1; ++i) {
         const int row = (tid >> 4) + 16 * i, c0 = (tid & 15) * 8;
         const float4 ya = *reinterpret_cast<const float4 *>(stage + row * 128 + c0 + 4 * swap);
         const float4 yb = *reinterpret_cast<const float4 *>(stage + row * 128 + c0 + 4 - 4 * swap);
@@ -720,6 +715,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
         put8<kLo>(gb, OFF_KQ, 128, 128, row, c0, x);
       }
+    };
+    uint32_t parity = 0;
+    bool failed = false;
+    for (int c = 0; c < nchunks; ++c) {
+      // ---------------------------------------------------- phase 0: inputs
+      // this chunk's K and Q rows are in the staging tile (its gates were
+      // written before the SIMT barrier that ended the previous wait)
+      if (!simt_and(mbar_wait(staged, parity, kWaitLimit))) { failed = true; break; }
+      // K operand rows (and for the first chunk Q's) from the staging tile;
+      // later chunks' Q rows were converted during the previous chunk's
+      // last products
+      if (c == 0)
+        kq_rows(0, 8);
+      else
+        kq_rows(0, 4);
       signal_ready(rdy_a);  // -> MMA-a: G, H = [K; Q] K^T
       if (c > 0) emit_o(c - 1);  // the previous chunk's output, into the o tile
       // V operand rows from registers (needed from MMA-u on)
@@ -847,7 +857,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_after_sync();
       for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
         float r[16];
-        tmem_ld16(tl + T_Y + c0, r);
+        tmem_ld16(tl + T_BUF + 128u * (uint32_t)(c & 1) + c0, r);
         put8<kLo>(gb, OFF_Y, 128, kC, myrow, c0, r);
         put8<kLo>(gb, OFF_Y, 128, kC, myrow, c0 + 8, r + 8);
       }
@@ -868,7 +878,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         put8<kLo>(gb, OFF_DTW, 128, kC, myrow, c0 + 8, u + 8);
       }
       signal_ready(rdy_d);  // -> MMA-3: (P Delta)^T;  MMA-4: S^T += ...
-      if (warp == 0 && c + 1 < nchunks) gates(c + 1);
+      if (c + 1 < nchunks) {
+        // Under MMA-3 and MMA-4: the next chunk's Q operand rows (this
+        // chunk's Q is consumed; MMA-4 reads only K's rows) and gates.
+        if (!simt_and(mbar_wait(staged, parity ^ 1u, kWaitLimit))) { failed = true; break; }
+        kq_rows(4, 8);
+        if (warp == 0) gates(c + 1);
+      }
       if (!simt_and(mbar_wait(done_4, parity, kWaitLimit))) { failed = true; break; }
       fence_after_sync();
       parity ^= 1u;
