@@ -22,21 +22,23 @@
 // the SIMT work on A and its inverse.  Per chunk (D = M x N accumulator in
 // TMEM, lanes = M):
 //   MMA-a  G,H  [t'][s]  = [K; Q] K^T                       (A, B K-major)
-//   SIMT   S^T operand from TMEM, then S^T *= gamma_63 in TMEM (under MMA-a)
+//   SIMT   S^T operand, then S^T *= gamma_63, both in TMEM (under MMA-a)
 //   MMA-s  [Y | (Q S)^T] [dv][t'] = S^T [K; Q]^T      (one N = 128 product)
 //   SIMT   o of the previous chunk;  A and P from G, H;
 //          T = (I + A)^-1, blocked 16 x 16, fp32 (under MMA-s)
 //   MMA-u  U^T  [dv][t]  = V^T (T diag(beta))^T             (A = V, MN-major)
-//   SIMT   Y operand from TMEM (under MMA-u)
-//   MMA-d  Delta^T = U^T - Y (T diag(beta gamma))^T   (negated A onto U^T)
-//   SIMT   Delta^T and Delta^T diag(w) operands
+//   SIMT   -Y operand in TMEM (under MMA-u)
+//   MMA-d  Delta^T = U^T + (-Y) (T diag(beta gamma))^T   (onto U^T)
+//   SIMT   Delta^T and Delta^T diag(w) operands in TMEM
 //   MMA-3  (P Delta)^T = Delta^T P^T
 //   MMA-4  S^T += (Delta^T diag(w)) K                        (B = K, MN-major)
 //   SIMT   O^T = diag(gamma) (Q S)^T + (P Delta)^T  -> o, emitted in the
 //          next chunk while its first products run
-// Every operand a thread writes is a row it owns (a row of an input, or a
-// TMEM lane of an earlier result), stored 8 elements at a time; transposes
-// happen in the MMA descriptors (MN-major operands), never in memory.  The
+// Every operand a thread writes is a row it owns: a row of an input, stored
+// in shared memory 8 elements at a time, or a TMEM lane of an earlier
+// result, which stays in its lane as an A operand in TMEM (S^T, -Y,
+// Delta^T); transposes happen in the MMA descriptors (MN-major operands),
+// never in memory.  The
 // next chunk's K and Q rows are tensor-copied into a staging tile about two
 // thirds of a chunk ahead; its V rows and gates are loaded into registers,
 // and its Q operand and gate vectors made, while the current chunk's last
@@ -78,25 +80,21 @@ constexpr int kThreads = kSimt + 64;
 // each).  Regions (byte offsets from a 1024-aligned base) are reused by
 // phase:
 //   Ra 64 KB: [K; Q] (128 x 128), the whole chunk
-//   Rb 32 KB: V (64 x 128)            -> Y (128 x 64) -> Delta^T (128 x 64)
-//   Rc 32 KB: o of the previous chunk (fp32 [t][dv], 64 x 128, read by
-//             bulk stores before the A build)
+//   Rb 32 KB: V (64 x 128)
+//   Rc 32 KB: o of the previous chunk (fp32 [t][dv], 64 x 128, read by a
+//             tensor store before the A build)
 //                                     -> A, T scratch (fp32)
 //                                     -> T diag(bg), T diag(b) (64 x 64 each)
-//                                     -> Delta^T diag(w) (128 x 64)
-//   Rd 64 KB: S^T (128 x 128)         -> fp32 [K; Q] of the next chunk
+//   Rd 64 KB: fp32 [K; Q] of the next chunk (staging)
 //   Rp 16 KB: P (64 x 64)
+// The operands made from TMEM results (S^T, Y, Delta^T) stay in TMEM.
 constexpr uint32_t RA = 0, RB = 65536, RC = 98304, RD = 131072, RP = 196608;
 constexpr uint32_t OFF_KQ = RA;             // 128 x 128
 constexpr uint32_t OFF_V = RB;              // 64 x 128
-constexpr uint32_t OFF_Y = RB;              // 128 x 64 (after MMA-u)
-constexpr uint32_t OFF_DT = RB;             // 128 x 64 (after MMA-d)
 constexpr uint32_t OFF_OT = RC;             // fp32 o tile [64][128]
 constexpr uint32_t OFF_SCR = RC;            // fp32 A [64][64] + T [64][64]
 constexpr uint32_t OFF_TB = RC;             // 64 x 64: T diag(beta gamma)
 constexpr uint32_t OFF_TB2 = RC + 16384;    // 64 x 64: T diag(beta)
-constexpr uint32_t OFF_DTW = RC;            // 128 x 64 (after MMA-d)
-constexpr uint32_t OFF_ST = RD;             // 128 x 128
 constexpr uint32_t OFF_P = RP;              // 64 x 64
 constexpr uint32_t OFF_VEC = RP + 16384;    // Gamma, gamma, w, beta, gamma x 2, ea, eb
 constexpr uint32_t OFF_STAGE = RD;          // fp32 [K; Q] of the next chunk (64 KB)
@@ -110,11 +108,16 @@ constexpr uint32_t T_SACC = 0;    // S^T: lanes dv, 128 columns dk
 constexpr uint32_t T_GH = 128;    // G (lanes 0-63), H (lanes 64-127): 64 columns
 constexpr uint32_t T_U = 192;     // second half-K of G, H; then U^T, then
                                   // Delta^T = U^T - (W S)^T: lanes dv
-// Two buffers of 128 columns (chunk parity), lanes dv, columns t: MMA-s
-// writes [Y | (Q S)^T] in one product (B = [K; Q]); once Y has been read
-// out, MMA-3 writes (P Delta)^T over it, and the next chunk reads
-// [(P Delta)^T | (Q S)^T] for the output.
+// 128 columns, lanes dv, columns t: MMA-s writes [Y | (Q S)^T] in one
+// product (B = [K; Q]); once Y has been read out, MMA-3 writes
+// (P Delta)^T over it, and the next chunk reads [(P Delta)^T | (Q S)^T]
+// for the output before its own MMA-s is issued.
 constexpr uint32_t T_BUF = 256;
+// 128 columns of bf16 A operands (lanes dv, two elements per column), hi
+// then lo: S^T (64 + 64 columns, K = dk) for MMA-s; then -Y (32 + 32, K =
+// t) for MMA-d; then Delta^T (32 + 32) and Delta^T diag(w) (the next 64)
+// for MMA-3 and MMA-4.
+constexpr uint32_t T_AOP = 384;
 
 constexpr uint32_t kWaitLimit = 1u << 24;
 
@@ -143,6 +146,27 @@ __device__ __forceinline__ void put8(unsigned char *gb, uint32_t off, int R,
   if (kLo)
     *reinterpret_cast<uint4 *>(gb + o + (uint32_t)(R * C * 2)) =
         make_uint4(lo[0], lo[1], lo[2], lo[3]);
+}
+
+// Columns c0 .. c0+15 (c0 % 16 == 0) of this thread's lane of a bf16 A
+// operand in tensor memory whose hi part starts at TMEM address `hi` and lo
+// part at `lo` (both including the lane): two elements per 32-bit column.
+// The stores are asynchronous; tmem_wait_st completes them.
+template <bool kLo>
+__device__ __forceinline__ void put16_tmem(uint32_t hi, uint32_t lo, int c0,
+                                           const float *x) {
+  uint32_t h[8], l[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+    h[i] = bf2_bits(v);
+    if (kLo) {
+      const float2 f = __bfloat1622float2(v);
+      l[i] = bf2_bits(__floats2bfloat162_rn(x[2 * i] - f.x, x[2 * i + 1] - f.y));
+    }
+  }
+  tmem_st8_async(hi + (uint32_t)(c0 >> 1), h);
+  if (kLo) tmem_st8_async(lo + (uint32_t)(c0 >> 1), l);
 }
 
 // Shared-memory descriptor of K step ks (16 bf16 of K) of a tile:
@@ -225,11 +249,42 @@ __device__ __forceinline__ void gemm(uint32_t d, const Operand &a,
   for (int ks = 0; ks < KSTEPS; ++ks) g.step(ks, ks == 0);
 }
 
+// The same with A in tensor memory (see mma_bf16_ta): the hi and lo parts
+// of A start at TMEM addresses a and a_lo, and K step ks is 8 columns on.
+template <bool kLo>
+struct GemmT {
+  uint32_t d, id, a, al;
+  uint64_t bh, bl;
+  const Operand *b;
+  bool accumulate;
+  __device__ __forceinline__ GemmT(uint32_t d_, uint32_t a_, uint32_t a_lo,
+                                   const Operand &b_, int M, int N,
+                                   bool accumulate_)
+      : d(d_), id(idesc_bf16(M, N, 0, b_.mn)), a(a_), al(a_lo),
+        bh(opdesc(b_, false)), bl(kLo ? opdesc(b_, true) : 0), b(&b_),
+        accumulate(accumulate_) {}
+  __device__ __forceinline__ void step(int ks, bool first) const {
+    const uint64_t bo = kstep16(*b, ks);
+    const uint32_t ao = 8u * (uint32_t)ks;
+    mma_bf16_ta(d, a + ao, bh + bo, id, (accumulate || !first) ? 1u : 0u);
+    if (kLo) {
+      mma_bf16_ta(d, a + ao, bl + bo, id, 1u);
+      mma_bf16_ta(d, al + ao, bh + bo, id, 1u);
+    }
+  }
+};
+
+template <int KSTEPS, class G>
+__device__ __forceinline__ void gemm_steps(const G &g) {
+#pragma unroll
+  for (int ks = 0; ks < KSTEPS; ++ks) g.step(ks, ks == 0);
+}
+
 // Two independent products (different accumulators), their K steps
 // interleaved so that one product's dependent chain runs while the other's
 // waits.
-template <bool kLo, int KSTEPS>
-__device__ __forceinline__ void gemm2(const Gemm<kLo> &x, const Gemm<kLo> &y) {
+template <int KSTEPS, class GX, class GY>
+__device__ __forceinline__ void gemm2(const GX &x, const GY &y) {
 #pragma unroll
   for (int ks = 0; ks < KSTEPS; ++ks) {
     x.step(ks, ks == 0);
@@ -537,11 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Operand opVmn{sb + OFF_V, 64, 128, true};     // MMA-u A
       const Operand opTB{sb + OFF_TB, 64, 64, false};     // MMA-d B
       const Operand opTB2{sb + OFF_TB2, 64, 64, false};   // MMA-u B
-      const Operand opST{sb + OFF_ST, 128, 128, false};   // MMA-s A
-      const Operand opY{sb + OFF_Y, 128, 64, false};      // MMA-d A
-      const Operand opDT{sb + OFF_DT, 128, 64, false};    // MMA-3 A
       const Operand opP{sb + OFF_P, 64, 64, false};       // MMA-3 B
-      const Operand opDTW{sb + OFF_DTW, 128, 64, false};  // MMA-4 A
       const Operand opKnB{sb + OFF_KQ, 128, 128, true};   // MMA-4 B (K rows)
       uint32_t ph = 0;
       for (int c = 0; c < nchunks; ++c) {
@@ -561,8 +612,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         commit(done_a);
         if (!mbar_wait(rdy_s, ph, kWaitLimit)) break;
         fence_after_sync();
-        gemm<kLo, kD / 16>(tmem + T_BUF + 128u * (uint32_t)(c & 1), opST, opKQ,
-                           128, 2 * kC, false);
+        gemm_steps<kD / 16>(GemmT<kLo>(tmem + T_BUF, tmem + T_AOP, tmem + T_AOP + 64,
+                                       opKQ, 128, 2 * kC, false));
         commit(done_s);
         if (!mbar_wait(rdy_t, ph, kWaitLimit)) break;
         fence_after_sync();
@@ -570,13 +621,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         commit(done_u);  // V's region then takes the Y operand
         if (!mbar_wait(rdy_y, ph, kWaitLimit)) break;
         fence_after_sync();
-        gemm<kLo, kC / 16>(tmem + T_U, opY, opTB, 128, kC, true, true);
+        gemm_steps<kC / 16>(GemmT<kLo>(tmem + T_U, tmem + T_AOP, tmem + T_AOP + 32,
+                                       opTB, 128, kC, true));
         commit(done_d);
         if (!mbar_wait(rdy_d, ph, kWaitLimit)) break;
         fence_after_sync();
-        gemm2<kLo, kC / 16>(Gemm<kLo>(tmem + T_BUF + 128u * (uint32_t)(c & 1), opDT,
-                                      opP, 128, kC, false),
-                            Gemm<kLo>(tmem + T_SACC, opDTW, opKnB, 128, kD, true));
+        gemm2<kC / 16>(GemmT<kLo>(tmem + T_BUF, tmem + T_AOP, tmem + T_AOP + 32, opP,
+                                  128, kC, false),
+                       GemmT<kLo>(tmem + T_SACC, tmem + T_AOP + 64, tmem + T_AOP + 96,
+                                  opKnB, 128, kD, true));
         commit(done_4);
         ph ^= 1u;
       }
@@ -636,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *otile = reinterpret_cast<float *>(gb + OFF_OT);
     auto emit_o = [&](int cc) {
       const float *gm = gam_o + (cc & 1) * 64;
-      const uint32_t pdq = T_BUF + 128u * (uint32_t)(cc & 1);
+      const uint32_t pdq = T_BUF;
       for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
         float r[16], pd[16];
         tmem_ld16(tl + pdq + 64 + c0, r);
@@ -744,22 +797,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       simt_sync();          // the staging tile is read; its region is reused
       if (c > 0 && tid == 0) store_o(c - 1);
 
-      // ------------- phase 1: S^T operand (rows dv, columns dk) from TMEM;
-      // the accumulator is then decayed in place, S^T *= gamma_63, ready for
+      // ------------- phase 1: S^T operand (lane dv, K = dk) in TMEM; the
+      // accumulator is then decayed in place, S^T *= gamma_63, ready for
       // MMA-4 (nothing reads it in between: MMA-s reads the operand)
       {
         const float gC = gam[kC - 1];
         for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
           float r[16];
           tmem_ld16(tl + T_SACC + c0, r);
-          put8<kLo>(gb, OFF_ST, 128, 128, myrow, c0, r);
-          put8<kLo>(gb, OFF_ST, 128, 128, myrow, c0 + 8, r + 8);
+          put16_tmem<kLo>(tl + T_AOP, tl + T_AOP + 64, c0, r);
 #pragma unroll
           for (int j = 0; j < 16; ++j) r[j] *= gC;
-          tmem_st16(tl + T_SACC + c0, r);
+          tmem_st16(tl + T_SACC + c0, r);  // waits for this thread's stores
         }
       }
-      signal_ready(rdy_s);  // -> MMA-s: Y = S^T K^T, (Q S)^T = S^T Q^T
+      signal_ready(rdy_s);  // -> MMA-s: [Y | (Q S)^T] = S^T [K; Q]^T
       if (c > 0 && tid == 0) bulk_wait_read();  // the o tile's region is reused
       if (!simt_and(mbar_wait(done_a, parity, kWaitLimit))) { failed = true; break; }
       fence_after_sync();
@@ -851,32 +903,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       signal_ready(rdy_t);  // -> MMA-u: U^T = V^T (T diag(beta))^T
 
-      // -------------------------------- phase 3: Y operand (lane dv, cols t)
+      // ------------- phase 3: -Y operand in TMEM (lane dv, K = t)
       if (!simt_and(mbar_wait(done_s, parity, kWaitLimit) &&
                     mbar_wait(done_u, parity, kWaitLimit))) { failed = true; break; }
       fence_after_sync();
       for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
         float r[16];
-        tmem_ld16(tl + T_BUF + 128u * (uint32_t)(c & 1) + c0, r);
-        put8<kLo>(gb, OFF_Y, 128, kC, myrow, c0, r);
-        put8<kLo>(gb, OFF_Y, 128, kC, myrow, c0 + 8, r + 8);
+        tmem_ld16(tl + T_BUF + c0, r);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) r[e] = -r[e];  // split of -Y: exact negation
+        put16_tmem<kLo>(tl + T_AOP, tl + T_AOP + 32, c0, r);
       }
+      tmem_wait_st();
       signal_ready(rdy_y);  // -> MMA-d: Delta^T = U^T - Y (T diag(beta gamma))^T
       if (c + 1 < nchunks) prefetch(c + 1);  // lands under the work below
       if (!simt_and(mbar_wait(done_d, parity, kWaitLimit))) { failed = true; break; }
       fence_after_sync();
 
-      // ------------- phase 4: Delta^T, Delta^T diag(w) operands
+      // ------------- phase 4: Delta^T, Delta^T diag(w) operands in TMEM
       for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
         float u[16];
         tmem_ld16(tl + T_U + c0, u);
-        put8<kLo>(gb, OFF_DT, 128, kC, myrow, c0, u);
-        put8<kLo>(gb, OFF_DT, 128, kC, myrow, c0 + 8, u + 8);
+        put16_tmem<kLo>(tl + T_AOP, tl + T_AOP + 32, c0, u);
 #pragma unroll
         for (int e = 0; e < 16; ++e) u[e] *= wv[c0 + e];
-        put8<kLo>(gb, OFF_DTW, 128, kC, myrow, c0, u);
-        put8<kLo>(gb, OFF_DTW, 128, kC, myrow, c0 + 8, u + 8);
+        put16_tmem<kLo>(tl + T_AOP + 64, tl + T_AOP + 96, c0, u);
       }
+      tmem_wait_st();
       signal_ready(rdy_d);  // -> MMA-3: (P Delta)^T;  MMA-4: S^T += ...
       if (c + 1 < nchunks) {
         // Under MMA-3 and MMA-4: the next chunk's Q operand rows (this

@@ -53,6 +53,20 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a,
       "l"(a), "l"(b), "r"(id), "r"(accumulate));
 }
 
+// The same product with A in tensor memory: A's row m is TMEM lane m, and
+// its K elements are packed two bf16 per 32-bit column (the lower index in
+// the low half), so one K step of 16 elements is 8 columns.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem,
+                                            uint64_t b, uint32_t id,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate));
+}
+
 // Arrive on the mbarrier once every tcgen05 operation issued so far by this
 // thread has completed.
 __device__ __forceinline__ void commit(uint32_t mbar) {
@@ -129,6 +143,21 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&r)[16]) 
       "r"(__float_as_uint(r[12])), "r"(__float_as_uint(r[13])),
       "r"(__float_as_uint(r[14])), "r"(__float_as_uint(r[15]))
       : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 32 lanes x 8 columns of 32-bit values from registers, without waiting for
+// completion (tmem_wait_st does, before the values are used elsewhere).
+__device__ __forceinline__ void tmem_st8_async(uint32_t taddr, const uint32_t (&u)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, "
+      "%8};" ::"r"(taddr),
+      "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]),
+      "r"(u[6]), "r"(u[7])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
