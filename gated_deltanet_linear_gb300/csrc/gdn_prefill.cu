@@ -80,7 +80,7 @@ constexpr int kThreads = kSimt + 64;
 // each).  Regions (byte offsets from a 1024-aligned base) are reused by
 // phase:
 //   Ra 64 KB: [K; Q] (128 x 128), the whole chunk
-//   Rb 32 KB: V (64 x 128)
+//   Rb 32 KB: fp32 V rows of the chunk (staging) -> V (64 x 128)
 //   Rc 32 KB: o of the previous chunk (fp32 [t][dv], 64 x 128, read by a
 //             tensor store before the A build)
 //                                     -> A, T scratch (fp32)
@@ -98,8 +98,8 @@ constexpr uint32_t OFF_TB2 = RC + 16384;    // 64 x 64: T diag(beta)
 constexpr uint32_t OFF_P = RP;              // 64 x 64
 constexpr uint32_t OFF_VEC = RP + 16384;    // Gamma, gamma, w, beta, gamma x 2, ea, eb
 constexpr uint32_t OFF_STAGE = RD;          // fp32 [K; Q] of the next chunk (64 KB)
-constexpr uint32_t OFF_BAR = OFF_VEC + 2048;  // 12 mbarriers
-constexpr uint32_t OFF_SLOT = OFF_BAR + 96;   // TMEM address; +104: int flag
+constexpr uint32_t OFF_BAR = OFF_VEC + 2048;  // 13 mbarriers
+constexpr uint32_t OFF_SLOT = OFF_BAR + 104;  // TMEM address; +112: int flag
 constexpr uint32_t kSmemUsed = OFF_BAR + 128;
 constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;  // room to align the base
 
@@ -504,7 +504,8 @@ template <bool kLo>
 __global__ void __launch_bounds__(kThreads, 1)
     gdn_chunk_kernel(float *__restrict__ S, const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
-                     const float *__restrict__ v, const float *__restrict__ g,
+                     const __grid_constant__ CUtensorMap tm_v,
+                     const float *__restrict__ g,
                      const float *__restrict__ beta,
                      const __grid_constant__ CUtensorMap tm_o, int T, int kh,
                      int vh, int rep) {
@@ -522,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // every factor is a normal fp32 number
   float *ea = Gam + 384;
   float *eb = Gam + 448;
-  volatile int *fac = reinterpret_cast<volatile int *>(gb + OFF_BAR + 104);
+  volatile int *fac = reinterpret_cast<volatile int *>(gb + OFF_BAR + 112);
   const float *stage = reinterpret_cast<const float *>(gb + OFF_STAGE);
   // mbarriers: products done (one commit each), operands ready (kSimt
   // arrivals each), and the final drain
@@ -534,6 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t drain = bar0 + 72;
   const uint32_t staged = bar0 + 80;  // next K, Q rows in the staging tile
   const uint32_t done_u = bar0 + 88;
+  const uint32_t vstaged = bar0 + 96;  // this chunk's fp32 V rows in region Rb
   volatile uint32_t *slot = reinterpret_cast<volatile uint32_t *>(gb + OFF_SLOT);
   float *Asc = reinterpret_cast<float *>(gb + OFF_SCR);
   float *Tsc = Asc + 64 * 64;
@@ -557,6 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(drain, 1);
     mbar_init(staged, 1);
     mbar_init(done_u, 1);
+    mbar_init(vstaged, 1);
   }
   cta_sync_tc();
   const uint32_t tmem = *slot;
@@ -566,9 +569,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // K and Q rows of chunk c, fp32, into the staging tile [128 rows: K then
     // Q][128] as soon as it is free: before the loop for chunk 0, else once
     // MMA-s of chunk c-1 has consumed the S^T operand that shares its region
-    // (about two thirds of a chunk ahead of use).  One tensor copy of 64
-    // rows each; rows past T arrive as zeros.
-    int issued = -1;
+    // (about two thirds of a chunk ahead of use).  Then its fp32 V rows
+    // into region Rb once MMA-u of chunk c-1 has consumed the V operand
+    // there.  One tensor copy of 64 rows each; rows past T arrive as zeros.
+    int issued = -1, v_issued = -1;
     for (int c = 0; c < nchunks; ++c) {
       if (c > 0 && !mbar_wait(done_s, (uint32_t)((c - 1) & 1), kWaitLimit)) break;
       if (lane == 0) {
@@ -578,9 +582,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       issued = c;
+      if (c > 0 && !mbar_wait(done_u, (uint32_t)((c - 1) & 1), kWaitLimit)) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(vstaged, kC * 512u);
+        tma_load_rows(sb + OFF_V, &tm_v, vi, c * kC, b, vstaged);
+      }
+      __syncwarp();
+      v_issued = c;
     }
     // nothing may still be copying into shared memory when the CTA ends
     if (issued >= 0) mbar_wait(staged, (uint32_t)(issued & 1), kWaitLimit);
+    if (v_issued >= 0) mbar_wait(vstaged, (uint32_t)(v_issued & 1), kWaitLimit);
   } else if (warp == kIssuer) {
     // ------------------------------------------------ the issuing warp
     // One thread issues every product of every chunk as soon as the SIMT
@@ -640,28 +652,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ the SIMT warps
     const uint32_t tl = tmem + lane_base;
 
-    // Next chunk's V rows (tid >> 4) + 16 i, i = 0..3, columns
-    // (tid & 15) * 8 .. + 7 in registers; on warp 0, the gates of tokens
-    // lane and lane + 32.  (K and Q come through the staging tile.)
-    float4 pv[8];
+    // On warp 0, the next chunk's gates of tokens lane and lane + 32 in
+    // registers.  (K, Q and V come through staging tiles.)
     float pg[2], pb[2];
     auto prefetch = [&](int c) {
       const int t0 = c * kC;
       const int n = min(kC, T - t0);
       const size_t v_base = ((size_t)b * T + t0) * vh + vi;
-      const int c0 = (tid & 15) * 8;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int t = (tid >> 4) + 16 * i;
-        if (t < n) {
-          const float *src = v + (v_base + (size_t)t * vh) * kD + c0;
-          pv[2 * i] = __ldg(reinterpret_cast<const float4 *>(src));
-          pv[2 * i + 1] = __ldg(reinterpret_cast<const float4 *>(src + 4));
-        } else {
-          pv[2 * i] = make_float4(0.f, 0.f, 0.f, 0.f);
-          pv[2 * i + 1] = pv[2 * i];
-        }
-      }
       if (warp == 0) {
         pg[0] = lane < n ? __ldg(g + v_base + (size_t)lane * vh) : 0.f;
         pg[1] = lane + 32 < n ? __ldg(g + v_base + (size_t)(lane + 32) * vh) : 0.f;
@@ -669,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         pb[1] = lane + 32 < n ? __ldg(beta + v_base + (size_t)(lane + 32) * vh) : 0.f;
       }
     };
-    prefetch(0);
+    if (warp == 0) prefetch(0);
 
     // State in: S[dk][dv] -> TMEM lane dv, column dk.
     {
@@ -785,17 +782,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         kq_rows(0, 4);
       signal_ready(rdy_a);  // -> MMA-a: G, H = [K; Q] K^T
       if (c > 0) emit_o(c - 1);  // the previous chunk's output, into the o tile
-      // V operand rows from registers (needed from MMA-u on)
+      // V operand rows (needed from MMA-u on), converted in place: the fp32
+      // rows (tid >> 4) + 16 i are read into registers (same bank order as
+      // kq_rows), then, after a barrier, written back as bf16 operand rows
+      float vx[4][8];
+      if (!simt_and(mbar_wait(vstaged, parity, kWaitLimit))) { failed = true; break; }
+      {
+        const float *vst = reinterpret_cast<const float *>(gb + OFF_V);
+        const int swap = (tid >> 2) & 1, c0 = (tid & 15) * 8;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int row = (tid >> 4) + 16 * i, c0 = (tid & 15) * 8;
-        const float x[8] = {pv[2 * i].x, pv[2 * i].y, pv[2 * i].z, pv[2 * i].w,
-                            pv[2 * i + 1].x, pv[2 * i + 1].y, pv[2 * i + 1].z,
-                            pv[2 * i + 1].w};
-        put8<kLo>(gb, OFF_V, 64, 128, row, c0, x);
+        for (int i = 0; i < 4; ++i) {
+          const int row = (tid >> 4) + 16 * i;
+          const float4 ya = *reinterpret_cast<const float4 *>(vst + row * 128 + c0 + 4 * swap);
+          const float4 yb = *reinterpret_cast<const float4 *>(vst + row * 128 + c0 + 4 - 4 * swap);
+          const float4 x0 = swap ? yb : ya, x1 = swap ? ya : yb;
+          vx[i][0] = x0.x; vx[i][1] = x0.y; vx[i][2] = x0.z; vx[i][3] = x0.w;
+          vx[i][4] = x1.x; vx[i][5] = x1.y; vx[i][6] = x1.z; vx[i][7] = x1.w;
+        }
       }
-      simt_sync();          // the staging tile is read; its region is reused
+      simt_sync();  // the staging tiles and the o tile's writes are done
       if (c > 0 && tid == 0) store_o(c - 1);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        put8<kLo>(gb, OFF_V, 64, 128, (tid >> 4) + 16 * i, (tid & 15) * 8, vx[i]);
 
       // ------------- phase 1: S^T operand (lane dv, K = dk) in TMEM; the
       // accumulator is then decayed in place, S^T *= gamma_63, ready for
@@ -916,7 +925,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_wait_st();
       signal_ready(rdy_y);  // -> MMA-d: Delta^T = U^T - Y (T diag(beta gamma))^T
-      if (c + 1 < nchunks) prefetch(c + 1);  // lands under the work below
+      if (warp == 0 && c + 1 < nchunks) prefetch(c + 1);  // lands under the work below
       if (!simt_and(mbar_wait(done_d, parity, kWaitLimit))) { failed = true; break; }
       fence_after_sync();
 
@@ -1021,23 +1030,24 @@ cudaError_t launch_prefill_chunked(float *S, const float *q, const float *k,
   const size_t nheads = (size_t)B * vh;
   if (nheads == 0) return cudaSuccess;
   if (nheads > 0x7fffffffull) return cudaErrorInvalidConfiguration;
-  CUtensorMap tm_q, tm_k, tm_o;
+  CUtensorMap tm_q, tm_k, tm_v, tm_o;
   cudaError_t e;
   if ((e = rows_map(&tm_q, q, kh, T, B)) != cudaSuccess) return e;
   if ((e = rows_map(&tm_k, k, kh, T, B)) != cudaSuccess) return e;
+  if ((e = rows_map(&tm_v, v, vh, T, B)) != cudaSuccess) return e;
   if ((e = rows_map(&tm_o, o, vh, T, B)) != cudaSuccess) return e;
   if (precision == 1) {
     e = cudaFuncSetAttribute(gdn_chunk_kernel<true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
     if (e != cudaSuccess) return e;
     gdn_chunk_kernel<true><<<(unsigned)nheads, kThreads, kSmemAlloc, stream>>>(
-        S, tm_q, tm_k, v, g, beta, tm_o, T, kh, vh, vh / kh);
+        S, tm_q, tm_k, tm_v, g, beta, tm_o, T, kh, vh, vh / kh);
   } else {
     e = cudaFuncSetAttribute(gdn_chunk_kernel<false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
     if (e != cudaSuccess) return e;
     gdn_chunk_kernel<false><<<(unsigned)nheads, kThreads, kSmemAlloc, stream>>>(
-        S, tm_q, tm_k, v, g, beta, tm_o, T, kh, vh, vh / kh);
+        S, tm_q, tm_k, tm_v, g, beta, tm_o, T, kh, vh, vh / kh);
   }
   return cudaGetLastError();
 }
