@@ -26,9 +26,10 @@
 //   MMA-s  [Y | (Q S)^T] [dv][t'] = S^T [K; Q]^T      (one N = 128 product)
 //   SIMT   o of the previous chunk;  A and P from G, H;
 //          T = (I + A)^-1, blocked 16 x 16, fp32 (under MMA-s)
+//   SIMT   -Y operand in TMEM (MMA-s is done by then)
 //   MMA-u  U^T  [dv][t]  = V^T (T diag(beta))^T             (A = V, MN-major)
-//   SIMT   -Y operand in TMEM (under MMA-u)
-//   MMA-d  Delta^T = U^T + (-Y) (T diag(beta gamma))^T   (onto U^T)
+//   MMA-d  Delta^T = U^T + (-Y) (T diag(beta gamma))^T   (onto U^T, right
+//          after MMA-u)
 //   SIMT   Delta^T and Delta^T diag(w) operands in TMEM
 //   MMA-3  (P Delta)^T = Delta^T P^T
 //   MMA-4  S^T += (Delta^T diag(w)) K                        (B = K, MN-major)
@@ -98,8 +99,8 @@ constexpr uint32_t OFF_TB2 = RC + 16384;    // 64 x 64: T diag(beta)
 constexpr uint32_t OFF_P = RP;              // 64 x 64
 constexpr uint32_t OFF_VEC = RP + 16384;    // Gamma, gamma, w, beta, gamma x 2, ea, eb
 constexpr uint32_t OFF_STAGE = RD;          // fp32 [K; Q] of the next chunk (64 KB)
-constexpr uint32_t OFF_BAR = OFF_VEC + 2048;  // 13 mbarriers
-constexpr uint32_t OFF_SLOT = OFF_BAR + 104;  // TMEM address; +112: int flag
+constexpr uint32_t OFF_BAR = OFF_VEC + 2048;  // 12 mbarriers
+constexpr uint32_t OFF_SLOT = OFF_BAR + 96;   // TMEM address; +104: int flag
 constexpr uint32_t kSmemUsed = OFF_BAR + 128;
 constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;  // room to align the base
 
@@ -523,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // every factor is a normal fp32 number
   float *ea = Gam + 384;
   float *eb = Gam + 448;
-  volatile int *fac = reinterpret_cast<volatile int *>(gb + OFF_BAR + 112);
+  volatile int *fac = reinterpret_cast<volatile int *>(gb + OFF_BAR + 104);
   const float *stage = reinterpret_cast<const float *>(gb + OFF_STAGE);
   // mbarriers: products done (one commit each), operands ready (kSimt
   // arrivals each), and the final drain
@@ -531,11 +532,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t done_a = bar0, done_s = bar0 + 8, done_d = bar0 + 16,
                  done_4 = bar0 + 24;
   const uint32_t rdy_a = bar0 + 32, rdy_s = bar0 + 40, rdy_t = bar0 + 48,
-                 rdy_y = bar0 + 56, rdy_d = bar0 + 64;
-  const uint32_t drain = bar0 + 72;
-  const uint32_t staged = bar0 + 80;  // next K, Q rows in the staging tile
-  const uint32_t done_u = bar0 + 88;
-  const uint32_t vstaged = bar0 + 96;  // this chunk's fp32 V rows in region Rb
+                 rdy_d = bar0 + 56;
+  const uint32_t drain = bar0 + 64;
+  const uint32_t staged = bar0 + 72;   // next K, Q rows in the staging tile
+  const uint32_t done_u = bar0 + 80;
+  const uint32_t vstaged = bar0 + 88;  // this chunk's fp32 V rows in region Rb
   volatile uint32_t *slot = reinterpret_cast<volatile uint32_t *>(gb + OFF_SLOT);
   float *Asc = reinterpret_cast<float *>(gb + OFF_SCR);
   float *Tsc = Asc + 64 * 64;
@@ -555,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) tmem_alloc(sb + OFF_SLOT, 512);
   if (tid == 0) {
     for (int i = 0; i < 4; ++i) mbar_init(bar0 + 8 * i, 1);
-    for (int i = 4; i < 9; ++i) mbar_init(bar0 + 8 * i, kSimt);
+    for (int i = 4; i < 8; ++i) mbar_init(bar0 + 8 * i, kSimt);
     mbar_init(drain, 1);
     mbar_init(staged, 1);
     mbar_init(done_u, 1);
@@ -630,9 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(rdy_t, ph, kWaitLimit)) break;
         fence_after_sync();
         gemm<kLo, kC / 16>(tmem + T_U, opVmn, opTB2, 128, kC, false);
-        commit(done_u);  // V's region then takes the Y operand
-        if (!mbar_wait(rdy_y, ph, kWaitLimit)) break;
-        fence_after_sync();
+        commit(done_u);  // V's region then takes the next chunk's V rows
         gemm_steps<kC / 16>(GemmT<kLo>(tmem + T_U, tmem + T_AOP, tmem + T_AOP + 32,
                                        opTB, 128, kC, true));
         commit(done_d);
@@ -884,6 +883,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       simt_sync();
       tri_inverse(Asc, Tsc, tid);
+
+      // -Y operand in TMEM (lane dv, K = t), once MMA-s is done (long since)
+      if (!simt_and(mbar_wait(done_s, parity, kWaitLimit))) { failed = true; break; }
+      fence_after_sync();
+      for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
+        float r[16];
+        tmem_ld16(tl + T_BUF + c0, r);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) r[e] = -r[e];  // split of -Y: exact negation
+        put16_tmem<kLo>(tl + T_AOP, tl + T_AOP + 32, c0, r);
+      }
       {
         // each thread takes one row-half of T: row t = tid >> 2, 16 columns
         const int t = tid >> 2, cq = (tid & 3) * 16;
@@ -910,21 +920,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           put8<kLo>(gb, OFF_TB2, kC, kC, t, cq + 8 * h8, x2);
         }
       }
-      signal_ready(rdy_t);  // -> MMA-u: U^T = V^T (T diag(beta))^T
-
-      // ------------- phase 3: -Y operand in TMEM (lane dv, K = t)
-      if (!simt_and(mbar_wait(done_s, parity, kWaitLimit) &&
-                    mbar_wait(done_u, parity, kWaitLimit))) { failed = true; break; }
-      fence_after_sync();
-      for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
-        float r[16];
-        tmem_ld16(tl + T_BUF + c0, r);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) r[e] = -r[e];  // split of -Y: exact negation
-        put16_tmem<kLo>(tl + T_AOP, tl + T_AOP + 32, c0, r);
-      }
       tmem_wait_st();
-      signal_ready(rdy_y);  // -> MMA-d: Delta^T = U^T - Y (T diag(beta gamma))^T
+      // -> MMA-u: U^T = V^T (T diag(beta))^T, then
+      //    MMA-d: Delta^T = U^T + (-Y) (T diag(beta gamma))^T
+      signal_ready(rdy_t);
       if (warp == 0 && c + 1 < nchunks) prefetch(c + 1);  // lands under the work below
       if (!simt_and(mbar_wait(done_d, parity, kWaitLimit))) { failed = true; break; }
       fence_after_sync();
