@@ -26,10 +26,10 @@
 //   MMA-s  [Y | (Q S)^T] [dv][t'] = S^T [K; Q]^T      (one N = 128 product)
 //   SIMT   o of the previous chunk;  A and P from G, H;
 //          T = (I + A)^-1, blocked 16 x 16, fp32 (under MMA-s)
-//   SIMT   -Y operand in TMEM (MMA-s is done by then)
+//   SIMT   T diag(beta) operand
 //   MMA-u  U^T  [dv][t]  = V^T (T diag(beta))^T             (A = V, MN-major)
-//   MMA-d  Delta^T = U^T + (-Y) (T diag(beta gamma))^T   (onto U^T, right
-//          after MMA-u)
+//   SIMT   -Y operand in TMEM, T diag(beta gamma) operand (under MMA-u)
+//   MMA-d  Delta^T = U^T + (-Y) (T diag(beta gamma))^T      (onto U^T)
 //   SIMT   Delta^T and Delta^T diag(w) operands in TMEM
 //   MMA-3  (P Delta)^T = Delta^T P^T
 //   MMA-4  S^T += (Delta^T diag(w)) K                        (B = K, MN-major)
@@ -99,8 +99,8 @@ constexpr uint32_t OFF_TB2 = RC + 16384;    // 64 x 64: T diag(beta)
 constexpr uint32_t OFF_P = RP;              // 64 x 64
 constexpr uint32_t OFF_VEC = RP + 16384;    // Gamma, gamma, w, beta, gamma x 2, ea, eb
 constexpr uint32_t OFF_STAGE = RD;          // fp32 [K; Q] of the next chunk (64 KB)
-constexpr uint32_t OFF_BAR = OFF_VEC + 2048;  // 12 mbarriers
-constexpr uint32_t OFF_SLOT = OFF_BAR + 96;   // TMEM address; +104: int flag
+constexpr uint32_t OFF_BAR = OFF_VEC + 2048;  // 13 mbarriers
+constexpr uint32_t OFF_SLOT = OFF_BAR + 104;  // TMEM address; +112: int flag
 constexpr uint32_t kSmemUsed = OFF_BAR + 128;
 constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;  // room to align the base
 
@@ -524,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // every factor is a normal fp32 number
   float *ea = Gam + 384;
   float *eb = Gam + 448;
-  volatile int *fac = reinterpret_cast<volatile int *>(gb + OFF_BAR + 104);
+  volatile int *fac = reinterpret_cast<volatile int *>(gb + OFF_BAR + 112);
   const float *stage = reinterpret_cast<const float *>(gb + OFF_STAGE);
   // mbarriers: products done (one commit each), operands ready (kSimt
   // arrivals each), and the final drain
@@ -537,6 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t staged = bar0 + 72;   // next K, Q rows in the staging tile
   const uint32_t done_u = bar0 + 80;
   const uint32_t vstaged = bar0 + 88;  // this chunk's fp32 V rows in region Rb
+  const uint32_t rdy_w = bar0 + 96;    // -Y and T diag(beta gamma) operands
   volatile uint32_t *slot = reinterpret_cast<volatile uint32_t *>(gb + OFF_SLOT);
   float *Asc = reinterpret_cast<float *>(gb + OFF_SCR);
   float *Tsc = Asc + 64 * 64;
@@ -561,6 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(staged, 1);
     mbar_init(done_u, 1);
     mbar_init(vstaged, 1);
+    mbar_init(rdy_w, kSimt);
   }
   cta_sync_tc();
   const uint32_t tmem = *slot;
@@ -632,6 +634,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_after_sync();
         gemm<kLo, kC / 16>(tmem + T_U, opVmn, opTB2, 128, kC, false);
         commit(done_u);  // V's region then takes the next chunk's V rows
+        if (!mbar_wait(rdy_w, ph, kWaitLimit)) break;
+        fence_after_sync();
         gemm_steps<kC / 16>(GemmT<kLo>(tmem + T_U, tmem + T_AOP, tmem + T_AOP + 32,
                                        opTB, 128, kC, true));
         commit(done_d);
@@ -884,7 +888,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       simt_sync();
       tri_inverse(Asc, Tsc, tid);
 
-      // -Y operand in TMEM (lane dv, K = t), once MMA-s is done (long since)
+      // T diag(beta) operand first, so that MMA-u runs under the rest;
+      // each thread takes one row-half of T: row t = tid >> 2, 16 columns
+      const int t_row = tid >> 2, cq = (tid & 3) * 16;
+      float tr[16];
+#pragma unroll
+      for (int e4 = 0; e4 < 16; e4 += 4) {
+        const float4 v4 = *reinterpret_cast<const float4 *>(Tsc + sidx(t_row, cq + e4));
+        tr[e4] = v4.x;
+        tr[e4 + 1] = v4.y;
+        tr[e4 + 2] = v4.z;
+        tr[e4 + 3] = v4.w;
+      }
+      simt_sync();  // everyone holds its T values; scratch may be reused
+#pragma unroll
+      for (int h8 = 0; h8 < 2; ++h8) {
+        float x2[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x2[e] = tr[8 * h8 + e] * bet[cq + 8 * h8 + e];
+        put8<kLo>(gb, OFF_TB2, kC, kC, t_row, cq + 8 * h8, x2);
+      }
+      signal_ready(rdy_t);  // -> MMA-u: U^T = V^T (T diag(beta))^T
+
+      // -Y operand in TMEM (lane dv, K = t), once MMA-s is done (long
+      // since), and T diag(beta gamma)
       if (!simt_and(mbar_wait(done_s, parity, kWaitLimit))) { failed = true; break; }
       fence_after_sync();
       for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
@@ -894,36 +921,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 16; ++e) r[e] = -r[e];  // split of -Y: exact negation
         put16_tmem<kLo>(tl + T_AOP, tl + T_AOP + 32, c0, r);
       }
-      {
-        // each thread takes one row-half of T: row t = tid >> 2, 16 columns
-        const int t = tid >> 2, cq = (tid & 3) * 16;
-        float tr[16];
 #pragma unroll
-        for (int e4 = 0; e4 < 16; e4 += 4) {
-          const float4 v4 = *reinterpret_cast<const float4 *>(Tsc + sidx(t, cq + e4));
-          tr[e4] = v4.x;
-          tr[e4 + 1] = v4.y;
-          tr[e4 + 2] = v4.z;
-          tr[e4 + 3] = v4.w;
+      for (int h8 = 0; h8 < 2; ++h8) {
+        float x1[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int s_ = cq + 8 * h8 + e;
+          x1[e] = tr[8 * h8 + e] * bet[s_] * gam[s_];
         }
-        simt_sync();  // everyone holds its T values; scratch may be reused
-        float x1[8], x2[8];
-#pragma unroll
-        for (int h8 = 0; h8 < 2; ++h8) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int s = cq + 8 * h8 + e;
-            x1[e] = tr[8 * h8 + e] * bet[s] * gam[s];
-            x2[e] = tr[8 * h8 + e] * bet[s];
-          }
-          put8<kLo>(gb, OFF_TB, kC, kC, t, cq + 8 * h8, x1);
-          put8<kLo>(gb, OFF_TB2, kC, kC, t, cq + 8 * h8, x2);
-        }
+        put8<kLo>(gb, OFF_TB, kC, kC, t_row, cq + 8 * h8, x1);
       }
       tmem_wait_st();
-      // -> MMA-u: U^T = V^T (T diag(beta))^T, then
-      //    MMA-d: Delta^T = U^T + (-Y) (T diag(beta gamma))^T
-      signal_ready(rdy_t);
+      signal_ready(rdy_w);  // -> MMA-d: Delta^T = U^T + (-Y) (T diag(beta gamma))^T
       if (warp == 0 && c + 1 < nchunks) prefetch(c + 1);  // lands under the work below
       if (!simt_and(mbar_wait(done_d, parity, kWaitLimit))) { failed = true; break; }
       fence_after_sync();
