@@ -80,17 +80,20 @@ constexpr int kThreads = kSimt + 64;
 // columns (see gdn_tc.cuh), hi tile followed by lo tile (R * C * 2 bytes
 // each).  Regions (byte offsets from a 1024-aligned base) are reused by
 // phase:
-//   Ra 64 KB: [K; Q] (128 x 128), the whole chunk
+//   Ra 64 KB: even chunks' K, Q rows: fp32 staging, converted in place
+//             (read, barrier, write) to the [K; Q] operand (128 x 128)
 //   Rb 32 KB: fp32 V rows of the chunk (staging) -> V (64 x 128)
 //   Rc 32 KB: o of the previous chunk (fp32 [t][dv], 64 x 128, read by a
 //             tensor store before the A build)
 //                                     -> A, T scratch (fp32)
 //                                     -> T diag(bg), T diag(b) (64 x 64 each)
-//   Rd 64 KB: fp32 [K; Q] of the next chunk (staging)
+//   Rd 64 KB: the same for odd chunks, so a chunk's K, Q arrive and are
+//             converted while the previous chunk still reads its own
 //   Rp 16 KB: P (64 x 64)
 // The operands made from TMEM results (S^T, Y, Delta^T) stay in TMEM.
 constexpr uint32_t RA = 0, RB = 65536, RC = 98304, RD = 131072, RP = 196608;
-constexpr uint32_t OFF_KQ = RA;             // 128 x 128
+// [K; Q] region of chunk c: fp32 staging, then the 128 x 128 operand
+__host__ __device__ constexpr uint32_t kq_region(int c) { return (c & 1) ? RD : RA; }
 constexpr uint32_t OFF_V = RB;              // 64 x 128
 constexpr uint32_t OFF_OT = RC;             // fp32 o tile [64][128]
 constexpr uint32_t OFF_SCR = RC;            // fp32 A [64][64] + T [64][64]
@@ -98,9 +101,8 @@ constexpr uint32_t OFF_TB = RC;             // 64 x 64: T diag(beta gamma)
 constexpr uint32_t OFF_TB2 = RC + 16384;    // 64 x 64: T diag(beta)
 constexpr uint32_t OFF_P = RP;              // 64 x 64
 constexpr uint32_t OFF_VEC = RP + 16384;    // Gamma, gamma, w, beta, gamma x 2, ea, eb
-constexpr uint32_t OFF_STAGE = RD;          // fp32 [K; Q] of the next chunk (64 KB)
-constexpr uint32_t OFF_BAR = OFF_VEC + 2048;  // 13 mbarriers
-constexpr uint32_t OFF_SLOT = OFF_BAR + 104;  // TMEM address; +112: int flag
+constexpr uint32_t OFF_BAR = OFF_VEC + 2048;  // 15 mbarriers
+constexpr uint32_t OFF_SLOT = OFF_BAR + 120;  // TMEM address; +124: int flag
 constexpr uint32_t kSmemUsed = OFF_BAR + 128;
 constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;  // room to align the base
 
@@ -524,8 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // every factor is a normal fp32 number
   float *ea = Gam + 384;
   float *eb = Gam + 448;
-  volatile int *fac = reinterpret_cast<volatile int *>(gb + OFF_BAR + 112);
-  const float *stage = reinterpret_cast<const float *>(gb + OFF_STAGE);
+  volatile int *fac = reinterpret_cast<volatile int *>(gb + OFF_BAR + 124);
   // mbarriers: products done (one commit each), operands ready (kSimt
   // arrivals each), and the final drain
   const uint32_t bar0 = sb + OFF_BAR;
@@ -534,10 +535,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t rdy_a = bar0 + 32, rdy_s = bar0 + 40, rdy_t = bar0 + 48,
                  rdy_d = bar0 + 56;
   const uint32_t drain = bar0 + 64;
-  const uint32_t staged = bar0 + 72;   // next K, Q rows in the staging tile
+  const uint32_t staged0 = bar0 + 72;  // K, Q rows of an even chunk in Ra
   const uint32_t done_u = bar0 + 80;
   const uint32_t vstaged = bar0 + 88;  // this chunk's fp32 V rows in region Rb
   const uint32_t rdy_w = bar0 + 96;    // -Y and T diag(beta gamma) operands
+  const uint32_t staged1 = bar0 + 104; // K, Q rows of an odd chunk in Rd
+  const uint32_t kq_free = bar0 + 112; // a chunk's [K; Q] region is free again
   volatile uint32_t *slot = reinterpret_cast<volatile uint32_t *>(gb + OFF_SLOT);
   float *Asc = reinterpret_cast<float *>(gb + OFF_SCR);
   float *Tsc = Asc + 64 * 64;
@@ -559,7 +562,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 4; ++i) mbar_init(bar0 + 8 * i, 1);
     for (int i = 4; i < 8; ++i) mbar_init(bar0 + 8 * i, kSimt);
     mbar_init(drain, 1);
-    mbar_init(staged, 1);
+    mbar_init(staged0, 1);
+    mbar_init(staged1, 1);
+    mbar_init(kq_free, 1);
     mbar_init(done_u, 1);
     mbar_init(vstaged, 1);
     mbar_init(rdy_w, kSimt);
@@ -569,22 +574,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kLoader) {
     // ------------------------------------------------ the copying warp
-    // K and Q rows of chunk c, fp32, into the staging tile [128 rows: K then
-    // Q][128] as soon as it is free: before the loop for chunk 0, else once
-    // MMA-s of chunk c-1 has consumed the S^T operand that shares its region
-    // (about two thirds of a chunk ahead of use).  Then its fp32 V rows
-    // into region Rb once MMA-u of chunk c-1 has consumed the V operand
-    // there.  One tensor copy of 64 rows each; rows past T arrive as zeros.
-    int issued = -1, v_issued = -1;
+    // K and Q rows of chunk c, fp32, into its region (Ra for even c, Rd for
+    // odd c) once chunk c-2's products have finished reading that region:
+    // a chunk ahead of use.  Then its fp32 V rows into region Rb once MMA-u
+    // of chunk c-1 has consumed the V operand there.  One tensor copy of 64
+    // rows each; rows past T arrive as zeros.
+    int issued[2] = {-1, -1}, v_issued = -1;
     for (int c = 0; c < nchunks; ++c) {
-      if (c > 0 && !mbar_wait(done_s, (uint32_t)((c - 1) & 1), kWaitLimit)) break;
+      if (c >= 2 && !mbar_wait(kq_free, (uint32_t)((c - 2) & 1), kWaitLimit)) break;
+      const uint32_t st = (c & 1) ? staged1 : staged0;
       if (lane == 0) {
-        mbar_arrive_expect_tx(staged, 2u * kC * 512u);
-        tma_load_rows(sb + OFF_STAGE, &tm_k, hh, c * kC, b, staged);
-        tma_load_rows(sb + OFF_STAGE + kC * 512, &tm_q, hh, c * kC, b, staged);
+        mbar_arrive_expect_tx(st, 2u * kC * 512u);
+        tma_load_rows(sb + kq_region(c), &tm_k, hh, c * kC, b, st);
+        tma_load_rows(sb + kq_region(c) + kC * 512, &tm_q, hh, c * kC, b, st);
       }
       __syncwarp();
-      issued = c;
+      issued[c & 1] = c;
       if (c > 0 && !mbar_wait(done_u, (uint32_t)((c - 1) & 1), kWaitLimit)) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(vstaged, kC * 512u);
@@ -594,7 +599,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       v_issued = c;
     }
     // nothing may still be copying into shared memory when the CTA ends
-    if (issued >= 0) mbar_wait(staged, (uint32_t)(issued & 1), kWaitLimit);
+    for (int j = 0; j < 2; ++j)
+      if (issued[j] >= 0)
+        mbar_wait(j ? staged1 : staged0, (uint32_t)((issued[j] >> 1) & 1), kWaitLimit);
     if (v_issued >= 0) mbar_wait(vstaged, (uint32_t)(v_issued & 1), kWaitLimit);
   } else if (warp == kIssuer) {
     // ------------------------------------------------ the issuing warp
@@ -602,15 +609,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // warps report its operands ready; tcgen05.mma issue waits while the
     // tensor pipe is busy, and here that wait holds up no SIMT work.
     if (lane == 0) {
-      const Operand opKQ{sb + OFF_KQ, 128, 128, false};   // MMA-a A; MMA-s B ([K; Q])
-      const Operand opKb{sb + OFF_KQ, 128, 128, false};   // MMA-a B (K: rows 0-63)
       const Operand opVmn{sb + OFF_V, 64, 128, true};     // MMA-u A
       const Operand opTB{sb + OFF_TB, 64, 64, false};     // MMA-d B
       const Operand opTB2{sb + OFF_TB2, 64, 64, false};   // MMA-u B
       const Operand opP{sb + OFF_P, 64, 64, false};       // MMA-3 B
-      const Operand opKnB{sb + OFF_KQ, 128, 128, true};   // MMA-4 B (K rows)
       uint32_t ph = 0;
       for (int c = 0; c < nchunks; ++c) {
+        const uint32_t kq = sb + kq_region(c);
+        const Operand opKQ{kq, 128, 128, false};   // MMA-a A; MMA-s B ([K; Q])
+        const Operand opKb{kq, 128, 128, false};   // MMA-a B (K: rows 0-63)
+        const Operand opKnB{kq, 128, 128, true};   // MMA-4 B (K rows)
         if (!mbar_wait(rdy_a, ph, kWaitLimit)) break;
         fence_after_sync();
         {
@@ -753,41 +761,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) *fac = (gmax - gmin <= 160.f) ? 1 : 0;
     };
     if (warp == 0) gates(0);
-    // [K; Q] operand rows (tid >> 4) + 16 i, i0 <= i < i1 (K: i < 4), from
-    // the staging tile.  Lanes 4-7 of each quarter warp read their two
-    // 16-byte halves in the other order, so each of the two loads covers all
-    // eight 16-byte bank groups of the quarter warp once.
-    auto kq_rows = [&](int i0, int i1) {
-      const int swap = (tid >> 2) & 1;
+    // [K; Q] operand of chunk cc, in place in its region: this thread's
+    // fp32 rows (tid >> 4) + 16 i, columns (tid & 15) * 8 .. + 7, are read
+    // into registers, then, after a barrier, written back as bf16 operand
+    // rows.  Lanes 4-7 of each quarter warp read their two 16-byte halves
+    // in the other order, so each of the two loads covers all eight 16-byte
+    // bank groups of the quarter warp once.  False if the rows never came.
+    auto kq_operand = [&](int cc) -> bool {
+      const uint32_t st = (cc & 1) ? staged1 : staged0;
+      if (!simt_and(mbar_wait(st, (uint32_t)((cc >> 1) & 1), kWaitLimit))) return false;
+      const float *stage = reinterpret_cast<const float *>(gb + kq_region(cc));
+      const int swap = (tid >> 2) & 1, c0 = (tid & 15) * 8;
+      float x[8][8];
 #pragma unroll
-      for (int i = i0; i < i1; ++i) {
-        const int row = (tid >> 4) + 16 * i, c0 = (tid & 15) * 8;
+      for (int i = 0; i < 8; ++i) {
+        const int row = (tid >> 4) + 16 * i;
         const float4 ya = *reinterpret_cast<const float4 *>(stage + row * 128 + c0 + 4 * swap);
         const float4 yb = *reinterpret_cast<const float4 *>(stage + row * 128 + c0 + 4 - 4 * swap);
         const float4 x0 = swap ? yb : ya, x1 = swap ? ya : yb;
-        const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-        put8<kLo>(gb, OFF_KQ, 128, 128, row, c0, x);
+        x[i][0] = x0.x; x[i][1] = x0.y; x[i][2] = x0.z; x[i][3] = x0.w;
+        x[i][4] = x1.x; x[i][5] = x1.y; x[i][6] = x1.z; x[i][7] = x1.w;
       }
+      simt_sync();
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        put8<kLo>(gb, kq_region(cc), 128, 128, (tid >> 4) + 16 * i, c0, x[i]);
+      return true;
     };
     uint32_t parity = 0;
-    bool failed = false;
-    for (int c = 0; c < nchunks; ++c) {
+    bool failed = !kq_operand(0);
+    if (!failed) signal_ready(rdy_a);  // -> MMA-a of chunk 0
+    for (int c = 0; !failed && c < nchunks; ++c) {
       // ---------------------------------------------------- phase 0: inputs
-      // this chunk's K and Q rows are in the staging tile (its gates were
-      // written before the SIMT barrier that ended the previous wait)
-      if (!simt_and(mbar_wait(staged, parity, kWaitLimit))) { failed = true; break; }
-      // K operand rows (and for the first chunk Q's) from the staging tile;
-      // later chunks' Q rows were converted during the previous chunk's
-      // last products
-      if (c == 0)
-        kq_rows(0, 8);
-      else
-        kq_rows(0, 4);
-      signal_ready(rdy_a);  // -> MMA-a: G, H = [K; Q] K^T
+      // This chunk's [K; Q] operand and gates were made, and MMA-a
+      // released, during the previous chunk's last products (before the
+      // loop for chunk 0).
       if (c > 0) emit_o(c - 1);  // the previous chunk's output, into the o tile
       // V operand rows (needed from MMA-u on), converted in place: the fp32
       // rows (tid >> 4) + 16 i are read into registers (same bank order as
-      // kq_rows), then, after a barrier, written back as bf16 operand rows
+      // kq_operand), then, after a barrier, written back as bf16 operand rows
       float vx[4][8];
       if (!simt_and(mbar_wait(vstaged, parity, kWaitLimit))) { failed = true; break; }
       {
@@ -949,14 +961,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_st();
       signal_ready(rdy_d);  // -> MMA-3: (P Delta)^T;  MMA-4: S^T += ...
       if (c + 1 < nchunks) {
-        // Under MMA-3 and MMA-4: the next chunk's Q operand rows (this
-        // chunk's Q is consumed; MMA-4 reads only K's rows) and gates.
-        if (!simt_and(mbar_wait(staged, parity ^ 1u, kWaitLimit))) { failed = true; break; }
-        kq_rows(4, 8);
+        // Under MMA-3 and MMA-4: the next chunk's [K; Q] operand (in the
+        // other region) and gates; then MMA-a of the next chunk is released
+        // (it queues behind this chunk's products).
+        if (!kq_operand(c + 1)) { failed = true; break; }
         if (warp == 0) gates(c + 1);
+        signal_ready(rdy_a);
       }
       if (!simt_and(mbar_wait(done_4, parity, kWaitLimit))) { failed = true; break; }
       fence_after_sync();
+      // this chunk's [K; Q] region may take the rows of chunk c + 2
+      if (tid == 0) mbar_arrive(kq_free);
       parity ^= 1u;
     }
 
