@@ -28,8 +28,8 @@
 //          T = (I + A)^-1, blocked 16 x 16, fp32 (under MMA-s)
 //   SIMT   T diag(beta) operand
 //   MMA-u  U^T  [dv][t]  = V^T (T diag(beta))^T             (A = V, MN-major)
-//   SIMT   -Y operand in TMEM, T diag(beta gamma) operand (under MMA-u)
-//   MMA-d  Delta^T = U^T + (-Y) (T diag(beta gamma))^T      (onto U^T)
+//   SIMT   -Y diag(gamma) operand in TMEM (under MMA-u)
+//   MMA-d  Delta^T = U^T + (-Y diag(gamma)) (T diag(beta))^T  (onto U^T)
 //   SIMT   Delta^T and Delta^T diag(w) operands in TMEM
 //   MMA-3  (P Delta)^T = Delta^T P^T
 //   MMA-4  S^T += (Delta^T diag(w)) K                        (B = K, MN-major)
@@ -86,7 +86,7 @@ constexpr int kThreads = kSimt + 64;
 //   Rc 32 KB: o of the previous chunk (fp32 [t][dv], 64 x 128, read by a
 //             tensor store before the A build)
 //                                     -> A, T scratch (fp32)
-//                                     -> T diag(bg), T diag(b) (64 x 64 each)
+//                                     -> T diag(beta) (64 x 64)
 //   Rd 64 KB: the same for odd chunks, so a chunk's K, Q arrive and are
 //             converted while the previous chunk still reads its own
 //   Rp 16 KB: P (64 x 64)
@@ -97,7 +97,6 @@ __host__ __device__ constexpr uint32_t kq_region(int c) { return (c & 1) ? RD : 
 constexpr uint32_t OFF_V = RB;              // 64 x 128
 constexpr uint32_t OFF_OT = RC;             // fp32 o tile [64][128]
 constexpr uint32_t OFF_SCR = RC;            // fp32 A [64][64] + T [64][64]
-constexpr uint32_t OFF_TB = RC;             // 64 x 64: T diag(beta gamma)
 constexpr uint32_t OFF_TB2 = RC + 16384;    // 64 x 64: T diag(beta)
 constexpr uint32_t OFF_P = RP;              // 64 x 64
 constexpr uint32_t OFF_VEC = RP + 16384;    // Gamma, gamma, w, beta, gamma x 2, ea, eb
@@ -117,9 +116,9 @@ constexpr uint32_t T_U = 192;     // second half-K of G, H; then U^T, then
 // for the output before its own MMA-s is issued.
 constexpr uint32_t T_BUF = 256;
 // 128 columns of bf16 A operands (lanes dv, two elements per column), hi
-// then lo: S^T (64 + 64 columns, K = dk) for MMA-s; then -Y (32 + 32, K =
-// t) for MMA-d; then Delta^T (32 + 32) and Delta^T diag(w) (the next 64)
-// for MMA-3 and MMA-4.
+// then lo: S^T (64 + 64 columns, K = dk) for MMA-s; then -Y diag(gamma)
+// (32 + 32, K = t) for MMA-d; then Delta^T (32 + 32) and Delta^T diag(w)
+// (the next 64) for MMA-3 and MMA-4.
 constexpr uint32_t T_AOP = 384;
 
 constexpr uint32_t kWaitLimit = 1u << 24;
@@ -538,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t staged0 = bar0 + 72;  // K, Q rows of an even chunk in Ra
   const uint32_t done_u = bar0 + 80;
   const uint32_t vstaged = bar0 + 88;  // this chunk's fp32 V rows in region Rb
-  const uint32_t rdy_w = bar0 + 96;    // -Y and T diag(beta gamma) operands
+  const uint32_t rdy_w = bar0 + 96;    // -Y diag(gamma) operand
   const uint32_t staged1 = bar0 + 104; // K, Q rows of an odd chunk in Rd
   const uint32_t kq_free = bar0 + 112; // a chunk's [K; Q] region is free again
   volatile uint32_t *slot = reinterpret_cast<volatile uint32_t *>(gb + OFF_SLOT);
@@ -610,8 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tensor pipe is busy, and here that wait holds up no SIMT work.
     if (lane == 0) {
       const Operand opVmn{sb + OFF_V, 64, 128, true};     // MMA-u A
-      const Operand opTB{sb + OFF_TB, 64, 64, false};     // MMA-d B
-      const Operand opTB2{sb + OFF_TB2, 64, 64, false};   // MMA-u B
+      const Operand opTB2{sb + OFF_TB2, 64, 64, false};   // MMA-u, MMA-d B
       const Operand opP{sb + OFF_P, 64, 64, false};       // MMA-3 B
       uint32_t ph = 0;
       for (int c = 0; c < nchunks; ++c) {
@@ -645,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(rdy_w, ph, kWaitLimit)) break;
         fence_after_sync();
         gemm_steps<kC / 16>(GemmT<kLo>(tmem + T_U, tmem + T_AOP, tmem + T_AOP + 32,
-                                       opTB, 128, kC, true));
+                                       opTB2, 128, kC, true));
         commit(done_d);
         if (!mbar_wait(rdy_d, ph, kWaitLimit)) break;
         fence_after_sync();
@@ -922,29 +920,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       signal_ready(rdy_t);  // -> MMA-u: U^T = V^T (T diag(beta))^T
 
-      // -Y operand in TMEM (lane dv, K = t), once MMA-s is done (long
-      // since), and T diag(beta gamma)
+      // -Y diag(gamma) operand in TMEM (lane dv, K = t), once MMA-s is done
+      // (long since): since (W S)^T = Y (T diag(beta gamma))^T
+      // = (Y diag(gamma)) (T diag(beta))^T, MMA-d shares MMA-u's B operand
       if (!simt_and(mbar_wait(done_s, parity, kWaitLimit))) { failed = true; break; }
       fence_after_sync();
       for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
         float r[16];
         tmem_ld16(tl + T_BUF + c0, r);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) r[e] = -r[e];  // split of -Y: exact negation
+        for (int e = 0; e < 16; ++e) r[e] = -r[e] * gam[c0 + e];
         put16_tmem<kLo>(tl + T_AOP, tl + T_AOP + 32, c0, r);
       }
-#pragma unroll
-      for (int h8 = 0; h8 < 2; ++h8) {
-        float x1[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int s_ = cq + 8 * h8 + e;
-          x1[e] = tr[8 * h8 + e] * bet[s_] * gam[s_];
-        }
-        put8<kLo>(gb, OFF_TB, kC, kC, t_row, cq + 8 * h8, x1);
-      }
       tmem_wait_st();
-      signal_ready(rdy_w);  // -> MMA-d: Delta^T = U^T + (-Y) (T diag(beta gamma))^T
+      signal_ready(rdy_w);  // -> MMA-d: Delta^T = U^T + (-Y diag(gamma)) (T diag(beta))^T
       if (warp == 0 && c + 1 < nchunks) prefetch(c + 1);  // lands under the work below
       if (!simt_and(mbar_wait(done_d, parity, kWaitLimit))) { failed = true; break; }
       fence_after_sync();
