@@ -381,11 +381,11 @@ def prefill_parts(torch, gdn, tens, stream, peaks, parts):
     toks = pin_.B * pin_.T
     flops = 7 * D * D * toks * pin_.vh
     # executed tensor-core flops of the chunked form per 64-token chunk
-    # and head: [K;Q]K^T 2*128*64*128; S^T K^T and S^T Q^T 2*(2*128*64*128);
-    # U^T and Y (T diag(beta gamma))^T 2*(2*128*64*64); Delta^T P^T
+    # and head: [K;Q]K^T 2*128*64*128; S^T [K;Q]^T 2*128*128*128;
+    # (V^T - Y diag(gamma)) (T diag(beta))^T 2*128*64*64; Delta^T P^T
     # 2*128*64*64; Delta^T K~ 2*128*128*64
-    tc_flops = (2 * 128 * 64 * 128 + 4 * 128 * 64 * 128 +
-                4 * 128 * 64 * 64 + 2 * 128 * 64 * 64 +
+    tc_flops = (2 * 128 * 64 * 128 + 2 * 128 * 128 * 128 +
+                2 * 128 * 64 * 64 + 2 * 128 * 64 * 64 +
                 2 * 128 * 128 * 64) * (pin_.T // 64) * pin_.B * pin_.vh
     for prec, name, reps in ((gdn.GDN_PREC_FP32, "fp32", 3),
                              (gdn.GDN_PREC_BF16X3, "bf16x3", 10),

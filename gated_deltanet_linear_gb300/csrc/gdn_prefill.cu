@@ -26,10 +26,9 @@
 //   MMA-s  [Y | (Q S)^T] [dv][t'] = S^T [K; Q]^T      (one N = 128 product)
 //   SIMT   o of the previous chunk;  A and P from G, H;
 //          T = (I + A)^-1, blocked 16 x 16, fp32 (under MMA-s)
-//   SIMT   T diag(beta) operand
-//   MMA-u  U^T  [dv][t]  = V^T (T diag(beta))^T             (A = V, MN-major)
-//   SIMT   -Y diag(gamma) operand in TMEM (under MMA-u)
-//   MMA-d  Delta^T = U^T + (-Y diag(gamma)) (T diag(beta))^T  (onto U^T)
+//   SIMT   V^T - Y diag(gamma) operand in TMEM; T diag(beta) operand
+//   MMA-ud Delta^T [dv][t] = (V^T - Y diag(gamma)) (T diag(beta))^T
+//          (= U^T - (W S)^T in one product)
 //   SIMT   Delta^T and Delta^T diag(w) operands in TMEM
 //   MMA-3  (P Delta)^T = Delta^T P^T
 //   MMA-4  S^T += (Delta^T diag(w)) K                        (B = K, MN-major)
@@ -82,7 +81,7 @@ constexpr int kThreads = kSimt + 64;
 // phase:
 //   Ra 64 KB: even chunks' K, Q rows: fp32 staging, converted in place
 //             (read, barrier, write) to the [K; Q] operand (128 x 128)
-//   Rb 32 KB: fp32 V rows of the chunk (staging) -> V (64 x 128)
+//   Rb 32 KB: fp32 V rows of the chunk
 //   Rc 32 KB: o of the previous chunk (fp32 [t][dv], 64 x 128, read by a
 //             tensor store before the A build)
 //                                     -> A, T scratch (fp32)
@@ -94,7 +93,7 @@ constexpr int kThreads = kSimt + 64;
 constexpr uint32_t RA = 0, RB = 65536, RC = 98304, RD = 131072, RP = 196608;
 // [K; Q] region of chunk c: fp32 staging, then the 128 x 128 operand
 __host__ __device__ constexpr uint32_t kq_region(int c) { return (c & 1) ? RD : RA; }
-constexpr uint32_t OFF_V = RB;              // 64 x 128
+constexpr uint32_t OFF_V = RB;              // fp32 V rows [64][128]
 constexpr uint32_t OFF_OT = RC;             // fp32 o tile [64][128]
 constexpr uint32_t OFF_SCR = RC;            // fp32 A [64][64] + T [64][64]
 constexpr uint32_t OFF_TB2 = RC + 16384;    // 64 x 64: T diag(beta)
@@ -108,7 +107,7 @@ constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;  // room to align the base
 // TMEM columns (512 allocated).
 constexpr uint32_t T_SACC = 0;    // S^T: lanes dv, 128 columns dk
 constexpr uint32_t T_GH = 128;    // G (lanes 0-63), H (lanes 64-127): 64 columns
-constexpr uint32_t T_U = 192;     // second half-K of G, H; then U^T, then
+constexpr uint32_t T_U = 192;     // second half-K of G, H; then
                                   // Delta^T = U^T - (W S)^T: lanes dv
 // 128 columns, lanes dv, columns t: MMA-s writes [Y | (Q S)^T] in one
 // product (B = [K; Q]); once Y has been read out, MMA-3 writes
@@ -116,8 +115,8 @@ constexpr uint32_t T_U = 192;     // second half-K of G, H; then U^T, then
 // for the output before its own MMA-s is issued.
 constexpr uint32_t T_BUF = 256;
 // 128 columns of bf16 A operands (lanes dv, two elements per column), hi
-// then lo: S^T (64 + 64 columns, K = dk) for MMA-s; then -Y diag(gamma)
-// (32 + 32, K = t) for MMA-d; then Delta^T (32 + 32) and Delta^T diag(w)
+// then lo: S^T (64 + 64 columns, K = dk) for MMA-s; then V^T - Y diag(gamma)
+// (32 + 32, K = t) for MMA-ud; then Delta^T (32 + 32) and Delta^T diag(w)
 // (the next 64) for MMA-3 and MMA-4.
 constexpr uint32_t T_AOP = 384;
 
@@ -535,9 +534,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                  rdy_d = bar0 + 56;
   const uint32_t drain = bar0 + 64;
   const uint32_t staged0 = bar0 + 72;  // K, Q rows of an even chunk in Ra
-  const uint32_t done_u = bar0 + 80;
+  const uint32_t v_free = bar0 + 80;   // the fp32 V rows in Rb are read
   const uint32_t vstaged = bar0 + 88;  // this chunk's fp32 V rows in region Rb
-  const uint32_t rdy_w = bar0 + 96;    // -Y diag(gamma) operand
   const uint32_t staged1 = bar0 + 104; // K, Q rows of an odd chunk in Rd
   const uint32_t kq_free = bar0 + 112; // a chunk's [K; Q] region is free again
   volatile uint32_t *slot = reinterpret_cast<volatile uint32_t *>(gb + OFF_SLOT);
@@ -564,9 +562,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(staged0, 1);
     mbar_init(staged1, 1);
     mbar_init(kq_free, 1);
-    mbar_init(done_u, 1);
+    mbar_init(v_free, 1);
     mbar_init(vstaged, 1);
-    mbar_init(rdy_w, kSimt);
   }
   cta_sync_tc();
   const uint32_t tmem = *slot;
@@ -575,8 +572,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ the copying warp
     // K and Q rows of chunk c, fp32, into its region (Ra for even c, Rd for
     // odd c) once chunk c-2's products have finished reading that region:
-    // a chunk ahead of use.  Then its fp32 V rows into region Rb once MMA-u
-    // of chunk c-1 has consumed the V operand there.  One tensor copy of 64
+    // a chunk ahead of use.  Then its fp32 V rows into region Rb once the
+    // SIMT warps have read chunk c-1's.  One tensor copy of 64
     // rows each; rows past T arrive as zeros.
     int issued[2] = {-1, -1}, v_issued = -1;
     for (int c = 0; c < nchunks; ++c) {
@@ -589,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       issued[c & 1] = c;
-      if (c > 0 && !mbar_wait(done_u, (uint32_t)((c - 1) & 1), kWaitLimit)) break;
+      if (c > 0 && !mbar_wait(v_free, (uint32_t)((c - 1) & 1), kWaitLimit)) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(vstaged, kC * 512u);
         tma_load_rows(sb + OFF_V, &tm_v, vi, c * kC, b, vstaged);
@@ -608,8 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // warps report its operands ready; tcgen05.mma issue waits while the
     // tensor pipe is busy, and here that wait holds up no SIMT work.
     if (lane == 0) {
-      const Operand opVmn{sb + OFF_V, 64, 128, true};     // MMA-u A
-      const Operand opTB2{sb + OFF_TB2, 64, 64, false};   // MMA-u, MMA-d B
+      const Operand opTB2{sb + OFF_TB2, 64, 64, false};   // MMA-ud B
       const Operand opP{sb + OFF_P, 64, 64, false};       // MMA-3 B
       uint32_t ph = 0;
       for (int c = 0; c < nchunks; ++c) {
@@ -621,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_after_sync();
         {
           // [K;Q] K^T as two half-K products in two accumulators (T_U is
-          // free until MMA-u); the A/P build adds them
+          // free until MMA-ud); the A/P build adds them
           const Gemm<kLo> lo_(tmem + T_GH, opKQ, opKb, 128, kC, false);
           const Gemm<kLo> hi_(tmem + T_U, opKQ, opKb, 128, kC, false);
 #pragma unroll
@@ -638,12 +634,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         commit(done_s);
         if (!mbar_wait(rdy_t, ph, kWaitLimit)) break;
         fence_after_sync();
-        gemm<kLo, kC / 16>(tmem + T_U, opVmn, opTB2, 128, kC, false);
-        commit(done_u);  // V's region then takes the next chunk's V rows
-        if (!mbar_wait(rdy_w, ph, kWaitLimit)) break;
-        fence_after_sync();
         gemm_steps<kC / 16>(GemmT<kLo>(tmem + T_U, tmem + T_AOP, tmem + T_AOP + 32,
-                                       opTB2, 128, kC, true));
+                                       opTB2, 128, kC, false));
         commit(done_d);
         if (!mbar_wait(rdy_d, ph, kWaitLimit)) break;
         fence_after_sync();
@@ -795,29 +787,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // released, during the previous chunk's last products (before the
       // loop for chunk 0).
       if (c > 0) emit_o(c - 1);  // the previous chunk's output, into the o tile
-      // V operand rows (needed from MMA-u on), converted in place: the fp32
-      // rows (tid >> 4) + 16 i are read into registers (same bank order as
-      // kq_operand), then, after a barrier, written back as bf16 operand rows
-      float vx[4][8];
-      if (!simt_and(mbar_wait(vstaged, parity, kWaitLimit))) { failed = true; break; }
-      {
-        const float *vst = reinterpret_cast<const float *>(gb + OFF_V);
-        const int swap = (tid >> 2) & 1, c0 = (tid & 15) * 8;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int row = (tid >> 4) + 16 * i;
-          const float4 ya = *reinterpret_cast<const float4 *>(vst + row * 128 + c0 + 4 * swap);
-          const float4 yb = *reinterpret_cast<const float4 *>(vst + row * 128 + c0 + 4 - 4 * swap);
-          const float4 x0 = swap ? yb : ya, x1 = swap ? ya : yb;
-          vx[i][0] = x0.x; vx[i][1] = x0.y; vx[i][2] = x0.z; vx[i][3] = x0.w;
-          vx[i][4] = x1.x; vx[i][5] = x1.y; vx[i][6] = x1.z; vx[i][7] = x1.w;
-        }
-      }
-      simt_sync();  // the staging tiles and the o tile's writes are done
+      simt_sync();  // the o tile is written
       if (c > 0 && tid == 0) store_o(c - 1);
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        put8<kLo>(gb, OFF_V, 64, 128, (tid >> 4) + 16 * i, (tid & 15) * 8, vx[i]);
 
       // ------------- phase 1: S^T operand (lane dv, K = dk) in TMEM; the
       // accumulator is then decayed in place, S^T *= gamma_63, ready for
@@ -898,8 +869,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       simt_sync();
       tri_inverse(Asc, Tsc, tid);
 
-      // T diag(beta) operand first, so that MMA-u runs under the rest;
-      // each thread takes one row-half of T: row t = tid >> 2, 16 columns
+      // The A operand of the correction product in TMEM (lane dv, K = s):
+      // V^T - Y diag(gamma), since Delta^T = U^T - (W S)^T
+      // = V^T (T diag(beta))^T - Y (T diag(beta gamma))^T
+      // = (V^T - Y diag(gamma)) (T diag(beta))^T.  V comes from its fp32
+      // rows in region Rb (row s, this lane's column), Y from MMA-s.
+      if (!simt_and(mbar_wait(done_s, parity, kWaitLimit) &&
+                    mbar_wait(vstaged, parity, kWaitLimit))) { failed = true; break; }
+      fence_after_sync();
+      {
+        const float *vst = reinterpret_cast<const float *>(gb + OFF_V);
+        for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
+          float r[16];
+          tmem_ld16(tl + T_BUF + c0, r);
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            r[e] = fmaf(-r[e], gam[c0 + e], vst[(c0 + e) * kD + myrow]);
+          put16_tmem<kLo>(tl + T_AOP, tl + T_AOP + 32, c0, r);
+        }
+      }
+      // T diag(beta), the B operand; each thread takes one row-half of T:
+      // row t = tid >> 2, 16 columns
       const int t_row = tid >> 2, cq = (tid & 3) * 16;
       float tr[16];
 #pragma unroll
@@ -910,7 +900,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tr[e4 + 2] = v4.z;
         tr[e4 + 3] = v4.w;
       }
-      simt_sync();  // everyone holds its T values; scratch may be reused
+      simt_sync();  // T values held, V rows read: scratch and Rb may be reused
+      if (tid == 0) mbar_arrive(v_free);
 #pragma unroll
       for (int h8 = 0; h8 < 2; ++h8) {
         float x2[8];
@@ -918,22 +909,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 8; ++e) x2[e] = tr[8 * h8 + e] * bet[cq + 8 * h8 + e];
         put8<kLo>(gb, OFF_TB2, kC, kC, t_row, cq + 8 * h8, x2);
       }
-      signal_ready(rdy_t);  // -> MMA-u: U^T = V^T (T diag(beta))^T
-
-      // -Y diag(gamma) operand in TMEM (lane dv, K = t), once MMA-s is done
-      // (long since): since (W S)^T = Y (T diag(beta gamma))^T
-      // = (Y diag(gamma)) (T diag(beta))^T, MMA-d shares MMA-u's B operand
-      if (!simt_and(mbar_wait(done_s, parity, kWaitLimit))) { failed = true; break; }
-      fence_after_sync();
-      for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
-        float r[16];
-        tmem_ld16(tl + T_BUF + c0, r);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) r[e] = -r[e] * gam[c0 + e];
-        put16_tmem<kLo>(tl + T_AOP, tl + T_AOP + 32, c0, r);
-      }
       tmem_wait_st();
-      signal_ready(rdy_w);  // -> MMA-d: Delta^T = U^T + (-Y diag(gamma)) (T diag(beta))^T
+      signal_ready(rdy_t);  // -> MMA-ud: Delta^T = (V^T - Y diag(gamma)) (T diag(beta))^T
       if (warp == 0 && c + 1 < nchunks) prefetch(c + 1);  // lands under the work below
       if (!simt_and(mbar_wait(done_d, parity, kWaitLimit))) { failed = true; break; }
       fence_after_sync();
