@@ -866,14 +866,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           put8<kLo>(gb, OFF_P, kC, kC, t, c0 + 8, r + 8);
         }
       }
-      simt_sync();
-      tri_inverse(Asc, Tsc, tid);
-
       // The A operand of the correction product in TMEM (lane dv, K = s):
       // V^T - Y diag(gamma), since Delta^T = U^T - (W S)^T
       // = V^T (T diag(beta))^T - Y (T diag(beta gamma))^T
       // = (V^T - Y diag(gamma)) (T diag(beta))^T.  V comes from its fp32
       // rows in region Rb (row s, this lane's column), Y from MMA-s.
+      // (The wait is also the barrier between the A build and the inverse.)
       if (!simt_and(mbar_wait(done_s, parity, kWaitLimit) &&
                     mbar_wait(vstaged, parity, kWaitLimit))) { failed = true; break; }
       fence_after_sync();
@@ -888,6 +886,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           put16_tmem<kLo>(tl + T_AOP, tl + T_AOP + 32, c0, r);
         }
       }
+      tri_inverse(Asc, Tsc, tid);
+
       // T diag(beta), the B operand; each thread takes one row-half of T:
       // row t = tid >> 2, 16 columns
       const int t_row = tid >> 2, cq = (tid & 3) * 16;
