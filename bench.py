@@ -515,24 +515,25 @@ def main():
 
     # ---- end to end through the public API with host buffers: the step's
     # inputs q | k | v | g | beta sit back to back in one pinned host buffer
-    # and go over in one copy; the kernel writes o straight into a pinned
-    # host buffer over the host link (no separate copy back)
+    # and o goes to another; the kernel reads the inputs and writes o over
+    # the host link itself (gdn_step takes page-locked host token buffers),
+    # so the transfers overlap the state streaming and no copy is issued.
+    # (One copy engine transfer in, then the kernel, measured 91.5 us
+    # against 86.4 us this way.)
     parts_in = (inp.q, inp.k, inp.v, inp.g, inp.beta)
     sizes = [x.size for x in parts_in]           # each a multiple of 4 floats
     h_pack = torch.empty(sum(sizes), dtype=torch.float32).pin_memory()
-    d_pack = torch.empty(sum(sizes), dtype=torch.float32, device=dev)
-    d_in, off = [], 0
+    h_in, off = [], 0
     for x, n_ in zip(parts_in, sizes):
         h_pack[off:off + n_] = torch.from_numpy(np.ascontiguousarray(x).ravel())
-        d_in.append(d_pack[off:off + n_].view(x.shape))
+        h_in.append(h_pack[off:off + n_].view(x.shape))
         off += n_
     h_o = torch.empty(tuple(o.shape), dtype=torch.float32).pin_memory()
     h2d = h_pack.numel() * 4
     d2h = h_o.numel() * 4
 
     def e2e_step(i):
-        d_pack.copy_(h_pack, non_blocking=True)
-        gdn.gdn_step(states[i % NSETS], *d_in, h_o, stream=stream)
+        gdn.gdn_step(states[i % NSETS], *h_in, h_o, stream=stream)
 
     for i in range(args.warmup):
         e2e_step(i)
@@ -543,10 +544,10 @@ def main():
     e2e = {"value": e2e_value, "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "ms_per_step": ms_e2e,
-           "note": "q, k, v, g, beta copied from one pinned host buffer "
-                   "(one copy) before each step's kernel; the kernel writes "
-                   "o into a pinned host buffer over the host link; the "
-                   "recurrent state stays resident on the device"}
+           "note": "the kernel reads q, k, v, g, beta from one pinned host "
+                   "buffer and writes o into another over the host link, "
+                   "every step; the recurrent state stays resident on the "
+                   "device"}
 
     # ---- parts: verify launches and prefill (rank 0 only, N = 1 shapes)
     parts = {}
