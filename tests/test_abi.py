@@ -81,6 +81,16 @@ def test_host_side_refusals(lib):
                            0, None) == gdn.GDN_ERANGE
     assert lib.gdn_prefill(ctypes.byref(ok), 8, *([None] * 7), 64, 7, None,
                            0, None) == gdn.GDN_ERANGE
+    # chunked modes: T * vh must stay below 2^31 (the tensor copies address
+    # a sequence's rows with strides below 2^40 bytes); the fp32 mode has no
+    # such limit and goes on to the buffer checks
+    wide = gdn.Shape(1, 16, 4096, 128, 128)
+    T = gdn.GDN_MAX_TOKENS                       # 2^20 * 4096 = 2^32
+    for prec in (gdn.GDN_PREC_BF16X3, gdn.GDN_PREC_BF16):
+        assert lib.gdn_prefill(ctypes.byref(wide), T, *([None] * 7), 64, prec,
+                               None, 0, None) == gdn.GDN_ERANGE
+    assert lib.gdn_prefill(ctypes.byref(wide), T, *([None] * 7), 64,
+                           gdn.GDN_PREC_FP32, None, 0, None) == gdn.GDN_EINVAL
 
 
 def test_binding_refuses_cpu_tensors(lib):
