@@ -36,13 +36,13 @@
 //          next chunk while its first products run
 // Every operand a thread writes is a row it owns: a row of an input, stored
 // in shared memory 8 elements at a time, or a TMEM lane of an earlier
-// result, which stays in its lane as an A operand in TMEM (S^T, -Y,
-// Delta^T); transposes happen in the MMA descriptors (MN-major operands),
-// never in memory.  The
-// next chunk's K and Q rows are tensor-copied into a staging tile about two
-// thirds of a chunk ahead; its V rows and gates are loaded into registers,
-// and its Q operand and gate vectors made, while the current chunk's last
-// products run.
+// result, which stays in its lane as an A operand in TMEM (S^T,
+// V^T - Y diag(gamma), Delta^T); transposes happen in the MMA descriptors
+// (MN-major operands), never in memory.  Every input tile arrives by tensor
+// copy a chunk ahead: K and Q into a region of their own per chunk parity,
+// where the next chunk's [K; Q] operand is made in place while the current
+// chunk's last products run; V into its region once the previous chunk's
+// rows are read.  The gates come through registers.
 //
 // Precision.  Operands are bf16 in shared memory:
 //   split-bf16 ("BF16X3"): x = hi + lo with hi = bf16(x), lo = bf16(x - hi);
@@ -99,8 +99,8 @@ constexpr uint32_t OFF_SCR = RC;            // fp32 A [64][64] + T [64][64]
 constexpr uint32_t OFF_TB2 = RC + 16384;    // 64 x 64: T diag(beta)
 constexpr uint32_t OFF_P = RP;              // 64 x 64
 constexpr uint32_t OFF_VEC = RP + 16384;    // Gamma, gamma, w, beta, gamma x 2, ea, eb
-constexpr uint32_t OFF_BAR = OFF_VEC + 2048;  // 15 mbarriers
-constexpr uint32_t OFF_SLOT = OFF_BAR + 120;  // TMEM address; +124: int flag
+constexpr uint32_t OFF_BAR = OFF_VEC + 2048;  // 14 mbarriers
+constexpr uint32_t OFF_SLOT = OFF_BAR + 112;  // TMEM address; +120: int flag
 constexpr uint32_t kSmemUsed = OFF_BAR + 128;
 constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;  // room to align the base
 
@@ -524,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // every factor is a normal fp32 number
   float *ea = Gam + 384;
   float *eb = Gam + 448;
-  volatile int *fac = reinterpret_cast<volatile int *>(gb + OFF_BAR + 124);
+  volatile int *fac = reinterpret_cast<volatile int *>(gb + OFF_BAR + 120);
   // mbarriers: products done (one commit each), operands ready (kSimt
   // arrivals each), and the final drain
   const uint32_t bar0 = sb + OFF_BAR;
@@ -536,8 +536,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t staged0 = bar0 + 72;  // K, Q rows of an even chunk in Ra
   const uint32_t v_free = bar0 + 80;   // the fp32 V rows in Rb are read
   const uint32_t vstaged = bar0 + 88;  // this chunk's fp32 V rows in region Rb
-  const uint32_t staged1 = bar0 + 104; // K, Q rows of an odd chunk in Rd
-  const uint32_t kq_free = bar0 + 112; // a chunk's [K; Q] region is free again
+  const uint32_t staged1 = bar0 + 96;  // K, Q rows of an odd chunk in Rd
+  const uint32_t kq_free = bar0 + 104; // a chunk's [K; Q] region is free again
   volatile uint32_t *slot = reinterpret_cast<volatile uint32_t *>(gb + OFF_SLOT);
   float *Asc = reinterpret_cast<float *>(gb + OFF_SCR);
   float *Tsc = Asc + 64 * 64;
@@ -654,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tl = tmem + lane_base;
 
     // On warp 0, the next chunk's gates of tokens lane and lane + 32 in
-    // registers.  (K, Q and V come through staging tiles.)
+    // registers.  (K, Q and V come by tensor copy.)
     float pg[2], pb[2];
     auto prefetch = [&](int c) {
       const int t0 = c * kC;
