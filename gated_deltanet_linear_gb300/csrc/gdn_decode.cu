@@ -395,26 +395,51 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, kCtasPerSm)
 
     const size_t hoff = head * (size_t)(kDim * kDim);
     const size_t eoff = (size_t)(8 * p) * kDim + col0;
-    for (int m = 0; m < M; ++m) {
-      TokenIn nxt = cur;
-      if constexpr (kOne) {
-        if (i + 1 < mine) nxt = token_at_one(i + 1);
-        token_update(s, cur, lane, o + o_off);
-      } else {
+    if constexpr (!kOne && !kCkpt) {
+      // tokens in pairs: cur and nxt take turns as the token being computed
+      // and the one being loaded, so no inputs are copied between registers
+      // (one copy per unit when M is odd)
+      TokenIn nxt;
+      auto load_after = [&](int m, TokenIn &dst) {
         if (m + 1 < M) {
-          nxt = token_at(cu, m + 1);
+          dst = token_at(cu, m + 1);
         } else if (i + 1 < mine) {
           nu = unit_at(i + 1);
-          nxt = token_at(nu, 0);
+          dst = token_at(nu, 0);
         }
+      };
+      for (int m = 0; m < M; m += 2) {
+        load_after(m, nxt);
         token_update(s, cur, lane, o + cu.v + (size_t)m * dv);
+        if (m + 1 == M) {
+          cur = nxt;
+          break;
+        }
+        load_after(m + 1, cur);
+        token_update(s, nxt, lane, o + cu.v + (size_t)(m + 1) * dv);
       }
-      if (kCkpt) {
-        float *cp = ckpt + (size_t)m * nheads * (kDim * kDim) + hoff + eoff;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) st_stream<kOne>(cp + j * kDim, s[j], pol);
+    } else {
+      for (int m = 0; m < M; ++m) {
+        TokenIn nxt = cur;
+        if constexpr (kOne) {
+          if (i + 1 < mine) nxt = token_at_one(i + 1);
+          token_update(s, cur, lane, o + o_off);
+        } else {
+          if (m + 1 < M) {
+            nxt = token_at(cu, m + 1);
+          } else if (i + 1 < mine) {
+            nu = unit_at(i + 1);
+            nxt = token_at(nu, 0);
+          }
+          token_update(s, cur, lane, o + cu.v + (size_t)m * dv);
+        }
+        if (kCkpt) {
+          float *cp = ckpt + (size_t)m * nheads * (kDim * kDim) + hoff + eoff;
+  #pragma unroll
+          for (int j = 0; j < 8; ++j) st_stream<kOne>(cp + j * kDim, s[j], pol);
+        }
+        cur = nxt;
       }
-      cur = nxt;
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j) st_stream<kOne>(S_out + hoff + eoff + j * kDim, s[j], pol);
