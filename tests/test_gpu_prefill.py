@@ -86,6 +86,21 @@ def test_chunked_full_size_sampled(oracle_mod, precision):
     assert gdn.gdn_prefill_timeouts() == 0
 
 
+@pytest.mark.parametrize("kh,vh,B", [(1, 1, 1), (4, 8, 3), (8, 8, 2)])
+def test_chunked_head_layouts(oracle_mod, kh, vh, B):
+    """Other key/value head counts: one head in all, two value heads per
+    key head, one value head per key head.  The tensor maps address q and k
+    by key head and v and o by value head, so every grouping must land on
+    the right rows (a ragged second chunk included)."""
+    inp = gdn_inputs.make_inputs(900 + kh * 10 + vh, B=B, T=70, kh=kh, vh=vh)
+    S, o = run_prefill(inp, gdn.GDN_PREC_BF16X3)
+    S_ref, o_ref = oracle_mod.run_inputs(inp)
+    es, eo = errs(host(S), host(o), S_ref, o_ref)
+    print(f"bf16x3 kh={kh} vh={vh} B={B}: state {es:.3e} o {eo:.3e}")
+    assert es < TOL[gdn.GDN_PREC_BF16X3] and eo < TOL[gdn.GDN_PREC_BF16X3]
+    assert gdn.gdn_prefill_timeouts() == 0
+
+
 def test_chunked_matches_token_serial_gpu():
     """The chunked form and the token-serial fp32 path agree (both on the
     GPU) to the split-bf16 tolerance on a 300-token run."""
