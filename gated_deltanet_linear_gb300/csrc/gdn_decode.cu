@@ -22,8 +22,9 @@
 // fused launch", section 3, split over 16 warps instead of one thread per
 // column).
 //
-// Memory pipeline.  The kernel is persistent (4 CTAs of 4 warps per SM, bound
-// by registers and shared memory): each warp walks a strided list
+// Memory pipeline.  The kernel is persistent (16 warps per SM, bound by
+// registers and shared memory, in CTAs of 8 warps for one token and of 4
+// for several): each warp walks a strided list
 // of units and keeps the next kStages - 1 of them in flight with cp.async
 // (16 bytes per lane per row, L2-only) into a private ring of 4 KB stages in
 // shared memory, so HBM reads continue while the warp computes.  A lane reads
@@ -52,12 +53,21 @@
 namespace gdn {
 namespace {
 
-constexpr int kWarpsPerCta = 4;   // warps are independent; 4 per CTA
 constexpr int kStages = 3;        // cp.async ring depth per warp
-constexpr int kCtasPerSm = 4;     // 4 x 48 KB of shared memory per SM
+constexpr int kWarpsPerSm = 16;   // bound by registers and shared memory
 constexpr int kUnitsPerHead = kDim / 8;          // 16 column groups
 constexpr int kUnitFloats = kDim * 8;            // 4 KB
-constexpr int kSmemPerCta = kWarpsPerCta * kStages * kUnitFloats * 4;
+// Warps per CTA: 8 for single-token launches, so that the 8 warps working
+// on neighbouring column groups of a head share its q and k rows in one
+// SM's L1 (with the token inputs in host memory the step took 86 us with 4
+// and 70 us with 8; with device inputs both take 70 us), and 4 for
+// multi-token launches (8 measured 2-7 % slower there).
+template <bool kOne>
+__host__ __device__ constexpr int warps_per_cta() { return kOne ? 8 : 4; }
+template <bool kOne>
+__host__ __device__ constexpr int smem_per_cta() {
+  return warps_per_cta<kOne>() * kStages * kUnitFloats * 4;
+}
 constexpr unsigned kFull = 0xffffffffu;
 
 // L2 policy for the single-token state stores: the written line keeps the
@@ -277,7 +287,8 @@ __device__ __forceinline__ void issue_unit(const float *S_in, size_t u,
 // otherwise a unit's offsets are found once and stepped per token (5 % faster
 // for M = 8).  The arithmetic is the same, so results are the same bits.
 template <bool kCkpt, bool kOne>
-__global__ void __launch_bounds__(kWarpsPerCta * 32, kCtasPerSm)
+__global__ void __launch_bounds__(warps_per_cta<kOne>() * 32,
+                                  kWarpsPerSm / warps_per_cta<kOne>())
     gdn_steps_kernel(const float *S_in, float *S_out,
                      float *__restrict__ ckpt, const float *__restrict__ q,
                      const float *__restrict__ k, const float *__restrict__ v,
@@ -294,8 +305,8 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, kCtasPerSm)
       (uint32_t)(warp * kStages * kUnitFloats * 4);
 
   const size_t nunits = nheads * kUnitsPerHead;
-  const size_t gw = (size_t)blockIdx.x * kWarpsPerCta + warp;
-  const size_t nw = (size_t)gridDim.x * kWarpsPerCta;
+  const size_t gw = (size_t)blockIdx.x * warps_per_cta<kOne>() + warp;
+  const size_t nw = (size_t)gridDim.x * warps_per_cta<kOne>();
   const size_t mine = gw < nunits ? (nunits - gw + nw - 1) / nw : 0;
   const uint64_t pol = kOne ? l2_keep_priority() : 0;
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -532,15 +543,17 @@ cudaError_t launch_steps(const float *S_in, float *S_out, float *ckpt,
   const size_t nheads = (size_t)B * vh;
   const size_t nunits = nheads * kUnitsPerHead;
   if (nunits == 0) return cudaSuccess;
-  size_t ctas = (nunits + kWarpsPerCta - 1) / kWarpsPerCta;
-  const size_t cap = (size_t)sm_count() * kCtasPerSm;
+  const int wpc = M == 1 ? warps_per_cta<true>() : warps_per_cta<false>();
+  const int smem = M == 1 ? smem_per_cta<true>() : smem_per_cta<false>();
+  size_t ctas = (nunits + wpc - 1) / wpc;
+  const size_t cap = (size_t)sm_count() * (kWarpsPerSm / wpc);
   if (ctas > cap) ctas = cap;
-  const dim3 grid((unsigned)ctas), block(kWarpsPerCta * 32);
+  const dim3 grid((unsigned)ctas), block(wpc * 32);
   auto go = [&](auto kernel, float *ck) {
     cudaError_t e = cudaFuncSetAttribute(
-        kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemPerCta);
+        kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return launch_maybe_overlapped(kernel, grid, block, kSmemPerCta, stream,
+    return launch_maybe_overlapped(kernel, grid, block, smem, stream,
                                    overlap, S_in, S_out, ck, q, k, v, g, beta,
                                    o, vh, kh, vh / kh, M, nheads);
   };
