@@ -53,15 +53,18 @@ int check_device_ptr(const void *p) {
 // mapped into the device's address space at the same address (any
 // cudaHostAlloc / cudaMallocHost block under unified addressing): kernels
 // then read and write it over the host link.  Pageable memory is refused.
-int check_io_ptr(const void *p) {
+// *host (if given) is set when p is host memory.
+int check_io_ptr(const void *p, bool *host = nullptr) {
   cudaPointerAttributes attr;
   memset(&attr, 0, sizeof(attr));
   if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
     cudaGetLastError();
     return GDN_EPTR;
   }
-  if (attr.type == cudaMemoryTypeHost)
+  if (attr.type == cudaMemoryTypeHost) {
+    if (host) *host = true;
     return attr.devicePointer == p ? GDN_OK : GDN_EPTR;
+  }
   return check_device_ptr(p);
 }
 
@@ -88,13 +91,13 @@ int check_bufs(const Buf *b, int n) {
 
 // check_bufs for token inputs and outputs (device, managed or mapped
 // page-locked host memory).
-int check_io_bufs(const Buf *b, int n) {
+int check_io_bufs(const Buf *b, int n, bool *any_host = nullptr) {
   for (int i = 0; i < n; ++i) {
     if (!b[i].p) return GDN_EINVAL;
     if (!aligned16(b[i].p)) return GDN_EALIGN;
   }
   for (int i = 0; i < n; ++i) {
-    const int r = check_io_ptr(b[i].p);
+    const int r = check_io_ptr(b[i].p, any_host);
     if (r != GDN_OK) return r;
   }
   return GDN_OK;
@@ -108,10 +111,12 @@ size_t state_floats(const gdn_shape *s) {
 
 // Validate and launch M serial tokens (shared by gdn_step, gdn_step_m and
 // the fp32 prefill path).
+// *host_inputs (if given) is set when a token input is host memory.
 int steps_common_check(const gdn_shape *s, int M, const float *S_in,
                        float *S_out, float *ckpt, const float *q,
                        const float *k, const float *v, const float *g,
-                       const float *beta, float *o) {
+                       const float *beta, float *o,
+                       bool *host_inputs = nullptr) {
   int r = check_shape(s);
   if (r) return r;
   if (M < 1 || M > GDN_MAX_TOKENS) return GDN_ERANGE;
@@ -128,7 +133,7 @@ int steps_common_check(const gdn_shape *s, int M, const float *S_in,
   Buf dev_bufs[] = {in[0], out[0], out[2]};
   r = check_bufs(dev_bufs, ckpt ? 3 : 2);
   if (r) return r;
-  r = check_io_bufs(in + 1, 5);
+  r = check_io_bufs(in + 1, 5, host_inputs);
   if (r) return r;
   r = check_io_bufs(out + 1, 1);
   if (r) return r;
@@ -149,11 +154,14 @@ int steps_common(const gdn_shape *s, int M, const float *S_in, float *S_out,
                  float *ckpt, const float *q, const float *k, const float *v,
                  const float *g, const float *beta, float *o,
                  cudaStream_t stream) {
-  const int r = steps_common_check(s, M, S_in, S_out, ckpt, q, k, v, g, beta, o);
+  bool host_inputs = false;
+  const int r = steps_common_check(s, M, S_in, S_out, ckpt, q, k, v, g, beta, o,
+                                   &host_inputs);
   if (r || s->B == 0) return r;
   cudaGetLastError();  // start from a clean per-thread error state
   return status_of(gdn::launch_steps(S_in, S_out, ckpt, q, k, v, g, beta, o,
-                                     s->B, s->kh, s->vh, M, stream));
+                                     s->B, s->kh, s->vh, M, stream, false,
+                                     host_inputs));
 }
 
 }  // namespace

@@ -23,8 +23,8 @@
 // column).
 //
 // Memory pipeline.  The kernel is persistent (16 warps per SM, bound by
-// registers and shared memory, in CTAs of 8 warps for one token and of 4
-// for several): each warp walks a strided list
+// registers and shared memory, in CTAs of 4 warps, or of 8 for one token
+// read from host memory): each warp walks a strided list
 // of units and keeps the next kStages - 1 of them in flight with cp.async
 // (16 bytes per lane per row, L2-only) into a private ring of 4 KB stages in
 // shared memory, so HBM reads continue while the warp computes.  A lane reads
@@ -57,16 +57,14 @@ constexpr int kStages = 3;        // cp.async ring depth per warp
 constexpr int kWarpsPerSm = 16;   // bound by registers and shared memory
 constexpr int kUnitsPerHead = kDim / 8;          // 16 column groups
 constexpr int kUnitFloats = kDim * 8;            // 4 KB
-// Warps per CTA: 8 for single-token launches, so that the 8 warps working
-// on neighbouring column groups of a head share its q and k rows in one
-// SM's L1 (with the token inputs in host memory the step took 86 us with 4
-// and 70 us with 8; with device inputs both take 70 us), and 4 for
-// multi-token launches (8 measured 2-7 % slower there).
-template <bool kOne>
-__host__ __device__ constexpr int warps_per_cta() { return kOne ? 8 : 4; }
-template <bool kOne>
+// Warps per CTA: 4, or 8 for single-token launches whose token inputs are
+// in host memory, so that the 8 warps working on neighbouring column groups
+// of a head share its q and k rows in one SM's L1 (the 64 x 48-head step
+// then takes 70 us instead of 86 us; with device inputs 4-warp CTAs are
+// 0.2 % faster, and 8 measured 2-7 % slower for several tokens).
+template <int kWarps>
 __host__ __device__ constexpr int smem_per_cta() {
-  return warps_per_cta<kOne>() * kStages * kUnitFloats * 4;
+  return kWarps * kStages * kUnitFloats * 4;
 }
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -286,9 +284,8 @@ __device__ __forceinline__ void issue_unit(const float *S_in, size_t u,
 // coordinates where its inputs are loaded (measured 0.8 % faster for M = 1);
 // otherwise a unit's offsets are found once and stepped per token (5 % faster
 // for M = 8).  The arithmetic is the same, so results are the same bits.
-template <bool kCkpt, bool kOne>
-__global__ void __launch_bounds__(warps_per_cta<kOne>() * 32,
-                                  kWarpsPerSm / warps_per_cta<kOne>())
+template <bool kCkpt, bool kOne, int kWarps>
+__global__ void __launch_bounds__(kWarps * 32, kWarpsPerSm / kWarps)
     gdn_steps_kernel(const float *S_in, float *S_out,
                      float *__restrict__ ckpt, const float *__restrict__ q,
                      const float *__restrict__ k, const float *__restrict__ v,
@@ -305,8 +302,8 @@ __global__ void __launch_bounds__(warps_per_cta<kOne>() * 32,
       (uint32_t)(warp * kStages * kUnitFloats * 4);
 
   const size_t nunits = nheads * kUnitsPerHead;
-  const size_t gw = (size_t)blockIdx.x * warps_per_cta<kOne>() + warp;
-  const size_t nw = (size_t)gridDim.x * warps_per_cta<kOne>();
+  const size_t gw = (size_t)blockIdx.x * kWarps + warp;
+  const size_t nw = (size_t)gridDim.x * kWarps;
   const size_t mine = gw < nunits ? (nunits - gw + nw - 1) / nw : 0;
   const uint64_t pol = kOne ? l2_keep_priority() : 0;
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -539,12 +536,12 @@ cudaError_t launch_steps(const float *S_in, float *S_out, float *ckpt,
                          const float *q, const float *k, const float *v,
                          const float *g, const float *beta, float *o, int B,
                          int kh, int vh, int M, cudaStream_t stream,
-                         bool overlap) {
+                         bool overlap, bool host_inputs) {
   const size_t nheads = (size_t)B * vh;
   const size_t nunits = nheads * kUnitsPerHead;
   if (nunits == 0) return cudaSuccess;
-  const int wpc = M == 1 ? warps_per_cta<true>() : warps_per_cta<false>();
-  const int smem = M == 1 ? smem_per_cta<true>() : smem_per_cta<false>();
+  const int wpc = M == 1 && host_inputs ? 8 : 4;
+  const int smem = wpc == 8 ? smem_per_cta<8>() : smem_per_cta<4>();
   size_t ctas = (nunits + wpc - 1) / wpc;
   const size_t cap = (size_t)sm_count() * (kWarpsPerSm / wpc);
   if (ctas > cap) ctas = cap;
@@ -559,11 +556,13 @@ cudaError_t launch_steps(const float *S_in, float *S_out, float *ckpt,
   };
   cudaError_t e;
   if (ckpt)
-    e = M == 1 ? go(gdn_steps_kernel<true, true>, ckpt)
-               : go(gdn_steps_kernel<true, false>, ckpt);
+    e = M > 1      ? go(gdn_steps_kernel<true, false, 4>, ckpt)
+        : wpc == 8 ? go(gdn_steps_kernel<true, true, 8>, ckpt)
+                   : go(gdn_steps_kernel<true, true, 4>, ckpt);
   else
-    e = M == 1 ? go(gdn_steps_kernel<false, true>, (float *)nullptr)
-               : go(gdn_steps_kernel<false, false>, (float *)nullptr);
+    e = M > 1      ? go(gdn_steps_kernel<false, false, 4>, (float *)nullptr)
+        : wpc == 8 ? go(gdn_steps_kernel<false, true, 8>, (float *)nullptr)
+                   : go(gdn_steps_kernel<false, true, 4>, (float *)nullptr);
   return e;
 }
 

@@ -14,11 +14,13 @@ constexpr int kDim = 128;  // kd == vd: the only head size the kernels serve
 // S_in.  ckpt may be nullptr.  overlap: launch as a programmatic dependent of
 // the previous kernel on the stream, which then must not write S_in (the
 // kernel starts loading the state before it waits for that kernel).
+// host_inputs: some token input is in mapped host memory (single-token
+// launches then use larger CTAs, whose warps share the inputs in L1).
 cudaError_t launch_steps(const float *S_in, float *S_out, float *ckpt,
                          const float *q, const float *k, const float *v,
                          const float *g, const float *beta, float *o, int B,
                          int kh, int vh, int M, cudaStream_t stream,
-                         bool overlap = false);
+                         bool overlap = false, bool host_inputs = false);
 
 // Layer prologue (conv1d + SiLU with a width-4 history, q/k normalisation,
 // gates) writing the token inputs q, k, v, g, beta of M tokens.  hist_in and
