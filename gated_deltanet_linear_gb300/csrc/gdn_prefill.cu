@@ -223,9 +223,9 @@ struct Gemm {
   bool accumulate;
   __device__ __forceinline__ Gemm(uint32_t d_, const Operand &a_,
                                   const Operand &b_, int M, int N,
-                                  bool accumulate_, bool negate_a = false)
+                                  bool accumulate_)
       : d(d_),
-        id(idesc_bf16(M, N, a_.mn, b_.mn) | (negate_a ? (1u << 13) : 0u)),
+        id(idesc_bf16(M, N, a_.mn, b_.mn)),
         ah(opdesc(a_, false)), bh(opdesc(b_, false)),
         al(kLo ? opdesc(a_, true) : 0), bl(kLo ? opdesc(b_, true) : 0),
         a(&a_), b(&b_), accumulate(accumulate_) {}
@@ -240,15 +240,6 @@ struct Gemm {
     }
   }
 };
-
-template <bool kLo, int KSTEPS>
-__device__ __forceinline__ void gemm(uint32_t d, const Operand &a,
-                                     const Operand &b, int M, int N,
-                                     bool accumulate, bool negate_a = false) {
-  const Gemm<kLo> g(d, a, b, M, N, accumulate, negate_a);
-#pragma unroll
-  for (int ks = 0; ks < KSTEPS; ++ks) g.step(ks, ks == 0);
-}
 
 // The same with A in tensor memory (see mma_bf16_ta): the hi and lo parts
 // of A start at TMEM addresses a and a_lo, and K step ks is 8 columns on.
