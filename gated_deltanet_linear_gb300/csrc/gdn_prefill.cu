@@ -377,67 +377,90 @@ __device__ __forceinline__ int sidx(int r, int c) {
   return r * 64 + ((((c >> 2) ^ (r & 7)) << 2) | (c & 3));
 }
 
+__device__ __forceinline__ void put_row4(float *X, int r, int c, float4 v) {
+  *reinterpret_cast<float4 *>(X + sidx(r, c)) = v;
+}
+
+__device__ __forceinline__ float4 get_row4(const float *X, int r, int c) {
+  return *reinterpret_cast<const float4 *>(X + sidx(r, c));
+}
+
+// Element e (a compile-time index after unrolling) of a float4.
+__device__ __forceinline__ float elem(const float4 &v, int e) {
+  return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+}
+
 // Y[r][c0..c0+3] = sum_{u0 <= u < n} X[xr][xc + u] * Z[zr + u][zc + c0 .. +3]
 // over the fp32 scratch layout (u0, n multiples of 4); returns the four sums.
+// (A compact loop: unrolled or software-pipelined forms of it measured
+// slower here, the instruction footprint and the shared-memory loads
+// counting for more than the load latency.)
 __device__ __forceinline__ float4 row_times(const float *X, int xr, int xc,
                                             const float *Z, int zr, int zc,
                                             int n, int u0 = 0) {
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int u4 = u0; u4 < n; u4 += 4) {
-    const float4 a = *reinterpret_cast<const float4 *>(X + sidx(xr, xc + u4));
-    const float av[4] = {a.x, a.y, a.z, a.w};
+    const float4 a = get_row4(X, xr, xc + u4);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float4 z = *reinterpret_cast<const float4 *>(Z + sidx(zr + u4 + e, zc));
-      acc.x = fmaf(av[e], z.x, acc.x);
-      acc.y = fmaf(av[e], z.y, acc.y);
-      acc.z = fmaf(av[e], z.z, acc.z);
-      acc.w = fmaf(av[e], z.w, acc.w);
+      const float4 z = get_row4(Z, zr + u4 + e, zc);
+      const float ae = elem(a, e);
+      acc.x = fmaf(ae, z.x, acc.x);
+      acc.y = fmaf(ae, z.y, acc.y);
+      acc.z = fmaf(ae, z.z, acc.z);
+      acc.w = fmaf(ae, z.w, acc.w);
     }
   }
   return acc;
-}
-
-__device__ __forceinline__ void put_row4(float *X, int r, int c, float4 v) {
-  *reinterpret_cast<float4 *>(X + sidx(r, c)) = v;
 }
 
 // T = (I + A)^-1 for strictly lower-triangular A (64 x 64), by divide and
 // conquer: invert the four 16 x 16 diagonal blocks, merge them into 32 x 32
 // inverses, then into the 64 x 64 inverse, using
 //   [[E1, 0], [A21, E2]]^-1 = [[E1^-1, 0], [-E2^-1 A21 E1^-1, E2^-1]].
-// The kSimt SIMT threads.  Reads the lower triangle of Asc; its upper triangle
-// (zero, never read as A) holds the intermediate products.  Writes Tsc.
+// The kSimt SIMT threads.  Reads the lower triangle of Asc (its upper
+// triangle is zero on entry and then holds the intermediate products);
+// writes all of Tsc, zeros above the diagonal.
 __device__ __forceinline__ void tri_inverse(float *Asc, float *Tsc, int tid) {
-  // 1. Diagonal blocks by forward substitution: column j of block i on 4
-  //    lanes, rows split by r mod 4.  Each lane keeps, for its rows t, the
-  //    running sum p_t of A[t][k] x_k over the x_k known so far; x_k is
-  //    final once p_k has all k terms, and its owner broadcasts it with one
-  //    shuffle, so the serial chain per step is a shuffle and an FMA.  A is
-  //    strictly lower, so terms with k >= t add exact zeros.
-  {
-    const int col = tid >> 2;          // 0..63: block i = col / 16
-    const int q4 = tid & 3;
-    const int blk = col >> 4, jj = col & 15, r0 = blk * 16;
-    const int lane = tid & 31;
-    float x[4] = {0.f, 0.f, 0.f, 0.f};  // rows r0 + q4 + 4i
-    float p[4] = {0.f, 0.f, 0.f, 0.f};
+  const int warp = tid >> 5, lane = tid & 31;
+  if (warp < 2) {
+    // 1. Diagonal blocks by forward substitution, one column per lane, in
+    //    registers: warp w takes blocks 2w (lanes 0-15) and 2w + 1 (lanes
+    //    16-31), lane its block's column jj.  p_t is the running sum of
+    //    A[t][k] x_k over the x_k known so far; x_k is final once p_k has
+    //    its k terms, and then enters the sums of the rows below it, so the
+    //    serial chain per step is one subtraction and one FMA.  The sums
+    //    run in order of k.
+    const int hi = lane >> 4, jj = lane & 15;
+    const int r0 = 32 * warp + 16 * hi;
+    float x[16], p[16];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      float xk = 0.f;
-      if ((k & 3) == q4) {
-        xk = (k == jj ? 1.f : 0.f) - p[k >> 2];
-        x[k >> 2] = xk;
+    for (int t = 0; t < 16; ++t) p[t] = 0.f;
+#pragma unroll
+    for (int k4 = 0; k4 < 4; ++k4) {
+      float4 a[16];  // A[r0 + t][r0 + 4 k4 .. + 3] for the rows t below
+#pragma unroll
+      for (int t = 4 * k4 + 1; t < 16; ++t) a[t] = get_row4(Asc, r0 + t, r0 + 4 * k4);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int k = 4 * k4 + e;
+        x[k] = (k == jj ? 1.f : 0.f) - p[k];
+#pragma unroll
+        for (int t = k + 1; t < 16; ++t) p[t] = fmaf(elem(a[t], e), x[k], p[t]);
       }
-      xk = __shfl_sync(0xffffffffu, xk, (lane & ~3) | (k & 3));
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        p[i] = fmaf(Asc[sidx(r0 + q4 + 4 * i, r0 + k)], xk, p[i]);
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) Tsc[sidx(r0 + q4 + 4 * i, r0 + jj)] = x[i];
-    // zero the strictly-upper part of this column
-    for (int r = q4; r < r0; r += 4) Tsc[sidx(r, r0 + jj)] = 0.f;
+    for (int t = 0; t < 16; ++t) Tsc[sidx(r0 + t, r0 + jj)] = x[t];
+  } else {
+    // Meanwhile the other warps write the zeros above the block diagonal:
+    // rows 0-15 of columns 16-31, rows 0-31 of 32-47, rows 0-47 of 48-63
+    // (64 + 128 + 192 groups of four).
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int idx = tid - 64; idx < 384; idx += kSimt - 64) {
+      const int b = idx < 64 ? 1 : idx < 192 ? 2 : 3;
+      const int rel = idx - (b == 1 ? 0 : b == 2 ? 64 : 192);
+      put_row4(Tsc, rel >> 2, 16 * b + 4 * (rel & 3), z);
+    }
   }
   simt_sync();
   // 2. 16 -> 32: blocks (1,0) and (3,2).  Thread: block pair p, row r,
@@ -457,15 +480,15 @@ __device__ __forceinline__ void tri_inverse(float *Asc, float *Tsc, int tid) {
     float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int u4 = 0; u4 < 16; u4 += 4) {
-      const float4 e = *reinterpret_cast<const float4 *>(Tsc + sidx(16 * i + r, 16 * i + u4));
-      const float ev[4] = {e.x, e.y, e.z, e.w};
+      const float4 e = get_row4(Tsc, 16 * i + r, 16 * i + u4);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const float4 z = *reinterpret_cast<const float4 *>(Asc + sidx(16 * j + u4 + q, 16 * i + c4));
-        y.x = fmaf(ev[q], z.x, y.x);
-        y.y = fmaf(ev[q], z.y, y.y);
-        y.z = fmaf(ev[q], z.z, y.z);
-        y.w = fmaf(ev[q], z.w, y.w);
+        const float4 z = get_row4(Asc, 16 * j + u4 + q, 16 * i + c4);
+        const float eq = elem(e, q);
+        y.x = fmaf(eq, z.x, y.x);
+        y.y = fmaf(eq, z.y, y.y);
+        y.z = fmaf(eq, z.z, y.z);
+        y.w = fmaf(eq, z.w, y.w);
       }
     }
     put_row4(Tsc, 16 * i + r, 16 * j + c4, make_float4(-y.x, -y.y, -y.z, -y.w));
@@ -478,15 +501,13 @@ __device__ __forceinline__ void tri_inverse(float *Asc, float *Tsc, int tid) {
   //    k = 4w on, then rows 4w .. 4w+3 of the result (lanes: row 4w + lane/8,
   //    columns 4 (lane % 8)) up to k = 4w+3.  The sums keep their order.
   {
-    const int w = tid >> 5, lane = tid & 31, c4 = 4 * w;
-    put_row4(Asc, lane, 32 + c4,
-             row_times(Asc, 32 + lane, 0, Tsc, 0, c4, 32, c4));
+    const int c4 = 4 * warp;
+    put_row4(Asc, lane, 32 + c4, row_times(Asc, 32 + lane, 0, Tsc, 0, c4, 32, c4));
   }
   simt_sync();
   {
-    const int w = tid >> 5, lane = tid & 31;
-    const int r = 4 * w + (lane >> 3), c4 = (lane & 7) * 4;
-    const float4 y = row_times(Tsc, 32 + r, 32, Asc, 0, 32 + c4, 4 * w + 4);
+    const int r = 4 * warp + (lane >> 3), c4 = (lane & 7) * 4;
+    const float4 y = row_times(Tsc, 32 + r, 32, Asc, 0, 32 + c4, 4 * warp + 4);
     put_row4(Tsc, 32 + r, c4, make_float4(-y.x, -y.y, -y.z, -y.w));
   }
   simt_sync();
