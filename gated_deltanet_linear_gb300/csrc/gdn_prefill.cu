@@ -85,7 +85,8 @@ constexpr int kThreads = kSimt + 64;
 //   Rc 32 KB: o of the previous chunk (fp32 [t][dv], 64 x 128, read by a
 //             tensor store before the A build)
 //                                     -> A, T scratch (fp32)
-//                                     -> T diag(beta) (64 x 64)
+//                                     -> T diag(beta) (64 x 64) over the
+//                                        A half, while T is still read
 //   Rd 64 KB: the same for odd chunks, so a chunk's K, Q arrive and are
 //             converted while the previous chunk still reads its own
 //   Rp 16 KB: P (64 x 64)
@@ -96,7 +97,7 @@ __host__ __device__ constexpr uint32_t kq_region(int c) { return (c & 1) ? RD : 
 constexpr uint32_t OFF_V = RB;              // fp32 V rows [64][128]
 constexpr uint32_t OFF_OT = RC;             // fp32 o tile [64][128]
 constexpr uint32_t OFF_SCR = RC;            // fp32 A [64][64] + T [64][64]
-constexpr uint32_t OFF_TB2 = RC + 16384;    // 64 x 64: T diag(beta)
+constexpr uint32_t OFF_TB2 = RC;            // 64 x 64: T diag(beta), over A
 constexpr uint32_t OFF_P = RP;              // 64 x 64
 constexpr uint32_t OFF_VEC = RP + 16384;    // Gamma, gamma, w, beta, gamma x 2, ea, eb
 constexpr uint32_t OFF_BAR = OFF_VEC + 2048;  // 14 mbarriers
@@ -899,9 +900,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tri_inverse(Asc, Tsc, tid);
+      // (its barriers also follow every read of the V rows above)
+      if (tid == 0) mbar_arrive(v_free);
 
-      // T diag(beta), the B operand; each thread takes one row-half of T:
-      // row t = tid >> 2, 16 columns
+      // T diag(beta), the B operand, over the A scratch (the inverse has
+      // finished with it); each thread takes one row-half of T: row
+      // t = tid >> 2, 16 columns
       const int t_row = tid >> 2, cq = (tid & 3) * 16;
       float tr[16];
 #pragma unroll
@@ -912,8 +916,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tr[e4 + 2] = v4.z;
         tr[e4 + 3] = v4.w;
       }
-      simt_sync();  // T values held, V rows read: scratch and Rb may be reused
-      if (tid == 0) mbar_arrive(v_free);
 #pragma unroll
       for (int h8 = 0; h8 < 2; ++h8) {
         float x2[8];
