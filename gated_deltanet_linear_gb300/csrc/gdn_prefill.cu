@@ -99,10 +99,14 @@ constexpr uint32_t OFF_OT = RC;             // fp32 o tile [64][128]
 constexpr uint32_t OFF_SCR = RC;            // fp32 A [64][64] + T [64][64]
 constexpr uint32_t OFF_TB2 = RC;            // 64 x 64: T diag(beta), over A
 constexpr uint32_t OFF_P = RP;              // 64 x 64
-constexpr uint32_t OFF_VEC = RP + 16384;    // Gamma, gamma, w, beta, gamma x 2, ea, eb
+// Gate vectors in buffers of 512 floats: Gamma +0, gamma +64, w +128,
+// beta +192, ea +384, eb +448; buffer 0's +256 holds gamma of the chunk
+// whose o is pending ([2][64], used when there is one buffer).
+constexpr uint32_t OFF_VEC = RP + 16384;      // buffer 0
 constexpr uint32_t OFF_BAR = OFF_VEC + 2048;  // 14 mbarriers
-constexpr uint32_t OFF_SLOT = OFF_BAR + 112;  // TMEM address; +120: int flag
-constexpr uint32_t kSmemUsed = OFF_BAR + 128;
+constexpr uint32_t OFF_SLOT = OFF_BAR + 112;  // TMEM address; +120: int flags
+constexpr uint32_t OFF_VEC1 = OFF_BAR + 128;  // buffer 1
+constexpr uint32_t kSmemUsed = OFF_VEC1 + 2048;
 constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;  // room to align the base
 
 // TMEM columns (512 allocated).
@@ -421,8 +425,12 @@ __device__ __forceinline__ float4 row_times(const float *X, int xr, int xc,
 //   [[E1, 0], [A21, E2]]^-1 = [[E1^-1, 0], [-E2^-1 A21 E1^-1, E2^-1]].
 // The kSimt SIMT threads.  Reads the lower triangle of Asc (its upper
 // triangle is zero on entry and then holds the intermediate products);
-// writes all of Tsc, zeros above the diagonal.
-__device__ __forceinline__ void tri_inverse(float *Asc, float *Tsc, int tid) {
+// writes all of Tsc, zeros above the diagonal.  With kSide, warp 7 runs
+// `side()` (work of its own that reads neither scratch) during the first
+// step instead of taking part in it.
+template <bool kSide, class Side>
+__device__ __forceinline__ void tri_inverse(float *Asc, float *Tsc, int tid,
+                                            Side &&side) {
   const int warp = tid >> 5, lane = tid & 31;
   if (warp < 2) {
     // 1. Diagonal blocks by forward substitution, one column per lane, in
@@ -452,12 +460,14 @@ __device__ __forceinline__ void tri_inverse(float *Asc, float *Tsc, int tid) {
     }
 #pragma unroll
     for (int t = 0; t < 16; ++t) Tsc[sidx(r0 + t, r0 + jj)] = x[t];
+  } else if (kSide && warp == kSimt / 32 - 1) {
+    side();
   } else {
     // Meanwhile the other warps write the zeros above the block diagonal:
     // rows 0-15 of columns 16-31, rows 0-31 of 32-47, rows 0-47 of 48-63
     // (64 + 128 + 192 groups of four).
     const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int idx = tid - 64; idx < 384; idx += kSimt - 64) {
+    for (int idx = tid - 64; idx < 384; idx += (kSide ? kSimt - 32 : kSimt) - 64) {
       const int b = idx < 64 ? 1 : idx < 192 ? 2 : 3;
       const int rel = idx - (b == 1 ? 0 : b == 2 ? 64 : 192);
       put_row4(Tsc, rel >> 2, 16 * b + 4 * (rel & 3), z);
@@ -523,21 +533,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const float *__restrict__ beta,
                      const __grid_constant__ CUtensorMap tm_o, int T, int kh,
                      int vh, int rep) {
+  // Where the gate warp makes the next chunk's gate vectors: warp 7, during
+  // the inverse's first step (bf16), or warp 0, after the next chunk's
+  // [K; Q] operand, under the chunk's last products (split-bf16, whose last
+  // products take long enough to hide them; measured faster there).
+  constexpr bool kGatesInInverse = !kLo;
+  constexpr int kGateWarp = kGatesInInverse ? kSimt / 32 - 1 : 0;
+  // Gate-vector buffer of chunk c: c & 1 when the next chunk's vectors are
+  // made while the chunk still reads its own (during the inverse), else
+  // one buffer, the next chunk's written after the chunk's last read.
+  auto vbuf = [](int c) { return kGatesInInverse ? (c & 1) : 0; };
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw_s = (uint32_t)__cvta_generic_to_shared(smem_raw);
   const uint32_t sb = (raw_s + 1023u) & ~1023u;
   unsigned char *gb = smem_raw + (sb - raw_s);
-  float *Gam = reinterpret_cast<float *>(gb + OFF_VEC);
-  float *gam = Gam + 64;
-  float *wv = Gam + 128;
-  float *bet = Gam + 192;
-  float *gam_o = Gam + 256;       // [2][64]: gamma of the chunk whose o is pending
-  // exp(Gamma_t - Gamma_s) = ea[t] eb[s] about the middle of the chunk's
-  // range of Gamma; used when that range is at most 160 (*fac != 0), where
-  // every factor is a normal fp32 number
-  float *ea = Gam + 384;
-  float *eb = Gam + 448;
-  volatile int *fac = reinterpret_cast<volatile int *>(gb + OFF_BAR + 120);
+  // Gate vectors by chunk parity (see gates below): Gamma, gamma, w, beta,
+  // and exp(Gamma_t - Gamma_s) = ea[t] eb[s] about the middle of the
+  // chunk's range of Gamma, used when that range is at most 160 (fac != 0),
+  // where every factor is a normal fp32 number.
+  auto gvec = [&](int buf) {
+    return reinterpret_cast<float *>(gb + (buf ? OFF_VEC1 : OFF_VEC));
+  };
+  float *const gam_o = gvec(0) + 256;  // [2][64], single-buffer mode
+  volatile int *const fac2 = reinterpret_cast<volatile int *>(gb + OFF_BAR + 120);
   // mbarriers: products done (one commit each), operands ready (kSimt
   // arrivals each), and the final drain
   const uint32_t bar0 = sb + OFF_BAR;
@@ -666,21 +684,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ the SIMT warps
     const uint32_t tl = tmem + lane_base;
 
-    // On warp 0, the next chunk's gates of tokens lane and lane + 32 in
-    // registers.  (K, Q and V come by tensor copy.)
+    // On the gate warp, the next chunk's g and beta of tokens lane and
+    // lane + 32 in registers.  (K, Q and V come by tensor copy.)
     float pg[2], pb[2];
     auto prefetch = [&](int c) {
       const int t0 = c * kC;
       const int n = min(kC, T - t0);
       const size_t v_base = ((size_t)b * T + t0) * vh + vi;
-      if (warp == 0) {
+      if (warp == kGateWarp) {
         pg[0] = lane < n ? __ldg(g + v_base + (size_t)lane * vh) : 0.f;
         pg[1] = lane + 32 < n ? __ldg(g + v_base + (size_t)(lane + 32) * vh) : 0.f;
         pb[0] = lane < n ? __ldg(beta + v_base + (size_t)lane * vh) : 0.f;
         pb[1] = lane + 32 < n ? __ldg(beta + v_base + (size_t)(lane + 32) * vh) : 0.f;
       }
     };
-    if (warp == 0) prefetch(0);
+    if (warp == kGateWarp) prefetch(0);
 
     // State in: S[dk][dv] -> TMEM lane dv, column dk.
     {
@@ -699,7 +717,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // global stores leave the SIMT warps' path.
     float *otile = reinterpret_cast<float *>(gb + OFF_OT);
     auto emit_o = [&](int cc) {
-      const float *gm = gam_o + (cc & 1) * 64;
+      const float *gm = kGatesInInverse ? gvec(cc & 1) + 64  // gamma of chunk cc
+                                        : gam_o + (cc & 1) * 64;
       const uint32_t pdq = T_BUF;
       for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
         float r[16], pd[16];
@@ -723,11 +742,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       bulk_commit();
     };
 
-    // Gate vectors of chunk cc from the prefetched g, beta (warp 0): the
-    // cumulative log-decay Gamma, gamma, w, beta, the factors ea, eb.
-    // Run for chunk c + 1 while chunk c's last products finish; the SIMT
-    // barrier that ends that wait makes them visible.
+    // Gate vectors of chunk cc from the prefetched g, beta (the gate warp):
+    // the cumulative log-decay Gamma, gamma, w, beta, the factors ea, eb,
+    // into buffer cc & 1.  Run for chunk c + 1 during chunk c (see
+    // kGatesInInverse), before a SIMT barrier that makes them visible; the
+    // buffer's previous contents (chunk c - 1) were last read by that
+    // chunk's output, at the top of chunk c.
     auto gates = [&](int cc) {
+      float *Gam = gvec(vbuf(cc));
+      float *gam = Gam + 64, *wv = Gam + 128, *bet = Gam + 192;
+      float *ea = Gam + 384, *eb = Gam + 448;
       bet[lane] = pb[0];
       bet[lane + 32] = pb[1];
       float sa = pg[0], sc = pg[1];
@@ -746,8 +770,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       Gam[lane + 32] = sc;
       gam[lane] = expf(sa);
       gam[lane + 32] = expf(sc);
-      gam_o[(cc & 1) * 64 + lane] = gam[lane];
-      gam_o[(cc & 1) * 64 + lane + 32] = gam[lane + 32];
+      if (!kGatesInInverse) {
+        gam_o[(cc & 1) * 64 + lane] = gam[lane];
+        gam_o[(cc & 1) * 64 + lane + 32] = gam[lane + 32];
+      }
       wv[lane] = expf(last - sa);
       wv[lane + 32] = expf(last - sc);
       float gmax = fmaxf(sa, sc), gmin = fminf(sa, sc);
@@ -761,9 +787,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ea[lane + 32] = expf(sc - ref);
       eb[lane] = expf(ref - sa);
       eb[lane + 32] = expf(ref - sc);
-      if (lane == 0) *fac = (gmax - gmin <= 160.f) ? 1 : 0;
+      if (lane == 0) fac2[vbuf(cc)] = (gmax - gmin <= 160.f) ? 1 : 0;
     };
-    if (warp == 0) gates(0);
+    if (warp == kGateWarp) gates(0);
     // [K; Q] operand of chunk cc, in place in its region: this thread's
     // fp32 rows (tid >> 4) + 16 i, columns (tid & 15) * 8 .. + 7, are read
     // into registers, then, after a barrier, written back as bf16 operand
@@ -796,9 +822,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!failed) signal_ready(rdy_a);  // -> MMA-a of chunk 0
     for (int c = 0; !failed && c < nchunks; ++c) {
       // ---------------------------------------------------- phase 0: inputs
-      // This chunk's [K; Q] operand and gates were made, and MMA-a
-      // released, during the previous chunk's last products (before the
-      // loop for chunk 0).
+      // This chunk's [K; Q] operand was made, and MMA-a released, during
+      // the previous chunk's last products, and its gates during the
+      // previous chunk's inverse (both before the loop for chunk 0).
+      const float *Gam = gvec(vbuf(c));
+      const float *gam = Gam + 64, *wv = Gam + 128, *bet = Gam + 192;
+      const float *ea = Gam + 384, *eb = Gam + 448;
+      if (kGatesInInverse && warp == kGateWarp && c + 1 < nchunks) prefetch(c + 1);
       if (c > 0) emit_o(c - 1);  // the previous chunk's output, into the o tile
       simt_sync();  // the o tile is written
       if (c > 0 && tid == 0) store_o(c - 1);
@@ -823,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_after_sync();
 
       // ----------------- phase 2: A and P, T = (I + A)^-1, T diag operands
-      const bool factored = *fac != 0;
+      const bool factored = fac2[vbuf(c)] != 0;
       if (quad < 2) {  // lanes 0-63 hold G rows t
         const int t = myrow;
         const float bt = bet[t], Gt = Gam[t], bea = bt * ea[t];
@@ -899,7 +929,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           put16_tmem<kLo>(tl + T_AOP, tl + T_AOP + 32, c0, r);
         }
       }
-      tri_inverse(Asc, Tsc, tid);
+      tri_inverse<kGatesInInverse>(Asc, Tsc, tid, [&] {
+        if (kGatesInInverse && c + 1 < nchunks) gates(c + 1);
+      });
       // (its barriers also follow every read of the V rows above)
       if (tid == 0) mbar_arrive(v_free);
 
@@ -925,7 +957,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_wait_st();
       signal_ready(rdy_t);  // -> MMA-ud: Delta^T = (V^T - Y diag(gamma)) (T diag(beta))^T
-      if (warp == 0 && c + 1 < nchunks) prefetch(c + 1);  // lands under the work below
+      if (!kGatesInInverse && warp == kGateWarp && c + 1 < nchunks) prefetch(c + 1);
       if (!simt_and(mbar_wait(done_d, parity, kWaitLimit))) { failed = true; break; }
       fence_after_sync();
 
@@ -942,10 +974,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       signal_ready(rdy_d);  // -> MMA-3: (P Delta)^T;  MMA-4: S^T += ...
       if (c + 1 < nchunks) {
         // Under MMA-3 and MMA-4: the next chunk's [K; Q] operand (in the
-        // other region) and gates; then MMA-a of the next chunk is released
-        // (it queues behind this chunk's products).
+        // other region), and, if not made during the inverse, its gates;
+        // then MMA-a of the next chunk is released (it queues behind this
+        // chunk's products).
         if (!kq_operand(c + 1)) { failed = true; break; }
-        if (warp == 0) gates(c + 1);
+        if (!kGatesInInverse && warp == kGateWarp) gates(c + 1);
         signal_ready(rdy_a);
       }
       if (!simt_and(mbar_wait(done_4, parity, kWaitLimit))) { failed = true; break; }
