@@ -929,9 +929,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           put16_tmem<kLo>(tl + T_AOP, tl + T_AOP + 32, c0, r);
         }
       }
-      tri_inverse<kGatesInInverse>(Asc, Tsc, tid, [&] {
-        if (kGatesInInverse && c + 1 < nchunks) gates(c + 1);
-      });
+      if constexpr (kGatesInInverse)
+        tri_inverse<true>(Asc, Tsc, tid, [&] {
+          if (c + 1 < nchunks) gates(c + 1);
+        });
+      else
+        tri_inverse<false>(Asc, Tsc, tid, [] {});
       // (its barriers also follow every read of the V rows above)
       if (tid == 0) mbar_arrive(v_free);
 
