@@ -98,6 +98,25 @@ def test_reset_inside_chunks(oracle_mod, precision):
 
 
 @pytest.mark.parametrize("precision", [gdn.GDN_PREC_BF16X3, gdn.GDN_PREC_BF16])
+def test_factored_flag_alternates(oracle_mod, precision):
+    """Chunks that alternate between the factored exponentials (range of
+    Gamma over the chunk at most 160) and one exp per element (a reset in
+    the chunk): the kernel keeps the choice per chunk, next to that chunk's
+    gate vectors, and the bf16 mode makes chunk c + 1's vectors while chunk
+    c still reads its own."""
+    inp = gdn_inputs.make_inputs(1206, B=2, T=200, g_scale=0.1)
+    for t in (100, 195):  # chunks 1 and 3 of 0..3
+        inp.g[:, t] = -200.0
+    S, o = _prefill(inp, precision)
+    S_ref, o_ref = oracle_mod.run_inputs(inp)
+    es = max_rel(S, S_ref, axes=(-2, -1))
+    eo = max_rel(o, o_ref, axes=(-2, -1))
+    print(f"alternating factored chunks {precision}: state {es:.3e} o {eo:.3e}")
+    assert es < TOL_CHUNK[precision] and eo < TOL_CHUNK[precision]
+    assert gdn.gdn_prefill_timeouts() == 0
+
+
+@pytest.mark.parametrize("precision", [gdn.GDN_PREC_BF16X3, gdn.GDN_PREC_BF16])
 @pytest.mark.parametrize("g_const", [-2.4, -2.6])
 def test_strong_uniform_decay_chunked(oracle_mod, precision, g_const):
     """A constant decay whose range over a 64-token chunk (63 |g|) is just
