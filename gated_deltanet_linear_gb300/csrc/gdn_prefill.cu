@@ -365,10 +365,12 @@ __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
-// Wait until this thread's bulk stores have read their shared-memory source
-// (the tile may be overwritten), or (`all`) have completed.
+// Wait until all but the last `kPending` of this thread's committed groups
+// of bulk stores have read their shared-memory source (which may then be
+// overwritten), or (bulk_wait_all) until every one has completed.
+template <int kPending>
 __device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(kPending) : "memory");
 }
 
 __device__ __forceinline__ void bulk_wait_all() {
@@ -713,8 +715,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // o for chunk cc = diag(gamma) (Q S)^T + (P Delta)^T, read from TMEM
     // into the o tile ([t][dv] rows of 512 bytes, the layout of o), then
-    // written out by one tensor store (store_o) after a SIMT barrier, so the
-    // global stores leave the SIMT warps' path.
+    // written out by two tensor stores (store_o) after a SIMT barrier, so
+    // the global stores leave the SIMT warps' path.
     float *otile = reinterpret_cast<float *>(gb + OFF_OT);
     auto emit_o = [&](int cc) {
       const float *gm = kGatesInInverse ? gvec(cc & 1) + 64  // gamma of chunk cc
@@ -735,11 +737,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async();  // the tile is read by the copy engine
     };
-    // Thread 0, after the barrier that follows emit_o(cc): one tensor store
-    // of the tile (rows past T are not written).
+    // Thread 0, after the barrier that follows emit_o(cc): the tile's two
+    // halves of 32 rows by one tensor store each, in two commit groups, so
+    // the first half (the A scratch's region) is free once its own store has
+    // read it.  Rows past T are not written; a half that starts past T is
+    // not stored (only the last chunk's can).
     auto store_o = [&](int cc) {
       tma_store_rows(&tm_o, vi, cc * kC, b, sb + OFF_OT);
       bulk_commit();
+      if (cc * kC + kC / 2 < T) {
+        tma_store_rows(&tm_o, vi, cc * kC + kC / 2, b, sb + OFF_OT + kC / 2 * kD * 4);
+        bulk_commit();
+      }
     };
 
     // Gate vectors of chunk cc from the prefetched g, beta (the gate warp):
@@ -848,7 +857,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       signal_ready(rdy_s);  // -> MMA-s: [Y | (Q S)^T] = S^T [K; Q]^T
-      if (c > 0 && tid == 0) bulk_wait_read();  // the o tile's region is reused
+      // the o tile's first half is reused by the A scratch (both halves
+      // were stored: chunk c - 1 is a full chunk)
+      if (c > 0 && tid == 0) bulk_wait_read<1>();
       if (!simt_and(mbar_wait(done_a, parity, kWaitLimit))) { failed = true; break; }
       fence_after_sync();
 
@@ -914,7 +925,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // = V^T (T diag(beta))^T - Y (T diag(beta gamma))^T
       // = (V^T - Y diag(gamma)) (T diag(beta))^T.  V comes from its fp32
       // rows in region Rb (row s, this lane's column), Y from MMA-s.
-      // (The wait is also the barrier between the A build and the inverse.)
+      // (The wait is also the barrier between the A build and the inverse,
+      // and, on thread 0, for the o tile's second half, which the inverse's
+      // T scratch reuses.)
+      if (c > 0 && tid == 0) bulk_wait_read<0>();
       if (!simt_and(mbar_wait(done_s, parity, kWaitLimit) &&
                     mbar_wait(vstaged, parity, kWaitLimit))) { failed = true; break; }
       fence_after_sync();
@@ -1037,11 +1051,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
 }
 
 // Tensor map over a [B][T][heads][128] fp32 array (q, k, v or o) as a 4-d
-// tensor {128, heads, T, B}; one box is the 64 token rows of one head of one
+// tensor {128, heads, T, B}; one box is `rows` token rows of one head of one
 // sequence.  Rows past T are outside the tensor: zeros when loaded, skipped
 // when stored.
 cudaError_t rows_map(CUtensorMap *map, const float *base, int heads, int T,
-                     int B) {
+                     int B, int rows) {
   const PFN_cuTensorMapEncodeTiled_v12000 fn = encode_tiled();
   if (fn == nullptr) return cudaErrorNotSupported;
   const cuuint64_t row = (cuuint64_t)kD * sizeof(float);
@@ -1049,7 +1063,7 @@ cudaError_t rows_map(CUtensorMap *map, const float *base, int heads, int T,
                               (cuuint64_t)B};
   const cuuint64_t strides[3] = {row, row * (cuuint64_t)heads,
                                  row * (cuuint64_t)heads * (cuuint64_t)T};
-  const cuuint32_t box[4] = {(cuuint32_t)kD, 1, (cuuint32_t)kC, 1};
+  const cuuint32_t box[4] = {(cuuint32_t)kD, 1, (cuuint32_t)rows, 1};
   const cuuint32_t step[4] = {1, 1, 1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
                         const_cast<float *>(base), dims, strides, box, step,
@@ -1071,10 +1085,10 @@ cudaError_t launch_prefill_chunked(float *S, const float *q, const float *k,
   if (nheads > 0x7fffffffull) return cudaErrorInvalidConfiguration;
   CUtensorMap tm_q, tm_k, tm_v, tm_o;
   cudaError_t e;
-  if ((e = rows_map(&tm_q, q, kh, T, B)) != cudaSuccess) return e;
-  if ((e = rows_map(&tm_k, k, kh, T, B)) != cudaSuccess) return e;
-  if ((e = rows_map(&tm_v, v, vh, T, B)) != cudaSuccess) return e;
-  if ((e = rows_map(&tm_o, o, vh, T, B)) != cudaSuccess) return e;
+  if ((e = rows_map(&tm_q, q, kh, T, B, kC)) != cudaSuccess) return e;
+  if ((e = rows_map(&tm_k, k, kh, T, B, kC)) != cudaSuccess) return e;
+  if ((e = rows_map(&tm_v, v, vh, T, B, kC)) != cudaSuccess) return e;
+  if ((e = rows_map(&tm_o, o, vh, T, B, kC / 2)) != cudaSuccess) return e;
   if (precision == 1) {
     e = cudaFuncSetAttribute(gdn_chunk_kernel<true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
