@@ -99,9 +99,8 @@ constexpr uint32_t OFF_OT = RC;             // fp32 o tile [64][128]
 constexpr uint32_t OFF_SCR = RC;            // fp32 A [64][64] + T [64][64]
 constexpr uint32_t OFF_TB2 = RC;            // 64 x 64: T diag(beta), over A
 constexpr uint32_t OFF_P = RP;              // 64 x 64
-// Gate vectors in buffers of 512 floats: Gamma +0, gamma +64, w +128,
-// beta +192, ea +384, eb +448; buffer 0's +256 holds gamma of the chunk
-// whose o is pending ([2][64], used when there is one buffer).
+// Gate vectors of chunk c in buffer c & 1, 512 floats: Gamma +0, gamma +64,
+// w +128, beta +192, ea +384, eb +448.
 constexpr uint32_t OFF_VEC = RP + 16384;      // buffer 0
 constexpr uint32_t OFF_BAR = OFF_VEC + 2048;  // 14 mbarriers
 constexpr uint32_t OFF_SLOT = OFF_BAR + 112;  // TMEM address; +120: int flags
@@ -535,16 +534,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const float *__restrict__ beta,
                      const __grid_constant__ CUtensorMap tm_o, int T, int kh,
                      int vh, int rep) {
-  // Where the gate warp makes the next chunk's gate vectors: warp 7, during
-  // the inverse's first step (bf16), or warp 0, after the next chunk's
-  // [K; Q] operand, under the chunk's last products (split-bf16, whose last
-  // products take long enough to hide them; measured faster there).
+  // Where the gate warp makes the next chunk's gate vectors, while the
+  // chunk still reads its own: warp 7 during the inverse's first step
+  // (bf16), or warp 0 while the SIMT warps wait for the correction product
+  // (split-bf16, where that wait is long; measured faster there than
+  // during the inverse or under the chunk's last products).
   constexpr bool kGatesInInverse = !kLo;
   constexpr int kGateWarp = kGatesInInverse ? kSimt / 32 - 1 : 0;
-  // Gate-vector buffer of chunk c: c & 1 when the next chunk's vectors are
-  // made while the chunk still reads its own (during the inverse), else
-  // one buffer, the next chunk's written after the chunk's last read.
-  auto vbuf = [](int c) { return kGatesInInverse ? (c & 1) : 0; };
+  // gate-vector buffer of chunk c
+  auto vbuf = [](int c) { return c & 1; };
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw_s = (uint32_t)__cvta_generic_to_shared(smem_raw);
   const uint32_t sb = (raw_s + 1023u) & ~1023u;
@@ -556,7 +554,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto gvec = [&](int buf) {
     return reinterpret_cast<float *>(gb + (buf ? OFF_VEC1 : OFF_VEC));
   };
-  float *const gam_o = gvec(0) + 256;  // [2][64], single-buffer mode
   volatile int *const fac2 = reinterpret_cast<volatile int *>(gb + OFF_BAR + 120);
   // mbarriers: products done (one commit each), operands ready (kSimt
   // arrivals each), and the final drain
@@ -719,8 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the global stores leave the SIMT warps' path.
     float *otile = reinterpret_cast<float *>(gb + OFF_OT);
     auto emit_o = [&](int cc) {
-      const float *gm = kGatesInInverse ? gvec(cc & 1) + 64  // gamma of chunk cc
-                                        : gam_o + (cc & 1) * 64;
+      const float *gm = gvec(cc & 1) + 64;  // gamma of chunk cc
       const uint32_t pdq = T_BUF;
       for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
         float r[16], pd[16];
@@ -779,10 +775,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       Gam[lane + 32] = sc;
       gam[lane] = expf(sa);
       gam[lane + 32] = expf(sc);
-      if (!kGatesInInverse) {
-        gam_o[(cc & 1) * 64 + lane] = gam[lane];
-        gam_o[(cc & 1) * 64 + lane + 32] = gam[lane + 32];
-      }
       wv[lane] = expf(last - sa);
       wv[lane + 32] = expf(last - sc);
       float gmax = fmaxf(sa, sc), gmin = fminf(sa, sc);
@@ -837,7 +829,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float *Gam = gvec(vbuf(c));
       const float *gam = Gam + 64, *wv = Gam + 128, *bet = Gam + 192;
       const float *ea = Gam + 384, *eb = Gam + 448;
-      if (kGatesInInverse && warp == kGateWarp && c + 1 < nchunks) prefetch(c + 1);
+      if (warp == kGateWarp && c + 1 < nchunks) prefetch(c + 1);  // for gates(c + 1)
       if (c > 0) emit_o(c - 1);  // the previous chunk's output, into the o tile
       simt_sync();  // the o tile is written
       if (c > 0 && tid == 0) store_o(c - 1);
@@ -974,7 +966,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_wait_st();
       signal_ready(rdy_t);  // -> MMA-ud: Delta^T = (V^T - Y diag(gamma)) (T diag(beta))^T
-      if (!kGatesInInverse && warp == kGateWarp && c + 1 < nchunks) prefetch(c + 1);
+      if (!kGatesInInverse && warp == kGateWarp && c + 1 < nchunks) gates(c + 1);
       if (!simt_and(mbar_wait(done_d, parity, kWaitLimit))) { failed = true; break; }
       fence_after_sync();
 
@@ -991,11 +983,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       signal_ready(rdy_d);  // -> MMA-3: (P Delta)^T;  MMA-4: S^T += ...
       if (c + 1 < nchunks) {
         // Under MMA-3 and MMA-4: the next chunk's [K; Q] operand (in the
-        // other region), and, if not made during the inverse, its gates;
-        // then MMA-a of the next chunk is released (it queues behind this
-        // chunk's products).
+        // other region); then MMA-a of the next chunk is released (it queues
+        // behind this chunk's products).
         if (!kq_operand(c + 1)) { failed = true; break; }
-        if (!kGatesInInverse && warp == kGateWarp) gates(c + 1);
         signal_ready(rdy_a);
       }
       if (!simt_and(mbar_wait(done_4, parity, kWaitLimit))) { failed = true; break; }
