@@ -623,7 +623,7 @@ def main():
                      "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved_gbs / hbm_peak,
                      "traffic": traffic, "peak_kind": peak_kind,
-                     "kernel": "gdn_steps_kernel<false, true, 4>"},
+                     "kernel": "gdn_step_c32_kernel"},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,
