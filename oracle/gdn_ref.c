@@ -158,6 +158,22 @@ void gdn_oracle_set_threads(int n) {
  * fp32, separately rounded, left-to-right sums.
  */
 
+/* The gate nonlinearity of the article's gate step: softplus, with the
+ * input itself returned above 20 and e^x returned below -20 (where
+ * log(1 + e^x) equals those to fp32 precision), log1p(e^x) in between. */
+static float gate_softplus(float x) {
+    if (x > 20.0f) return x;
+    if (x < -20.0f) return expf(x);
+    return log1pf(expf(x));
+}
+
+/* The logistic function 1 / (1 + e^-x). */
+static float logistic(float x) {
+    const float e = expf(-x);
+    const float den = 1.0f + e;
+    return 1.0f / den;
+}
+
 /* Advance the whole layer core over T tokens for every sequence.
  *   S      [B][vh][kd][vd]       in/out
  *   hist   [B][ck-1][conv_dim]   in/out (oldest row first)
@@ -166,6 +182,12 @@ void gdn_oracle_set_threads(int n) {
  *   a, b   [B][T][vh];  A_log, dt_bias [vh]
  *   o      [B][T][vh][vd]
  *   ckpt   [T][B][vh][kd][vd] or NULL
+ * The convolution is read as a sliding window: per sequence, the rows
+ * R = [hist rows 0..ck-2, x rows 0..T-1] (ck-1+T rows of conv_dim
+ * channels, oldest first); token t sees rows t .. t+ck-1 of R, and channel
+ * ch of its output is sum_j conv_w[ch][j] * R[t+j][ch] over j = 0..ck-1
+ * (oldest row first, fp32, left to right).  The history after the call is
+ * the last ck-1 rows of R.
  * Returns 0, -1 on a bad shape, -2 when scratch cannot be allocated. */
 int gdn_oracle_layer(int B, int T, int kh, int vh, int kd, int vd, int ck,
                      float eps, float *S, float *hist, const float *x,
@@ -175,80 +197,70 @@ int gdn_oracle_layer(int B, int T, int kh, int vh, int kd, int vd, int ck,
     if (B < 0 || T < 0 || kh <= 0 || vh <= 0 || kd <= 0 || vd <= 0 ||
         ck < 1 || vh % kh)
         return -1;
-    const int conv_dim = 2 * kh * kd + vh * vd;
-    const int nprev = ck - 1;
+    const size_t C = (size_t)(2 * kh * kd + vh * vd); /* conv channels */
+    const size_t nh = (size_t)(ck - 1);               /* history rows   */
     const size_t hsz = (size_t)kd * (size_t)vd;
-    float *xc = (float *)malloc(sizeof(float) * (size_t)conv_dim);
-    float *qn = (float *)malloc(sizeof(float) * (size_t)kh * kd);
-    float *kn = (float *)malloc(sizeof(float) * (size_t)kh * kd);
-    float *gg = (float *)malloc(sizeof(float) * (size_t)vh);
-    float *bb = (float *)malloc(sizeof(float) * (size_t)vh);
-    float *ot = (float *)malloc(sizeof(float) * (size_t)vh * vd);
-    if (!xc || !qn || !kn || !gg || !bb || !ot) {
-        free(xc); free(qn); free(kn); free(gg); free(bb); free(ot);
-        return -2;
-    }
-    int rc = 0;
-    for (int bi = 0; bi < B && rc == 0; bi++) {
-        float *hb = hist + (size_t)bi * (size_t)nprev * (size_t)conv_dim;
+    const size_t qk_len = (size_t)kh * (size_t)kd;
+    float *rows = (float *)malloc(sizeof(float) * (nh + (size_t)T) * C + 1);
+    float *act = (float *)malloc(sizeof(float) * C);   /* conv + SiLU out */
+    float *qu = (float *)malloc(sizeof(float) * qk_len);
+    float *ku = (float *)malloc(sizeof(float) * qk_len);
+    float *gv = (float *)malloc(sizeof(float) * (size_t)vh);
+    float *bv = (float *)malloc(sizeof(float) * (size_t)vh);
+    float *ob = (float *)malloc(sizeof(float) * (size_t)vh * vd);
+    int rc = (rows && act && qu && ku && gv && bv && ob) ? 0 : -2;
+    for (int s = 0; s < B && rc == 0; s++) {
+        float *hs = hist + (size_t)s * nh * C;
+        /* R: the stored rows, then this call's inputs */
+        memcpy(rows, hs, sizeof(float) * nh * C);
+        memcpy(rows + nh * C, x + (size_t)s * (size_t)T * C,
+               sizeof(float) * (size_t)T * C);
         for (int t = 0; t < T && rc == 0; t++) {
-            const float *xr = x + ((size_t)bi * T + t) * (size_t)conv_dim;
-            /* conv + SiLU, history advanced per channel (read, then shift) */
-            for (int ch = 0; ch < conv_dim; ch++) {
-                const float *cw = conv_w + (size_t)ch * (size_t)ck;
-                const float raw = xr[ch];
-                float acc = 0.0f;
-                for (int j = 0; j < nprev; j++) {
-                    const float p = cw[j] * hb[(size_t)j * conv_dim + ch];
-                    acc = acc + p;
+            const float *win = rows + (size_t)t * C;  /* oldest window row */
+            for (size_t ch = 0; ch < C; ch++) {
+                float y = 0.0f;
+                for (int j = 0; j < ck; j++) {
+                    const float p = conv_w[ch * (size_t)ck + (size_t)j] *
+                                    win[(size_t)j * C + ch];
+                    y = y + p;
                 }
-                const float p = cw[nprev] * raw;
-                acc = acc + p;
-                for (int j = 0; j + 1 < nprev; j++)
-                    hb[(size_t)j * conv_dim + ch] = hb[(size_t)(j + 1) * conv_dim + ch];
-                if (nprev > 0) hb[(size_t)(nprev - 1) * conv_dim + ch] = raw;
-                xc[ch] = acc / (1.0f + expf(-acc));
+                act[ch] = y * logistic(y);  /* SiLU */
             }
-            /* q, k normalised per key head */
-            for (int h = 0; h < kh; h++) {
-                const float *qs = xc + (size_t)h * kd;
-                const float *ks = xc + (size_t)kh * kd + (size_t)h * kd;
-                float sq = 0.0f, sk = 0.0f;
+            /* unit L2 norm of every key head's q and k rows */
+            for (size_t r = 0; r < 2 * (size_t)kh; r++) {
+                const float *src = act + r * (size_t)kd;
+                float ss = 0.0f;
                 for (int d = 0; d < kd; d++) {
-                    const float pq = qs[d] * qs[d];
-                    sq = sq + pq;
-                    const float pk = ks[d] * ks[d];
-                    sk = sk + pk;
+                    const float p = src[d] * src[d];
+                    ss = ss + p;
                 }
-                const float nq = sqrtf(sq + eps), nk = sqrtf(sk + eps);
-                for (int d = 0; d < kd; d++) {
-                    qn[(size_t)h * kd + d] = qs[d] / nq;
-                    kn[(size_t)h * kd + d] = ks[d] / nk;
-                }
+                const float nrm = sqrtf(ss + eps);
+                float *dst = r < (size_t)kh ? qu + r * (size_t)kd
+                                            : ku + (r - (size_t)kh) * (size_t)kd;
+                for (int d = 0; d < kd; d++) dst[d] = src[d] / nrm;
             }
-            /* gates */
+            /* decay and write strength of every value head */
+            const size_t row = (size_t)s * (size_t)T + (size_t)t;
             for (int h = 0; h < vh; h++) {
-                const size_t gi = ((size_t)bi * T + t) * vh + h;
-                const float xa = a[gi] + dt_bias[h];
-                float sp;
-                if (xa > 20.0f) sp = xa;
-                else if (xa < -20.0f) sp = expf(xa);
-                else sp = log1pf(expf(xa));
-                gg[h] = -expf(A_log[h]) * sp;
-                bb[h] = 1.0f / (1.0f + expf(-b[gi]));
+                const float sp = gate_softplus(a[row * vh + h] + dt_bias[h]);
+                gv[h] = -expf(A_log[h]) * sp;
+                bv[h] = logistic(b[row * vh + h]);
             }
-            /* the recurrence, one token, this sequence */
-            const float *vs = xc + (size_t)2 * kh * kd;
-            rc = gdn_oracle_run(1, 1, kh, vh, kd, vd, S + (size_t)bi * vh * hsz,
-                                qn, kn, vs, gg, bb, ot, NULL);
-            for (size_t e = 0; e < (size_t)vh * vd; e++)
-                o[((size_t)bi * T + t) * (size_t)vh * vd + e] = ot[e];
+            /* the recurrence, one token, this sequence; v is the last block
+             * of channels */
+            float *Ss = S + (size_t)s * (size_t)vh * hsz;
+            rc = gdn_oracle_run(1, 1, kh, vh, kd, vd, Ss, qu, ku,
+                                act + 2 * qk_len, gv, bv, ob, NULL);
+            memcpy(o + row * (size_t)vh * vd, ob, sizeof(float) * (size_t)vh * vd);
             if (ckpt)
-                memcpy(ckpt + ((size_t)t * B + bi) * vh * hsz,
-                       S + (size_t)bi * vh * hsz, sizeof(float) * vh * hsz);
+                memcpy(ckpt + ((size_t)t * (size_t)B + (size_t)s) * vh * hsz,
+                       Ss, sizeof(float) * (size_t)vh * hsz);
         }
+        /* the history after the call: the last ck-1 rows of R */
+        if (rc == 0)
+            memcpy(hs, rows + (size_t)T * C, sizeof(float) * nh * C);
     }
-    free(xc); free(qn); free(kn); free(gg); free(bb); free(ot);
+    free(rows); free(act); free(qu); free(ku); free(gv); free(bv); free(ob);
     return rc;
 }
 

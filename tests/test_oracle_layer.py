@@ -22,18 +22,20 @@ def test_layer_pin(oracle_mod, pin):
 
 
 LAYER_MUTANTS = {
-    "a_b_swapped": ("const float xa = a[gi] + dt_bias[h];",
-                    "const float xa = b[gi] + dt_bias[h];"),
-    "history_newest_first": ("const float p = cw[j] * hb[(size_t)j * conv_dim + ch];",
-                             "const float p = cw[j] * hb[(size_t)(nprev - 1 - j) * conv_dim + ch];"),
-    "no_history_shift": ("hb[(size_t)j * conv_dim + ch] = hb[(size_t)(j + 1) * conv_dim + ch];",
+    "a_b_swapped": ("gate_softplus(a[row * vh + h] + dt_bias[h])",
+                    "gate_softplus(b[row * vh + h] + dt_bias[h])"),
+    "history_newest_first": ("win[(size_t)j * C + ch];",
+                             "win[(size_t)(ck - 1 - j) * C + ch];"),
+    "no_history_shift": ("memcpy(hs, rows + (size_t)T * C, sizeof(float) * nh * C);",
                          "(void)0;"),
-    "no_silu": ("xc[ch] = acc / (1.0f + expf(-acc));", "xc[ch] = acc;"),
-    "softplus_branch": ("if (xa > 20.0f) sp = xa;", "if (xa > 20.0f) sp = 20.0f;"),
-    "no_norm_eps_sqrt": ("const float nq = sqrtf(sq + eps), nk = sqrtf(sk + eps);",
-                         "const float nq = sq + eps, nk = sqrtf(sk + eps);"),
-    "k_head_offset": ("const float *ks = xc + (size_t)kh * kd + (size_t)h * kd;",
-                      "const float *ks = xc + (size_t)h * kd;"),
+    "no_silu": ("act[ch] = y * logistic(y);  /* SiLU */", "act[ch] = y;"),
+    "softplus_branch": ("if (x > 20.0f) return x;", "if (x > 20.0f) return 20.0f;"),
+    "no_norm_eps_sqrt": ("const float nrm = sqrtf(ss + eps);",
+                         "const float nrm = ss + eps;"),
+    "k_head_offset": ("r < (size_t)kh ? qu + r * (size_t)kd",
+                      "r < (size_t)kh ? ku + r * (size_t)kd"),
+    "window_one_row_late": ("const float *win = rows + (size_t)t * C;",
+                            "const float *win = rows + (size_t)(t + (t > 0)) * C;"),
 }
 
 
