@@ -335,6 +335,36 @@ int check_layer(const gdn_shape *s, int M, int ck, float eps,
   return GDN_OK;
 }
 
+// gdn_layer_step_m's checks of every argument but the workspace, in the
+// order that call makes them: the layer inputs and history, then the
+// state, checkpoints and o (device memory; o may also be mapped host
+// memory), then their overlaps.
+int layer_step_args(const gdn_shape *s, int M, int ck, float eps,
+                    const float *S_in, float *S_out, float *ckpt,
+                    const float *hist_in, float *hist_out, const float *x,
+                    const float *conv_w, const float *a, const float *b,
+                    const float *A_log, const float *dt_bias, float *o) {
+  int r = check_layer(s, M, ck, eps, hist_in, hist_out, x, conv_w, a, b, A_log,
+                      dt_bias);
+  if (r || s->B == 0) return r;
+  const LayerSizes z = layer_sizes(s, M, ck);
+  const size_t sb = state_floats(s) * 4;
+  Buf dev_bufs[] = {{S_in, sb}, {S_out, sb}, {ckpt, sb * (size_t)M}};
+  r = check_bufs(dev_bufs, ckpt ? 3 : 2);
+  if (r) return r;
+  Buf ob{o, z.vb};
+  r = check_io_bufs(&ob, 1);
+  if (r) return r;
+  Buf outs[] = {dev_bufs[0], dev_bufs[1], ob, dev_bufs[2]};
+  const int n = ckpt ? 4 : 3;
+  for (int i = 1; i < n; ++i)
+    for (int j = 0; j < i; ++j) {
+      if (i == 1 && j == 0 && S_out == S_in) continue;
+      if (overlaps(outs[i], outs[j])) return GDN_EALIAS;
+    }
+  return GDN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -487,3 +517,14 @@ const char *gdn_strerror(int status) {
 int gdn_version(void) { return 100; }
 
 }  // extern "C"
+
+namespace gdn {
+int layer_step_check(const gdn_shape *s, int M, int ck, float eps,
+                     const float *S_in, float *S_out, float *ckpt,
+                     const float *hist_in, float *hist_out, const float *x,
+                     const float *conv_w, const float *a, const float *b,
+                     const float *A_log, const float *dt_bias, float *o) {
+  return layer_step_args(s, M, ck, eps, S_in, S_out, ckpt, hist_in, hist_out,
+                         x, conv_w, a, b, A_log, dt_bias, o);
+}
+}  // namespace gdn

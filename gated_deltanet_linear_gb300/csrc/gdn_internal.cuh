@@ -66,3 +66,17 @@ cudaError_t launch_prefill_chunked(float *S, const float *q, const float *k,
 cudaError_t prefill_timeouts(unsigned int *count);
 
 }  // namespace gdn
+
+struct gdn_shape;
+
+namespace gdn {
+
+// The checks gdn_layer_step_m makes of every argument except its workspace
+// (a gdn.h status; GDN_OK also for B == 0).  Defined in gdn_api.cu.
+int layer_step_check(const gdn_shape *s, int M, int ck, float eps,
+                     const float *S_in, float *S_out, float *ckpt,
+                     const float *hist_in, float *hist_out, const float *x,
+                     const float *conv_w, const float *a, const float *b,
+                     const float *A_log, const float *dt_bias, float *o);
+
+}  // namespace gdn

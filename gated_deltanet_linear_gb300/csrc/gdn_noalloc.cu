@@ -16,7 +16,15 @@
 // code its name is only a host-side stand-in for the symbol, never a device
 // address: the address is looked up with cudaGetSymbolAddress, once per
 // device, with that device current, on the first call made on that device.
-// Make that first call before any stream capture starts.
+// Make that first call before any stream capture starts.  The lookup is
+// tied to the device's CUDA context: after cudaDeviceReset the runtime
+// loads the device code again (possibly at another address), and the next
+// call repeats the set-up in the new context instead of using the old
+// address.
+//
+// Status codes.  Every argument is checked as gdn_layer_step_m checks it
+// first; GDN_ESCRATCH is returned only for a request that is otherwise
+// valid and larger than the array.
 //
 // Sharing.  Every call on a device uses the same array and leaves its
 // contents behind.  Nothing in it has to start at zero: the prologue writes
@@ -25,9 +33,12 @@
 // ordering between them) race on the array and give wrong results; order
 // such calls on one stream or with events.
 
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "gdn.h"
+#include "gdn_internal.cuh"
 
 namespace {
 
@@ -36,10 +47,53 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char
     g_noalloc_scratch[GDN_NOALLOC_SCRATCH_BYTES];
 
-std::mutex g_setup_mutex;
-void *g_scratch_of_device[kMaxDevices];  // guarded by g_setup_mutex
+struct Setup {
+  unsigned long long ctx_id;  // context the address belongs to (0: none yet)
+  void *addr;
+};
 
-// Device address of the scratch on the current device (set-up on first use).
+std::mutex g_setup_mutex;
+Setup g_setup[kMaxDevices];  // guarded by g_setup_mutex
+
+// The driver's current-context queries, reached through the runtime (the
+// library does not link the driver library); null if unavailable.
+struct CtxQueries {
+  PFN_cuCtxGetCurrent_v4000 current = nullptr;
+  PFN_cuCtxGetId_v12000 id = nullptr;
+};
+
+const CtxQueries &ctx_queries() {
+  static CtxQueries q;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult r;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000,
+                                         cudaEnableDefault, &r) == cudaSuccess &&
+        r == cudaDriverEntryPointSuccess)
+      q.current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000,
+                                         cudaEnableDefault, &r) == cudaSuccess &&
+        r == cudaDriverEntryPointSuccess)
+      q.id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  return q;
+}
+
+// Unique id of the calling thread's current context, 0 if there is none.
+unsigned long long current_ctx_id() {
+  const CtxQueries &q = ctx_queries();
+  if (!q.current || !q.id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (q.current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  if (q.id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of the scratch on the current device, looked up once per
+// device and context (the set-up).
 int scratch_of_current_device(void **out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -48,15 +102,20 @@ int scratch_of_current_device(void **out) {
   }
   if (dev < 0 || dev >= kMaxDevices) return GDN_ECUDA;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (!g_scratch_of_device[dev]) {
+  Setup &st = g_setup[dev];
+  unsigned long long id = current_ctx_id();
+  if (!st.addr || id == 0 || id != st.ctx_id) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
       cudaGetLastError();
       return GDN_ECUDA;
     }
-    g_scratch_of_device[dev] = p;
+    // the lookup makes the device's context current if it was not yet
+    if (id == 0) id = current_ctx_id();
+    st.addr = p;
+    st.ctx_id = id;  // 0 (queries unavailable): the set-up runs every call
   }
-  *out = g_scratch_of_device[dev];
+  *out = st.addr;
   return GDN_OK;
 }
 
@@ -67,17 +126,16 @@ extern "C" int gdn_layer_step_m_noalloc(
     float *S_out, float *ckpt, const float *hist_in, float *hist_out,
     const float *x, const float *conv_w, const float *a, const float *b,
     const float *A_log, const float *dt_bias, float *o, gdn_stream_t stream) {
-  if (!s) return GDN_EINVAL;
-  // a bad shape or count gets the same status as from gdn_layer_step_m
+  // every argument but the workspace first, with gdn_layer_step_m's status
+  const int r = gdn::layer_step_check(s, M, ck, eps, S_in, S_out, ckpt,
+                                      hist_in, hist_out, x, conv_w, a, b,
+                                      A_log, dt_bias, o);
+  if (r || s->B == 0) return r;
   const size_t need = gdn_layer_workspace(s, M);
-  if (need == 0 || s->B == 0)
-    return gdn_layer_step_m(s, M, ck, eps, S_in, S_out, ckpt, hist_in,
-                            hist_out, x, conv_w, a, b, A_log, dt_bias, o,
-                            nullptr, 0, stream);
   if (need > (size_t)GDN_NOALLOC_SCRATCH_BYTES) return GDN_ESCRATCH;
   void *scratch = nullptr;
-  const int r = scratch_of_current_device(&scratch);
-  if (r) return r;
+  const int rs = scratch_of_current_device(&scratch);
+  if (rs) return rs;
   return gdn_layer_step_m(s, M, ck, eps, S_in, S_out, ckpt, hist_in, hist_out,
                           x, conv_w, a, b, A_log, dt_bias, o, scratch,
                           (size_t)GDN_NOALLOC_SCRATCH_BYTES, stream);

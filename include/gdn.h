@@ -103,6 +103,10 @@ enum {
 
 /*
  * gdn_step - one token for all B * vh heads, state updated in place.
+ * The operation is the delta-recurrence kernel of "24 · GDN linear
+ * attention to GPU", section 4 (figure 1, step 5): decay, read-out S^T k,
+ * delta, rank-1 update and o from the updated state, with its argument set
+ * (S, q, k, v, g, beta, o and the head counts), extended by B sequences.
  *   S     [B][vh][kd][vd]  in/out
  *   q, k  [B][kh][kd]      in
  *   v     [B][vh][vd]      in
@@ -119,7 +123,10 @@ int gdn_step(const gdn_shape *shape, float *S, const float *q, const float *k,
 
 /*
  * gdn_step_m - M tokens in one launch; the state is read once, kept on chip
- * across the M serial updates, and written once.
+ * across the M serial updates, and written once.  "34 · batched M rows",
+ * section 3.6, defines the M tokens of a verify launch as M serial state
+ * updates (no chunked scan); the per-token checkpoints serve the rollback of
+ * its section 3.7 to any accepted count.
  *   S_in   [B][vh][kd][vd]      in  (state before token 0)
  *   S_out  [B][vh][kd][vd]      out (state after token M-1); may equal S_in
  *                               exactly (in place), no other overlap
@@ -139,14 +146,18 @@ int gdn_step_m(const gdn_shape *shape, int M, const float *S_in, float *S_out,
 
 /*
  * gdn_mark - snapshot the state: snap = S (B*vh*kd*vd floats, device to
- * device, on `stream`).  snap must not overlap S.
+ * device, on `stream`).  snap must not overlap S.  The one-shot
+ * device-to-device clone of the recurrent state that "34 · batched M rows",
+ * section 3.7, takes before a speculative launch.
  */
 int gdn_mark(const gdn_shape *shape, const float *S, float *snap,
              gdn_stream_t stream);
 
 /*
  * gdn_rollback - restore the state after m of the M tokens of a gdn_step_m
- * call:  m == 0 copies snap (the state before the call, from gdn_mark or the
+ * call ("34 · batched M rows", section 3.7: roll the state back to the
+ * accepted prefix; the article restores its one snapshot, and the
+ * per-token checkpoints extend that to any m):  m == 0 copies snap (the state before the call, from gdn_mark or the
  * S_in of an out-of-place call) into S;  1 <= m <= M copies ckpt[m-1].
  * snap may be NULL when m > 0; ckpt may be NULL when m == 0.  0 <= m <= M
  * (GDN_ERANGE otherwise).  The copy is bit-exact.  Sources must not overlap
@@ -157,7 +168,8 @@ int gdn_rollback(const gdn_shape *shape, int M, int m, const float *snap,
 
 /*
  * gdn_rollback_seq - per-sequence rollback: sequence b restores the state
- * after m_dev[b] tokens (same rule as gdn_rollback), where m_dev is an int
+ * after m_dev[b] tokens (same rule as gdn_rollback, "34 · batched M rows",
+ * section 3.7, applied to each sequence of a batch), where m_dev is an int
  * array [B] in DEVICE memory, so a count produced on the device needs no
  * host round trip.  A value outside 0..M leaves that sequence's S
  * untouched and sets *err_dev (device int, may be NULL) to 1; the host call
@@ -170,7 +182,11 @@ int gdn_rollback_seq(const gdn_shape *shape, int M, const int *m_dev,
 /*
  * gdn_prefill_workspace - bytes of device workspace gdn_prefill needs for
  * this shape, T, chunk and precision (0 for GDN_PREC_FP32).  Returns 0 and
- * sets nothing on invalid arguments; gdn_prefill validates again.
+ * sets nothing on invalid arguments; gdn_prefill validates again.  The
+ * size-query convention of "24 · GDN linear attention to GPU", section 10
+ * (ask for the size first, then pass a buffer that is large enough; a
+ * buffer that is too small is refused, never truncated into), with the
+ * caller owning the workspace as in "34 · batched M rows", section 3.5.
  */
 size_t gdn_prefill_workspace(const gdn_shape *shape, int T, int chunk,
                              int precision);
@@ -205,7 +221,8 @@ int gdn_prefill(const gdn_shape *shape, int T, float *S, const float *q,
                 void *workspace, size_t ws_bytes, gdn_stream_t stream);
 
 /*
- * gdn_prefill_timeouts - number of chunked-prefill CTAs, since the library
+ * gdn_prefill_timeouts - (an interface addition with no counterpart in the
+ * articles) number of chunked-prefill CTAs, since the library
  * was loaded on the current device, that gave up waiting for a tensor-core
  * operation (each wait is bounded) and left their head's state unwritten.
  * Synchronises the current device.  Expected to stay 0; a non-zero count
@@ -249,12 +266,15 @@ int gdn_layer_prologue_m(const gdn_shape *shape, int M, int ck, float eps,
 /*
  * gdn_layer_workspace - bytes of device workspace gdn_layer_step_m needs to
  * hold the M tokens' q, k, v, g and beta between its two kernels (0 on
- * invalid arguments).
+ * invalid arguments).  Size query as in "24 · GDN linear attention to GPU",
+ * section 10; the caller-owned M-token slab of "34 · batched M rows",
+ * section 3.5.
  */
 size_t gdn_layer_workspace(const gdn_shape *shape, int M);
 
 /*
- * gdn_layer_step_m - gdn_layer_prologue_m followed by gdn_step_m on the same
+ * gdn_layer_step_m - steps 2-5 of figure 1 of "24 · GDN linear attention to
+ * GPU" for M tokens: gdn_layer_prologue_m followed by gdn_step_m on the same
  * stream, with the intermediate q, k, v, g, beta in the caller's workspace
  * (at least gdn_layer_workspace() bytes, 16-byte aligned, device memory;
  * GDN_ERANGE if smaller).  Arguments as in those two calls.  Output m and
@@ -270,7 +290,9 @@ int gdn_layer_step_m(const gdn_shape *shape, int M, int ck, float eps,
 
 /*
  * gdn_layer_hist_rollback - the convolution history after m_dev[b] of the
- * M tokens of a gdn_layer_step_m call, for every sequence b: rows
+ * M tokens of a gdn_layer_step_m call, for every sequence b ("34 · batched
+ * M rows", section 3.7, rolls the convolution history back together with
+ * the recurrent state): rows
  * m .. m+ck-2 of the sequence [hist_snap rows, x rows], where hist_snap is
  * that call's hist_in and x its raw inputs (the history stores inputs, so
  * no per-token copy is needed).  m_dev: device int [B]; a value outside
@@ -321,7 +343,10 @@ int gdn_gated_rmsnorm_m(const gdn_shape *shape, int M, float eps,
  *     token: B * M > 405).
  *   - Set-up: the first call on a device, with that device current, looks
  *     up the array's device address (cudaGetSymbolAddress) and keeps it;
- *     make that first call before any stream capture begins.
+ *     make that first call before any stream capture begins.  The address
+ *     is kept per device and CUDA context: after cudaDeviceReset the next
+ *     call on that device repeats the set-up (make it, too, outside any
+ *     capture).
  *   - Sharing: all calls on a device share the one array, which keeps the
  *     last call's contents.  Nothing in it needs to start at zero (every
  *     byte read is written first in the same call), so nothing is cleared.
@@ -329,7 +354,9 @@ int gdn_gated_rmsnorm_m(const gdn_shape *shape, int M, float eps,
  *     ordering between them) race on the array: order them on one stream or
  *     with events.
  * Other arguments, results and status codes are those of gdn_layer_step_m,
- * and results are bit-identical to it on the same inputs.
+ * and results are bit-identical to it on the same inputs.  Arguments are
+ * checked first, exactly as gdn_layer_step_m checks them, so GDN_ESCRATCH
+ * is returned only for a request that is otherwise valid.
  */
 int gdn_layer_step_m_noalloc(const gdn_shape *shape, int M, int ck, float eps,
                              const float *S_in, float *S_out, float *ckpt,
@@ -339,10 +366,14 @@ int gdn_layer_step_m_noalloc(const gdn_shape *shape, int M, int ck, float eps,
                              const float *A_log, const float *dt_bias,
                              float *o, gdn_stream_t stream);
 
-/* Static description of a status code (never NULL). */
+/* Static description of a status code (never NULL).  The codes are the
+ * refusals of "24 · GDN linear attention to GPU", section 8 (a request the
+ * library cannot serve as asked is refused with an error, never served by a
+ * silent fallback), and of its section 10 (no truncation). */
 const char *gdn_strerror(int status);
 
-/* Library ABI version: major * 10000 + minor * 100 + patch. */
+/* Library ABI version: major * 10000 + minor * 100 + patch (an interface
+ * addition; the articles have no counterpart). */
 int gdn_version(void);
 
 #ifdef __cplusplus
