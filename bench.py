@@ -70,6 +70,22 @@ def decode_bytes(B, kh, vh, M=1, ckpt=False):
     return 2 * state + (M * state if ckpt else 0) + qk + vo + gb
 
 
+# FP32 issue floor of the token-serial update: per head-token and state
+# element, two fused multiply-adds (S^T k and S^T q), one multiply (the
+# decay) and one fused multiply-add (the rank-1 update) -- 4 FP32 lane
+# operations for the 7 flops per element of the definition.  The GB300 has
+# 152 SMs x 128 FP32 lanes; at the measured maximum SM clock that is
+# 152 * 128 * clock lane operations per second.
+FP32_LANE_OPS_PER_ELEM = 4
+SMS = 152
+FP32_LANES_PER_SM = 128
+
+
+def fp32_floor_s(head_tokens, sm_mhz):
+    lane_ops = head_tokens * FP32_LANE_OPS_PER_ELEM * D * D
+    return lane_ops / (SMS * FP32_LANES_PER_SM * sm_mhz * 1e6)
+
+
 # ------------------------------------------------------------- clocks
 
 CLOCK_FIELDS = ("timestamp,uuid,clocks.sm,clocks.max.sm,power.draw,"
@@ -235,6 +251,37 @@ def cpu_baseline(inp, seconds=10.0):
             "gbs": decode_bytes(sub.B, sub.kh, sub.vh) * calls / el / 1e9}
 
 
+def cpu_configs(seconds=2.0):
+    """The oracle on the other decode workloads (one sequence, one token;
+    one sequence, 64 chained tokens; 32 sequences x M tokens), each
+    repeated for about `seconds`: head-steps/s per workload."""
+    import oracle
+    oracle.build()
+
+    def rate(run, head_steps):
+        calls, t0 = 0, time.perf_counter()
+        while True:
+            run()
+            calls += 1
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                return head_steps * calls / el, calls, el
+
+    out = {"cores": oracle.threads(), "kind": "oracle", "unit": UNIT}
+    for name in ("decode_b1", "decode_b1_t64"):
+        w = gdn_inputs.make_workload(name)
+        r, c, el = rate(lambda w=w: oracle.run_inputs(w), w.B * w.vh * w.T)
+        out[name] = {"value": r, "sample": f"{c} calls in {el:.1f} s"}
+    vin = gdn_inputs.make_workload("verify_b32")
+    for M in (2, 4, 8):
+        sub = vin.tokens(0, M)
+        r, c, el = rate(lambda sub=sub: oracle.run_inputs(sub, ckpt=True),
+                        sub.B * sub.vh * M)
+        out[f"verify_b32_m{M}_ckpt"] = {"value": r,
+                                        "sample": f"{c} calls in {el:.1f} s"}
+    return out
+
+
 # ------------------------------------------------------------ reference
 
 def run_reference(args, rank, world):
@@ -283,36 +330,100 @@ def tens_fn(torch, dev):
 
 
 def verify_parts(torch, gdn, tens, stream, hbm_peak, parts, steps,
-                 warmup=5):
-    """The M-token verify launches on 32 sequences x 48 heads, M = 2, 4, 8,
-    without and with per-token checkpoints, in that order; each timed over
-    max(20, min(200, steps)) launches after `warmup` untimed ones."""
+                 warmup=5, sm_mhz=2070.0):
+    """The M-token verify launches, M = 2, 4, 8, without and with per-token
+    checkpoints, on 32 sequences x 48 heads (the verify workload) and on
+    64 sequences x 48 heads (the batched decode size); each timed over
+    max(20, min(200, steps)) launches after `warmup` untimed ones, with
+    three state sets in turn (each larger than L2 at B = 64, 100 MB at
+    B = 32).  Besides the HBM fraction each entry gives the FP32 issue floor
+    and the fraction of max(HBM floor, FP32 floor)."""
     dev = torch.device("cuda", torch.cuda.current_device())
-    vin = gdn_inputs.make_workload("verify_b32")
-    Sv = [tens(vin.S) for _ in range(NSETS)]
-    ck = torch.empty((8,) + tuple(vin.S.shape), device=dev)
-    for M in (2, 4, 8):
-        sub = vin.tokens(0, M)
-        vq, vk, vv, vg, vb = (tens(x) for x in
-                              (sub.q, sub.k, sub.v, sub.g, sub.beta))
-        vo = torch.empty(sub.B, M, sub.vh, D, device=dev)
-        for use_ck in (False, True):
-            def vstep(i, M=M, use_ck=use_ck):
-                s = Sv[i % NSETS]
-                gdn.gdn_step_m(s, s, ck[:M] if use_ck else None, vq, vk,
-                               vv, vg, vb, vo, M=M, stream=stream)
-            n = max(20, min(200, steps))
-            for i in range(warmup):
-                vstep(i)
-            vms = time_launches(torch, vstep, n, stream)
-            nb = decode_bytes(sub.B, sub.kh, sub.vh, M, use_ck)
-            parts[f"verify_b32_m{M}{'_ckpt' if use_ck else ''}"] = {
-                "ms": vms, "head_steps_per_s": sub.B * sub.vh * M / (vms * 1e-3),
-                "gbs": nb / (vms * 1e-3) / 1e9,
-                "frac_of_measured_hbm": nb / (vms * 1e-3) / 1e9 / hbm_peak,
-                "bytes_per_launch": nb}
-    del Sv, ck
-    torch.cuda.empty_cache()
+    for wname in ("verify_b32", "verify_b64"):
+        if wname == "verify_b32":
+            vin = gdn_inputs.make_workload("verify_b32")
+        else:
+            vin = gdn_inputs.make_inputs(gdn_inputs.SEED_BASE + 5, B=64, T=8,
+                                         kh=16, vh=48)
+        Sv = [tens(vin.S) for _ in range(NSETS)]
+        ck = torch.empty((8,) + tuple(vin.S.shape), device=dev)
+        for M in (2, 4, 8):
+            sub = vin.tokens(0, M)
+            toks = [tuple(tens(x) for x in (sub.q, sub.k, sub.v, sub.g,
+                                            sub.beta)) for _ in range(NSETS)]
+            vo = torch.empty(sub.B, M, sub.vh, D, device=dev)
+            for use_ck in (False, True):
+                def vstep(i, M=M, use_ck=use_ck):
+                    s = Sv[i % NSETS]
+                    gdn.gdn_step_m(s, s, ck[:M] if use_ck else None,
+                                   *toks[i % NSETS], vo, M=M, stream=stream)
+                n = max(20, min(200, steps))
+                for i in range(warmup):
+                    vstep(i)
+                vms = time_launches(torch, vstep, n, stream)
+                nb = decode_bytes(sub.B, sub.kh, sub.vh, M, use_ck)
+                ht = sub.B * sub.vh * M
+                hbm_floor = nb / (hbm_peak * 1e9)
+                fp_floor = fp32_floor_s(ht, sm_mhz)
+                parts[f"{wname}_m{M}{'_ckpt' if use_ck else ''}"] = {
+                    "ms": vms, "head_steps_per_s": ht / (vms * 1e-3),
+                    "gbs": nb / (vms * 1e-3) / 1e9,
+                    "frac_of_measured_hbm": nb / (vms * 1e-3) / 1e9 / hbm_peak,
+                    "bytes_per_launch": nb,
+                    "fp32_floor_us": fp_floor * 1e6,
+                    "hbm_floor_us": hbm_floor * 1e6,
+                    "frac_of_max_floor": max(hbm_floor, fp_floor) / (vms * 1e-3)}
+        del Sv, ck
+        torch.cuda.empty_cache()
+
+
+def small_decode_parts(torch, gdn, tens, stream, parts, steps):
+    """Latency of the small decode cases (one sequence x 48 heads, state
+    6.3 MB, L2-resident): one gdn_step per call; 64 chained gdn_step calls
+    with fresh inputs each token; the same 64 tokens as one gdn_step_m
+    launch.  Times are CUDA-event averages over back-to-back launches on one
+    stream (launch gaps included)."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    one = gdn_inputs.make_workload("decode_b1")
+    S1 = tens(one.S)
+    ins = tuple(tens(x) for x in (one.q, one.k, one.v, one.g, one.beta))
+    o1 = torch.empty(1, 1, one.vh, D, device=dev)
+    f = lambda i: gdn.gdn_step(S1, *ins, o1, stream=stream)
+    for i in range(20):
+        f(i)
+    n = max(200, min(2000, steps))
+    ms = time_launches(torch, f, n, stream)
+    parts["decode_b1"] = {
+        "us_per_call": ms * 1e3, "head_steps_per_s": one.vh / (ms * 1e-3),
+        "note": "gdn_step, B=1 x 48 heads, back-to-back launches"}
+
+    ch = gdn_inputs.make_workload("decode_b1_t64")
+    T = ch.T
+    q, k, v, g, beta = (tens(x) for x in (ch.q, ch.k, ch.v, ch.g, ch.beta))
+    per_tok = [tuple(x[:, t:t + 1].contiguous() for x in (q, k, v, g, beta))
+               for t in range(T)]
+    Sc = tens(ch.S)
+    oc = torch.empty(1, 1, ch.vh, D, device=dev)
+    chain = lambda i: gdn.gdn_step(Sc, *per_tok[i % T], oc, stream=stream)
+    for i in range(T):
+        chain(i)
+    ms = time_launches(torch, chain, 10 * T, stream)
+    om = torch.empty(1, T, ch.vh, D, device=dev)
+    Sm = tens(ch.S)
+    multi = lambda i: gdn.gdn_step_m(Sm, Sm, None, q, k, v, g, beta, om,
+                                     M=T, stream=stream)
+    for i in range(5):
+        multi(i)
+    msm = time_launches(torch, multi, 50, stream)
+    parts["decode_b1_t64"] = {
+        "us_per_step_chained": ms * 1e3,
+        "head_steps_per_s_chained": ch.vh / (ms * 1e-3),
+        "us_per_launch_m64": msm * 1e3,
+        "us_per_token_m64": msm * 1e3 / T,
+        "head_steps_per_s_m64": ch.vh * T / (msm * 1e-3),
+        "note": "64 tokens, B=1 x 48 heads: 64 chained gdn_step calls, and "
+                "one gdn_step_m launch over the same 64 tokens"}
+    del S1, Sc, Sm
 
 
 def layer_parts(torch, gdn, tens, stream, hbm_peak, parts, steps,
@@ -428,7 +539,7 @@ def main():
                     help="skip the verify / prefill sub-measurements")
     ap.add_argument("--no-cpu", action="store_true",
                     help="skip the CPU-baseline leg")
-    ap.add_argument("--only", choices=["prefill", "layer", "verify"],
+    ap.add_argument("--only", choices=["prefill", "layer", "verify", "small"],
                     default=None,
                     help="time only the prefill, layer or verify parts (used "
                          "for profiling)")
@@ -459,6 +570,7 @@ def main():
     stream = torch.cuda.current_stream()
     peaks, peak_kind = load_peaks()
     hbm_peak = float(peaks["hbm_gbs"])
+    sm_max = float(peaks.get("sm_max_mhz", 2070.0))
 
     def barrier():
         if dist is not None:
@@ -476,7 +588,10 @@ def main():
             prefill_parts(torch, gdn, tens_fn(torch, dev), stream, peaks, parts)
         elif args.only == "verify":
             verify_parts(torch, gdn, tens_fn(torch, dev), stream, hbm_peak,
-                         parts, args.steps, max(5, args.warmup))
+                         parts, args.steps, max(5, args.warmup), sm_max)
+        elif args.only == "small":
+            small_decode_parts(torch, gdn, tens_fn(torch, dev), stream, parts,
+                               args.steps)
         else:
             layer_parts(torch, gdn, tens_fn(torch, dev), stream, hbm_peak,
                         parts, args.steps, max(5, args.warmup))
@@ -493,11 +608,16 @@ def main():
     S0 = tens(inp.S)
     states = [S0.clone() for _ in range(NSETS)]
     del S0
-    q, k, v, g, beta = (tens(x) for x in (inp.q, inp.k, inp.v, inp.g, inp.beta))
-    o = torch.empty(B, 1, vh, D, device=dev)
+    # token inputs and outputs rotate with the state sets (their own
+    # buffers per set), so no step finds them in L2 from the step before
+    tok_sets = [tuple(tens(x) for x in (inp.q, inp.k, inp.v, inp.g, inp.beta))
+                for _ in range(NSETS)]
+    o_sets = [torch.empty(B, 1, vh, D, device=dev) for _ in range(NSETS)]
+    o = o_sets[0]
 
     def step(i):
-        gdn.gdn_step(states[i % NSETS], q, k, v, g, beta, o, stream=stream)
+        gdn.gdn_step(states[i % NSETS], *tok_sets[i % NSETS], o_sets[i % NSETS],
+                     stream=stream)
 
     sampler = ClockSampler()
     sampler.start()
@@ -582,7 +702,9 @@ def main():
         torch.cuda.empty_cache()
         del states
         torch.cuda.empty_cache()
-        verify_parts(torch, gdn, tens, stream, hbm_peak, parts, args.steps)
+        verify_parts(torch, gdn, tens, stream, hbm_peak, parts, args.steps,
+                     sm_mhz=sm_max)
+        small_decode_parts(torch, gdn, tens, stream, parts, args.steps)
         layer_parts(torch, gdn, tens, stream, hbm_peak, parts, args.steps)
         prefill_parts(torch, gdn, tens, stream, peaks, parts)
 
@@ -602,6 +724,7 @@ def main():
     cpu = None
     if world == 1 and not args.no_cpu:
         cpu = cpu_baseline(inp)
+        cpu["other_workloads"] = cpu_configs()
 
     traffic = kernel_traffic(["gated_deltanet_linear_gb300/csrc/gdn_decode.cu"],
                              "gdn_steps_decode_b64.traffic.txt")

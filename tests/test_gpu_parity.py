@@ -80,6 +80,59 @@ def test_decode_b64_full_size(oracle_mod):
     assert es < TOL_STEP and eo < TOL_STEP
 
 
+def _per_head_o_err(o, o64):
+    """Normwise error of o per (sequence, token, value head) slice of vd
+    elements, max|o - o64| / max|o64| (the survey's per-head reading of the
+    pages' measure), against the fp64 matrix form."""
+    o64 = np.asarray(o64, np.float64)
+    num = np.abs(np.asarray(o, np.float64) - o64).max(axis=-1)
+    return num / np.abs(o64).max(axis=-1)
+
+
+def test_decode_b64_every_element_and_head():
+    """The headline kernel (64 sequences x 48 heads, one token, device
+    inputs) element by element: every o element against the fp64 matrix
+    form within the fp32 rounding bound of its sum (as in
+    test_output_elementwise_rounding_bound, with the normwise slack taken per
+    head), and the normwise error per (sequence, value head) of o and of the
+    state within 1e-5."""
+    from oracle import ref64
+    inp = gdn_inputs.make_workload("decode_b64")
+    S, o = run_step(inp)
+    o_h = host(o).astype(np.float64)            # [B][1][vh][vd]
+    S64, o64, ck64 = ref64.run_matrix(inp.S, inp.q, inp.k, inp.v, inp.g,
+                                      inp.beta, ckpt=True)
+    eh = _per_head_o_err(o_h, o64)
+    es = max_rel(host(S), S64, axes=(-2, -1))
+    rep = inp.vh // inp.kh
+    u = 2.0 ** -24
+    qv = np.abs(inp.q[:, 0].astype(np.float64))            # [B][kh][kd]
+    qrep = np.repeat(qv, rep, axis=1)                      # [B][vh][kd]
+    mag = np.einsum("bvkd,bvk->bvd", np.abs(ck64[0]), qrep)  # sum |S q|
+    scale = np.abs(o64[:, 0]).max(axis=-1, keepdims=True)
+    bound = 1e-5 * scale + 2 * (inp.kd + 8) * u * mag
+    worst = float(np.max(np.abs(o_h[:, 0] - o64[:, 0]) / bound))
+    print(f"decode_b64 per head: o max {eh.max():.3e} (median "
+          f"{np.median(eh):.3e}), state {es:.3e}; elementwise "
+          f"|o - o64| / bound max {worst:.3f}")
+    assert eh.max() < TOL_STEP and es < TOL_STEP
+    assert worst <= 1.0
+
+
+def test_decode_b1_chained_64_per_head():
+    """64 chained single-token launches: o per (token, value head) and the
+    final state per value head against the fp64 matrix form within 1e-4."""
+    from oracle import ref64
+    inp = gdn_inputs.make_workload("decode_b1_t64")
+    S, o, _ = run_single_steps(inp)
+    S64, o64 = ref64.run_matrix(inp.S, inp.q, inp.k, inp.v, inp.g, inp.beta)
+    eh = _per_head_o_err(host(o), o64)
+    es = max_rel(host(S), S64, axes=(-2, -1))
+    print(f"decode_b1_t64 per head: o max {eh.max():.3e} (median "
+          f"{np.median(eh):.3e}), state {es:.3e}")
+    assert eh.max() < TOL_MULTI and es < TOL_MULTI
+
+
 @pytest.mark.parametrize("B,kh,vh,T", [(1, 1, 1, 1), (3, 1, 1, 2),
                                        (2, 4, 4, 3), (1, 1, 3, 5),
                                        (5, 2, 6, 3), (7, 16, 48, 1)])

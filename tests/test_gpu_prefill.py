@@ -86,6 +86,42 @@ def test_chunked_full_size_sampled(oracle_mod, precision):
     assert gdn.gdn_prefill_timeouts() == 0
 
 
+@pytest.mark.parametrize("precision", [gdn.GDN_PREC_BF16X3, gdn.GDN_PREC_BF16],
+                         ids=lambda p: NAME[p])
+def test_chunked_per_head(precision):
+    """o per (sequence, token, value head) against the fp64 matrix form,
+    300 tokens (five chunks, the last ragged), random initial state.  The
+    normwise error of one head's vector can be large where |o| is small by
+    cancellation, so the check is the error relative to the magnitude of
+    the sum that forms it: max|o - o64| / max(sum_dk |S_t[dk][dv] q[dk]|)
+    per head, within the precision's tolerance; the plain per-head
+    normwise error as well (on this seeded case both hold: split-bf16
+    measured 5.9e-6 and 2.6e-5, bf16 3.4e-3 and 1.0e-2 on GB300)."""
+    from oracle import ref64
+    inp = gdn_inputs.make_inputs(6060, B=2, T=300, kh=16, vh=48,
+                                 zero_state=False, g_scale=0.1)
+    S, o = run_prefill(inp, precision)
+    # the fp64 reference on two key-head groups (6 value heads) of both
+    # sequences
+    bs, vis = [0, 1], [0, 1, 2, 45, 46, 47]
+    sub = inp.heads(bs, vis)
+    o_h = host(o)[bs][:, :, vis].astype(np.float64)
+    _, o64, ck64 = ref64.run_matrix(sub.S, sub.q, sub.k, sub.v, sub.g,
+                                    sub.beta, ckpt=True)
+    rep = sub.vh // sub.kh
+    qrep = np.repeat(np.abs(sub.q.astype(np.float64)), rep, axis=2)
+    mag = np.einsum("tbvkd,btvk->btvd", np.abs(ck64), qrep)
+    err = np.abs(o_h - o64).max(axis=-1)
+    rel_mag = err / mag.max(axis=-1)
+    normwise = err / np.abs(o64).max(axis=-1)
+    print(f"{NAME[precision]} per head: error / magnitude max "
+          f"{rel_mag.max():.3e}; normwise max {normwise.max():.3e}, 99.9% "
+          f"{np.quantile(normwise, 0.999):.3e}, median {np.median(normwise):.3e}")
+    assert rel_mag.max() < TOL[precision]
+    assert normwise.max() < TOL[precision]
+    assert gdn.gdn_prefill_timeouts() == 0
+
+
 @pytest.mark.parametrize("kh,vh,B", [(1, 1, 1), (4, 8, 3), (8, 8, 2)])
 def test_chunked_head_layouts(oracle_mod, kh, vh, B):
     """Other key/value head counts: one head in all, two value heads per
