@@ -42,7 +42,7 @@ GDN_NOALLOC_SCRATCH_BYTES = 16 << 20
 # Every symbol include/gdn.h declares.
 EXPORTS = ("gdn_step", "gdn_step_m", "gdn_mark", "gdn_rollback",
            "gdn_rollback_seq", "gdn_prefill_workspace", "gdn_prefill",
-           "gdn_prefill_timeouts", "gdn_layer_prologue_m",
+           "gdn_prefill_timeouts", "gdn_wait_timeouts", "gdn_layer_prologue_m",
            "gdn_layer_workspace", "gdn_layer_step_m",
            "gdn_layer_hist_rollback", "gdn_gated_rmsnorm_m",
            "gdn_layer_step_m_noalloc", "gdn_strerror", "gdn_version")
@@ -108,6 +108,8 @@ def load():
     lib.gdn_layer_hist_rollback.restype = ctypes.c_int
     lib.gdn_prefill_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint)]
     lib.gdn_prefill_timeouts.restype = ctypes.c_int
+    lib.gdn_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+    lib.gdn_wait_timeouts.restype = ctypes.c_int
     lib.gdn_strerror.argtypes = [ctypes.c_int]
     lib.gdn_strerror.restype = ctypes.c_char_p
     lib.gdn_version.restype = ctypes.c_int
@@ -251,6 +253,14 @@ def gdn_prefill_timeouts():
     c = ctypes.c_uint(0)
     _check(load().gdn_prefill_timeouts(ctypes.byref(c)), "gdn_prefill_timeouts")
     return int(c.value)
+
+
+def gdn_wait_timeouts():
+    """Bounded waits that ran out in any kernel since the library was loaded
+    on the current device (synchronises the device)."""
+    n = ctypes.c_uint(0)
+    _check(load().gdn_wait_timeouts(ctypes.byref(n)), "gdn_wait_timeouts")
+    return int(n.value)
 
 
 def gdn_prefill(S, q, k, v, g, beta, o, precision=GDN_PREC_FP32, chunk=64,

@@ -289,6 +289,18 @@ int gdn_prefill_timeouts(unsigned int *count) {
   return status_of(gdn::prefill_timeouts(count));
 }
 
+int gdn_wait_timeouts(unsigned int *count) {
+  if (!count) return GDN_EINVAL;
+  cudaGetLastError();
+  unsigned int a = 0, b = 0;
+  const int r = status_of(gdn::prefill_timeouts(&a));
+  if (r) return r;
+  const int r2 = status_of(gdn::steps_timeouts(&b));
+  if (r2) return r2;
+  *count = a + b;
+  return GDN_OK;
+}
+
 }  // extern "C"
 
 namespace {

@@ -43,22 +43,34 @@
 // once.  The kernel also lets its own dependents launch early; they wait
 // for its completion in the same way before reading its outputs.
 //
-// Single-token launches with device-resident inputs use a second layout
-// (gdn_step_c32_kernel): a CTA of 4 warps takes a 32-column group of a head,
-// warp w key rows 32w .. 32w+31 of all 32 columns, so every warp request
-// covers whole 128-byte row segments; the reductions over the key rows
-// finish across the 4 warps through shared memory, one barrier per unit.
-// On the 64 x 48-head step it measured 65.1 us against 69.7 us.
+// Three layouts share that arithmetic:
+//   - gdn_step_c32_kernel: single-token launches with device-resident
+//     inputs.  A CTA of 4 warps takes a 32-column group of a head, warp w
+//     key rows 32w .. 32w+31 of all 32 columns, so every warp request covers
+//     whole 128-byte row segments; the reductions over the key rows finish
+//     across the 4 warps through shared memory, one barrier per unit.  On
+//     the 64 x 48-head step it measured 65.1 us against 69.7 us for the
+//     8-column layout.
+//   - gdn_steps_head_kernel: several tokens, or checkpoints, with
+//     device-resident inputs.  One CTA of 8 warps per head, 16 columns per
+//     warp, two 8-row blocks per lane; the token inputs stream through a
+//     shared-memory ring filled by bulk copies (see its comment).  On
+//     64 x 48 heads it measured 73 / 79 / 121 us for M = 2 / 4 / 8 without
+//     checkpoints, against 82 / 109 / 170 us for the 8-column layout.
+//   - gdn_steps_kernel (the 8-column layout above): launches whose token
+//     inputs are in host memory, whose warps then share the q and k rows
+//     of a head in L1.
 //
 // Determinism.  Every product and sum is an explicit round-to-nearest
 // intrinsic and the reduction tree is fixed, so a token gives the same bits
-// whether it is the only token of a launch or one of M, and in either
-// layout: gdn_step_m(M) is bit-identical to M gdn_step calls.  The tree over
+// whether it is the only token of a launch or one of M, and in any of the
+// layouts: gdn_step_m(M) is bit-identical to M gdn_step calls.  The tree over
 // the 16 blocks of 8 key rows (block p = rows 8p .. 8p+7, each summed in row
 // order): W_w = (B_4w + B_4w+2) + (B_4w+1 + B_4w+3) for w = 0..3, then
 // (W_0 + W_2) + (W_1 + W_3); q . k the same way.
 
 #include "gdn_internal.cuh"
+#include "gdn_tc.cuh"
 
 namespace gdn {
 namespace {
@@ -637,6 +649,401 @@ __global__ void __launch_bounds__(kC32Warps * 32, kWarpsPerSm / kC32Warps)
   cp_async_wait<0>();
 }
 
+// Multi-token update (M > 1, or checkpoints) with device-resident token
+// inputs: one CTA of 8 warps per head, warp c on the head's 16-column group
+// c.  Lane = 4 rg + cq holds columns 16 c + 4 cq .. +3 of the two 8-row
+// blocks that the first level of the reduction tree adds: rg = 2 w + j,
+// blocks pA = 4 w + j and pB = pA + 2 (rows 8 pA .. +7 and 8 pB .. +7).  So
+// the lane's own partials already form B_pA + B_pB (tree level 1), and the
+// remaining levels are lane xor 4 (j: W_w), xor 16 (w bit 1: W_0 + W_2,
+// W_1 + W_3) and xor 8 (w bit 0): the tree of the file header term for
+// term, so a token gives the same bits here as in the single-token kernels.
+// After the reduce-scatter, lane (w, j, cq) holds S^T k (j = 0) or S^T q
+// (j = 1) of column 4 cq + w; the j = 0 lanes form tmp, four shuffles give
+// every lane its columns' tmp, and the j = 1 lanes write o.  The state
+// arithmetic runs as packed pairs (__ffma2_rn / __fmul2_rn: per component
+// the rounding of __fmaf_rn / __fmul_rn).
+//
+// Token inputs.  The head's q, k and v rows of a token (512 bytes each) are
+// shared by the CTA's 8 warps through a ring of kHSlots slots in shared
+// memory, filled by bulk copies (cp.async.bulk, completion on one mbarrier
+// per slot) kHSlots - 1 tokens ahead: the warp that releases a slot last
+// (a shared counter) refills it with the token kHSlots further on, so no
+// warp waits for another except through the ring itself.  g and beta come
+// 32 tokens at a time, one token per lane (loaded a chunk ahead), alpha =
+// exp(g) computed once per token, and reach every lane by shuffles.  With
+// q, k and v read from shared memory as they are used, no token input is
+// held in registers across a token.
+//
+// State.  Each warp copies its next unit's 8 KB with cp.async into a private
+// stage as soon as it has read the current one into registers, so one unit
+// is in flight while one computes; a lane reads back only what it copied.
+// The stage layout [register r][lane] makes every 128-bit shared access of a
+// quarter warp one contiguous 128-byte line; the q and k reads of a quarter
+// warp touch two addresses (broadcast), so no access has bank conflicts.
+//
+// Waits on the ring are bounded: a wait that runs out counts a time-out
+// (gdn_wait_timeouts), marks every result the CTA had not yet written as NaN
+// (state and o of the remaining units), and the CTA waits, bounded again,
+// for its copies in flight before it exits.
+constexpr int kHWarps = 8;
+constexpr int kHCtasPerSm = 2;
+constexpr int kHSlots = 6;
+constexpr int kHStage = 16 * kDim * 4;                   // one warp's 8 KB
+constexpr int kHSlotBytes = 3 * kDim * 4;                // k | q | v rows
+constexpr int kHOffSlots = kHWarps * kHStage;
+constexpr int kHOffBar = kHOffSlots + kHSlots * kHSlotBytes;
+constexpr int kHOffCnt = kHOffBar + kHSlots * 8;
+constexpr int kHOffLast = kHOffCnt + kHSlots * 4;
+constexpr int kHOffFail = kHOffLast + kHSlots * 4;
+constexpr int kHSmem = kHOffFail + 16;
+constexpr uint32_t kHWaitLimit = 1u << 24;
+
+__device__ unsigned int g_steps_timeouts = 0;
+
+__device__ __forceinline__ float4 f4_of(float2 lo, float2 hi) {
+  return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+
+// sum over the 8 rows of a block (row order) of s[row] * x[row]: the first
+// product rounded, then fused multiply-adds -- partial_dot's arithmetic.
+__device__ __forceinline__ float4 block_dot(const float4 *s, const float4 &x0,
+                                            const float4 &x1) {
+  float2 lo = __fmul2_rn(make_float2(s[0].x, s[0].y), make_float2(x0.x, x0.x));
+  float2 hi = __fmul2_rn(make_float2(s[0].z, s[0].w), make_float2(x0.x, x0.x));
+#pragma unroll
+  for (int r = 1; r < 8; ++r) {
+    const float xr = comp(r < 4 ? x0 : x1, r & 3);
+    const float2 xx = make_float2(xr, xr);
+    lo = __ffma2_rn(make_float2(s[r].x, s[r].y), xx, lo);
+    hi = __ffma2_rn(make_float2(s[r].z, s[r].w), xx, hi);
+  }
+  return f4_of(lo, hi);
+}
+
+__device__ __forceinline__ float block_qk(const float4 &q0, const float4 &q1,
+                                          const float4 &k0, const float4 &k1) {
+  float a = __fmul_rn(q0.x, k0.x);
+  a = __fmaf_rn(q0.y, k0.y, a);
+  a = __fmaf_rn(q0.z, k0.z, a);
+  a = __fmaf_rn(q0.w, k0.w, a);
+  a = __fmaf_rn(q1.x, k1.x, a);
+  a = __fmaf_rn(q1.y, k1.y, a);
+  a = __fmaf_rn(q1.z, k1.z, a);
+  a = __fmaf_rn(q1.w, k1.w, a);
+  return a;
+}
+
+__device__ __forceinline__ float4 add4(const float4 &a, const float4 &b) {
+  return f4_of(__fadd2_rn(make_float2(a.x, a.y), make_float2(b.x, b.y)),
+               __fadd2_rn(make_float2(a.z, a.w), make_float2(b.z, b.w)));
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t smem, const float *src,
+                                          uint32_t bytes, uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1], %2, [%3];" ::"r"(smem),
+      "l"(src), "r"(bytes), "r"(mbar)
+      : "memory");
+}
+
+__device__ __forceinline__ void arrive_expect_tx(uint32_t mbar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ float lds32(uint32_t smem) {
+  float r;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(r) : "r"(smem));
+  return r;
+}
+
+template <bool kCkpt>
+__global__ void __launch_bounds__(kHWarps * 32, kHCtasPerSm)
+    gdn_steps_head_kernel(const float *S_in, float *S_out,
+                          float *__restrict__ ckpt, const float *__restrict__ q,
+                          const float *__restrict__ k,
+                          const float *__restrict__ v,
+                          const float *__restrict__ g,
+                          const float *__restrict__ beta,
+                          float *__restrict__ o, int vh, int kh, int rep, int M,
+                          unsigned nheads) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rg = lane >> 2, cq = lane & 3;
+  const int j = rg & 1, w = rg >> 1;
+  const int rowA = 8 * (4 * w + j);             // block pA; pB = rows + 16
+  const int col = 16 * warp + 4 * cq;           // the lane's first column
+  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem_raw);
+  const uint32_t stage = sbase + (uint32_t)(warp * kHStage + lane * 16);
+  const uint32_t slots = sbase + kHOffSlots;
+  const uint32_t bars = sbase + kHOffBar;
+  unsigned int *cnt = reinterpret_cast<unsigned int *>(smem_raw + kHOffCnt);
+  int *last = reinterpret_cast<int *>(smem_raw + kHOffLast);
+  int *failed = reinterpret_cast<int *>(smem_raw + kHOffFail);
+  const unsigned mine =
+      blockIdx.x < nheads ? (nheads - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  const size_t hstride = (size_t)vh * kDim;     // o / v stride per token
+  const size_t ckstride = (size_t)nheads * (kDim * kDim);
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  auto head_of = [&](unsigned i) { return blockIdx.x + i * gridDim.x; };
+  // offset of this lane's first state element (row rowA, column col) in
+  // unit i's head; its 16 rows are at + r * kDim (r < 8) and + (r + 8) * kDim
+  auto s_off = [&](unsigned i) {
+    return (size_t)head_of(i) * (kDim * kDim) + (size_t)(rowA * kDim + col);
+  };
+  auto issue_state = [&](unsigned i) {
+    const float *src = S_in + s_off(i);
+#pragma unroll
+    for (int r = 0; r < 16; ++r)
+      cp_async16(stage + r * 512, src + (r < 8 ? r : r + 8) * kDim);
+  };
+  if (mine > 0) issue_state(0);
+  cp_async_commit();
+
+  if (threadIdx.x == 0) {
+    for (int sl = 0; sl < kHSlots; ++sl) {
+      tc::mbar_init(bars + 8 * sl, 1);
+      cnt[sl] = 0;
+      last[sl] = -1;
+    }
+    *failed = 0;
+  }
+  __syncthreads();
+
+  // the k, q and v rows of token m of unit i into slot sl, whose use-th
+  // filling this is (one thread at a time)
+  auto issue_item = [&](unsigned i, int m, int sl, int use) {
+    const unsigned head = head_of(i);
+    const unsigned b = head / (unsigned)vh;
+    const unsigned vi = head - b * (unsigned)vh;
+    const unsigned hh = vi / (unsigned)rep;
+    const size_t bm = (size_t)b * (size_t)M + (size_t)m;
+    const uint32_t dst = slots + (uint32_t)(sl * kHSlotBytes);
+    const uint32_t bar = bars + 8 * sl;
+    last[sl] = use;
+    tc::fence_proxy_async();
+    arrive_expect_tx(bar, kHSlotBytes);
+    bulk_load(dst, k + (bm * kh + hh) * kDim, kDim * 4, bar);
+    bulk_load(dst + kDim * 4, q + (bm * kh + hh) * kDim, kDim * 4, bar);
+    bulk_load(dst + 2 * kDim * 4, v + (bm * vh + vi) * kDim, kDim * 4, bar);
+  };
+  // (unit, token) kHSlots items after (i, m)
+  auto ahead = [&](unsigned &i2, int &m2) {
+    m2 += kHSlots;
+    while (m2 >= M) {
+      m2 -= M;
+      ++i2;
+    }
+  };
+
+  // the token inputs may come from the kernel this one overlaps with
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) {
+    unsigned i2 = 0;
+    int m2 = 0;
+    for (int sl = 0; sl < kHSlots && i2 < mine; ++sl) {
+      issue_item(i2, m2, sl, 0);
+      if (++m2 == M) {
+        m2 = 0;
+        ++i2;
+      }
+    }
+  }
+
+  // g and beta of the 32 tokens m0 .. m0 + 31 of unit i, one per lane
+  auto gb_load = [&](unsigned i, int m0, float &gv, float &bv) {
+    gv = 0.0f;
+    bv = 0.0f;
+    const int m = m0 + lane;
+    if (i < mine && m < M) {
+      const unsigned head = head_of(i);
+      const unsigned b = head / (unsigned)vh;
+      const size_t gi = ((size_t)b * (size_t)M + (size_t)m) * (size_t)vh + (head - b * (unsigned)vh);
+      gv = __ldg(g + gi);
+      bv = __ldg(beta + gi);
+    }
+  };
+  float g_nx, b_nx, a_ch = 0.0f, b_ch = 0.0f;
+  gb_load(0, 0, g_nx, b_nx);
+
+  // j = 1 lanes take q as their first operand and k as their second, so the
+  // first reduction level keeps its first vector on every lane
+  const uint32_t x1off = (uint32_t)(rowA * 4 + (j ? kDim * 4 : 0));
+  const uint32_t x2off = (uint32_t)(rowA * 4 + (j ? 0 : kDim * 4));
+  const uint32_t koff = (uint32_t)(rowA * 4);
+  const uint32_t voff = (uint32_t)(2 * kDim * 4 + (col + w) * 4);
+
+  float4 s[16];
+  bool ok = true;
+  unsigned i = 0;
+  int m = 0, sl = 0, use = 0;
+  for (; i < mine; ++i) {
+    cp_async_wait<0>();  // unit i has landed (this lane's bytes)
+#pragma unroll
+    for (int r = 0; r < 16; ++r) s[r] = lds128(stage + r * 512);
+    if (i + 1 < mine) issue_state(i + 1);  // after this lane's own reads
+    cp_async_commit();
+    const size_t soff = s_off(i);
+    float *op;
+    {
+      const unsigned head = head_of(i);
+      const unsigned b = head / (unsigned)vh;
+      op = o + ((size_t)b * (size_t)M * vh + (head - b * (unsigned)vh)) * kDim + col + w;
+    }
+    float *cp = kCkpt ? ckpt + soff : nullptr;
+
+    for (m = 0; m < M; ++m) {
+      if ((m & 31) == 0) {  // the next 32 tokens' gates, and the chunk after
+        a_ch = expf(g_nx);
+        b_ch = b_nx;
+        if (m + 32 < M) gb_load(i, m + 32, g_nx, b_nx);
+        else gb_load(i + 1, 0, g_nx, b_nx);
+      }
+      const float alpha = __shfl_sync(kFull, a_ch, m & 31);
+      const float bt = __shfl_sync(kFull, b_ch, m & 31);
+      const uint32_t slot = slots + (uint32_t)(sl * kHSlotBytes);
+      if (!__all_sync(kFull, tc::mbar_wait(bars + 8 * sl, (uint32_t)(use & 1),
+                                           kHWaitLimit))) {
+        ok = false;
+        break;
+      }
+
+      // partials of blocks A and B, then tree level 1 (B_pA + B_pB); x1 is
+      // k on j = 0 lanes and q on j = 1 lanes
+      float4 d1, d2;
+      float qk;
+      {
+        const float4 a0 = lds128(slot + x1off), a1 = lds128(slot + x1off + 16);
+        const float4 b0 = lds128(slot + x2off), b1 = lds128(slot + x2off + 16);
+        d1 = block_dot(s, a0, a1);
+        d2 = block_dot(s, b0, b1);
+        qk = block_qk(a0, a1, b0, b1);
+      }
+      {
+        const float4 a0 = lds128(slot + x1off + 64), a1 = lds128(slot + x1off + 80);
+        const float4 b0 = lds128(slot + x2off + 64), b1 = lds128(slot + x2off + 80);
+        d1 = add4(d1, block_dot(s + 8, a0, a1));
+        d2 = add4(d2, block_dot(s + 8, b0, b1));
+        qk = __fadd_rn(qk, block_qk(a0, a1, b0, b1));
+      }
+      // level 2 (lane xor 4): j = 0 keeps S^T k, j = 1 keeps S^T q
+      float r4[4];
+      r4[0] = __fadd_rn(d1.x, __shfl_xor_sync(kFull, d2.x, 4));
+      r4[1] = __fadd_rn(d1.y, __shfl_xor_sync(kFull, d2.y, 4));
+      r4[2] = __fadd_rn(d1.z, __shfl_xor_sync(kFull, d2.z, 4));
+      r4[3] = __fadd_rn(d1.w, __shfl_xor_sync(kFull, d2.w, 4));
+      // level 3 (lane xor 16): w bit 1 keeps columns (2, 3), else (0, 1)
+      const bool w1 = w & 2, w0 = w & 1;
+      float r2[2];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const float keep = w1 ? r4[c + 2] : r4[c];
+        const float send = w1 ? r4[c] : r4[c + 2];
+        r2[c] = __fadd_rn(keep, __shfl_xor_sync(kFull, send, 16));
+      }
+      // level 4 (lane xor 8): w bit 0 keeps the odd column of the pair
+      const float red = __fadd_rn(w0 ? r2[1] : r2[0],
+                                  __shfl_xor_sync(kFull, w0 ? r2[0] : r2[1], 8));
+      qk = __fadd_rn(qk, __shfl_xor_sync(kFull, qk, 4));
+      qk = __fadd_rn(qk, __shfl_xor_sync(kFull, qk, 16));
+      qk = __fadd_rn(qk, __shfl_xor_sync(kFull, qk, 8));
+
+      // tmp of column col + w on the j = 0 lanes; every lane gets its four
+      // columns' tmp from lanes 8 c + cq
+      const float vv = lds32(slot + voff);
+      const float tmp_mine = __fmul_rn(__fsub_rn(vv, __fmul_rn(alpha, red)), bt);
+      float tmp[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmp[c] = __shfl_sync(kFull, tmp_mine, 8 * c + cq);
+      const float tmp_pair = __shfl_xor_sync(kFull, tmp_mine, 4);
+      if (j)  // o = alpha (S^T q) + (q . k) tmp
+        *op = __fmaf_rn(qk, tmp_pair, __fmul_rn(alpha, red));
+      op += hstride;
+
+      // S = alpha S + k tmp^T
+      {
+        const float2 al = make_float2(alpha, alpha);
+        const float2 t01 = make_float2(tmp[0], tmp[1]), t23 = make_float2(tmp[2], tmp[3]);
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const float4 kk4 = lds128(slot + koff + (h < 2 ? 16 * h : 64 + 16 * (h - 2)));
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int r = 4 * h + e;
+            const float kr = comp(kk4, e);
+            const float2 kk = make_float2(kr, kr);
+            s[r] = f4_of(__ffma2_rn(kk, t01, __fmul2_rn(al, make_float2(s[r].x, s[r].y))),
+                         __ffma2_rn(kk, t23, __fmul2_rn(al, make_float2(s[r].z, s[r].w))));
+          }
+        }
+      }
+      // release the slot; the warp that releases it last refills it
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence_block();
+        const unsigned old = atomicAdd(&cnt[sl], 1u);
+        if ((old & (kHWarps - 1)) == kHWarps - 1) {
+          unsigned i2 = i;
+          int m2 = m;
+          ahead(i2, m2);
+          if (i2 < mine) {
+            __threadfence_block();
+            issue_item(i2, m2, sl, use + 1);
+          }
+        }
+      }
+      if (kCkpt) {
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+          st_stream<false>(cp + (r < 8 ? r : r + 8) * kDim, s[r], 0);
+        cp += ckstride;
+      }
+      if (++sl == kHSlots) {
+        sl = 0;
+        ++use;
+      }
+    }
+    if (!ok) break;
+    float *dst = S_out + soff;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) st_stream<false>(dst + (r < 8 ? r : r + 8) * kDim, s[r], 0);
+  }
+
+  if (!ok) {
+    // a wait ran out: every result of this warp not yet written becomes NaN
+    // (the state and checkpoints of unit i on, o of token m of unit i on)
+    if (lane == 0 && atomicExch(failed, 1) == 0) atomicAdd(&g_steps_timeouts, 1u);
+    const float nan = __int_as_float(0x7fffffff);
+    const float4 nan4 = make_float4(nan, nan, nan, nan);
+    for (unsigned ii = i; ii < mine; ++ii) {
+      const size_t soff = s_off(ii);
+      const unsigned head = head_of(ii);
+      const unsigned b = head / (unsigned)vh;
+      float *op = o + ((size_t)b * (size_t)M * vh + (head - b * (unsigned)vh)) * kDim + col + w;
+      for (int r = 0; r < 16; ++r) st_stream<false>(S_out + soff + (r < 8 ? r : r + 8) * kDim, nan4, 0);
+      for (int mm = ii == i ? m : 0; mm < M; ++mm) {
+        if (j) op[(size_t)mm * hstride] = nan;
+        if (kCkpt)
+          for (int r = 0; r < 16; ++r)
+            st_stream<false>(ckpt + (size_t)mm * ckstride + soff + (r < 8 ? r : r + 8) * kDim,
+                             nan4, 0);
+      }
+    }
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+  // copies still in flight into the ring (only after a time-out): wait for
+  // them, bounded, before the CTA's shared memory is released
+  if (threadIdx.x == 0 && *failed)
+    for (int q_ = 0; q_ < kHSlots; ++q_)
+      if (last[q_] >= 0)
+        tc::mbar_wait(bars + 8 * q_, (uint32_t)(last[q_] & 1), kHWaitLimit);
+}
+
 // One tile of kCopyUnroll x blockDim 16-byte elements per CTA, as many CTAs
 // as tiles: a thread has its kCopyUnroll loads in flight before it stores,
 // and the hardware hands tiles to SMs as they free up.  For the 201 MB state
@@ -734,6 +1141,25 @@ cudaError_t launch_steps(const float *S_in, float *S_out, float *ckpt,
                                    overlap, S_in, S_out, q, k, v, g, beta, o,
                                    vh, kh, vh / kh, nheads);
   }
+  if (!host_inputs) {
+    // several tokens or checkpoints, device-resident inputs: one CTA per
+    // head (head indices in 32 bits)
+    if (nheads > 0xffffffffull) return cudaErrorInvalidConfiguration;
+    size_t ctas = (size_t)sm_count() * kHCtasPerSm;
+    if (ctas > nheads) ctas = nheads;
+    auto goh = [&](auto kernel) {
+      cudaError_t e = cudaFuncSetAttribute(
+          kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kHSmem);
+      if (e != cudaSuccess) return e;
+      return launch_maybe_overlapped(kernel, dim3((unsigned)ctas),
+                                     dim3(kHWarps * 32), kHSmem, stream,
+                                     overlap, S_in, S_out, ckpt, q, k, v, g,
+                                     beta, o, vh, kh, vh / kh, M,
+                                     (unsigned)nheads);
+    };
+    return ckpt ? goh(gdn_steps_head_kernel<true>)
+                : goh(gdn_steps_head_kernel<false>);
+  }
   const int wpc = M == 1 && host_inputs ? 8 : 4;
   const int smem = wpc == 8 ? smem_per_cta<8>() : smem_per_cta<4>();
   size_t ctas = (nunits + wpc - 1) / wpc;
@@ -758,6 +1184,10 @@ cudaError_t launch_steps(const float *S_in, float *S_out, float *ckpt,
         : wpc == 8 ? go(gdn_steps_kernel<false, true, 8>, (float *)nullptr)
                    : go(gdn_steps_kernel<false, true, 4>, (float *)nullptr);
   return e;
+}
+
+cudaError_t steps_timeouts(unsigned int *count) {
+  return cudaMemcpyFromSymbol(count, g_steps_timeouts, sizeof(unsigned int));
 }
 
 cudaError_t launch_copy(float *dst, const float *src, size_t n,

@@ -64,6 +64,8 @@ cudaError_t launch_prefill_chunked(float *S, const float *q, const float *k,
                                    int vh, int T, int precision,
                                    void *workspace, cudaStream_t stream);
 cudaError_t prefill_timeouts(unsigned int *count);
+// Ring waits of the multi-token kernel that ran out (gdn_decode.cu).
+cudaError_t steps_timeouts(unsigned int *count);
 
 }  // namespace gdn
 

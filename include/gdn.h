@@ -231,6 +231,19 @@ int gdn_prefill(const gdn_shape *shape, int T, float *S, const float *q,
 int gdn_prefill_timeouts(unsigned int *count);
 
 /*
+ * gdn_wait_timeouts - (an interface addition with no counterpart in the
+ * articles) number of bounded waits, since the library was loaded on the
+ * current device, that ran out in any kernel: the chunked prefill's
+ * tensor-core waits (as gdn_prefill_timeouts) and the multi-token update's
+ * waits for its token inputs (gdn_step_m with M > 1 or checkpoints, the
+ * fp32 prefill, the layer step; device-resident inputs).  A CTA whose wait
+ * runs out writes NaN into every state, checkpoint and o element it had not
+ * yet produced, so the failure also shows in the results themselves.
+ * Synchronises the current device.  Expected to stay 0.
+ */
+int gdn_wait_timeouts(unsigned int *count);
+
+/*
  * gdn_layer_prologue_m - the per-token layer core that produces the inputs
  * of the update from raw projections, for M tokens: a depthwise causal
  * convolution of width ck over the raw mixed q|k|v projection with a

@@ -220,6 +220,32 @@ def test_verify_m_bit_exact_vs_single_steps(oracle_mod, M):
     assert es < TOL_MULTI and eo < TOL_MULTI and ec < TOL_MULTI
 
 
+@pytest.mark.parametrize("M", [2, 4, 8])
+def test_verify_b64_bit_exact(oracle_mod, M):
+    """64 sequences x 48 heads (the batched decode size), M tokens in one
+    launch, with checkpoints and without (in place): o, every checkpoint and
+    the final state bit-identical to M single-token launches; the oracle
+    recomputes sequences 0, 31 and 63 within 1e-4."""
+    inp = gdn_inputs.make_inputs(gdn_inputs.SEED_BASE + 5, B=64, T=8, kh=16,
+                                 vh=48).tokens(0, M)
+    S_in, S_out, ck, o = run_step_m(inp)
+    S_ss, o_ss, states = run_single_steps(inp)
+    assert torch.equal(o, o_ss)
+    assert torch.equal(S_out, S_ss)
+    for m in range(M):
+        assert torch.equal(ck[m], states[m]), m
+    del ck, states
+    _, S_ip, _, o_ip = run_step_m(inp, ckpt=False, inplace=True)
+    assert torch.equal(S_ip, S_ss) and torch.equal(o_ip, o_ss)
+    bs = [0, 31, 63]
+    S_ref, o_ref = oracle_mod.run_inputs(inp.heads(bs, range(inp.vh)))
+    es = err_state(host(S_out)[bs], S_ref)
+    eo = err_out(host(o)[bs], o_ref)
+    print(f"verify_b64 M={M} (sequences 0, 31, 63): state {es:.3e} o {eo:.3e}")
+    assert es < TOL_MULTI and eo < TOL_MULTI
+    assert gdn.gdn_wait_timeouts() == 0
+
+
 def test_verify_variants_identical():
     """In place vs out of place, with vs without checkpoints: same bits."""
     inp = gdn_inputs.make_workload("verify_b32").tokens(0, 4).heads(
@@ -374,6 +400,7 @@ def test_prefill_fp32_full_size_sampled(oracle_mod):
     print(f"prefill fp32 B=8 T=4096 (sampled heads): state {es:.3e} o {eo:.3e}")
     assert es < TOL_MULTI and eo < TOL_MULTI
     assert torch.isfinite(o).all() and torch.isfinite(S).all()
+    assert gdn.gdn_wait_timeouts() == 0
 
 
 # ------------------------------------------------ refusals with real memory
