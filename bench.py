@@ -14,8 +14,9 @@ Prints one JSON line (rank 0).  --impl reference times the CPU oracle on a
 bounded sample of the same workload instead.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gdn|reference]
-Multi-GPU: launched by torchrun, one rank per GPU; each rank runs its own
-independent batch (weak scaling, no collective on the data path).
+Multi-GPU: launched by torchrun, one rank per GPU; each rank decodes its own
+64-sequence batch (rank_workload: weak scaling, no collective on the data
+path; only the timing is reduced over ranks).
 """
 
 from __future__ import annotations
@@ -169,12 +170,15 @@ class ClockSampler:
 
 # ------------------------------------------------------------ multi-rank
 
-def shard_range(n, world, rank):
-    """Contiguous share [lo, hi) of n independent units for `rank` of
-    `world` (the first n % world ranks take one extra)."""
-    base, extra = divmod(n, world)
-    lo = rank * base + min(rank, extra)
-    return lo, lo + base + (1 if rank < extra else 0)
+def rank_workload(rank, **overrides):
+    """The headline batch that `rank` decodes: 64 sequences x 48 heads of
+    its own (the workload's seed plus 1000 x rank), so ranks share no data
+    and the data path needs no collective; rank 0's batch is the
+    single-GPU workload.  `overrides` change the sizes (tests)."""
+    kw = dict(gdn_inputs.WORKLOADS["decode_b64"])
+    kw.update(overrides)
+    return gdn_inputs.make_inputs(
+        gdn_inputs.WORKLOAD_SEED["decode_b64"] + 1000 * rank, **kw)
 
 
 def aggregate(ms_local, units_local, dist=None, device=None):
@@ -602,7 +606,7 @@ def main():
         return 0
 
     # ---- headline workload: batched decode step
-    inp = gdn_inputs.make_workload("decode_b64")
+    inp = rank_workload(rank)
     B, kh, vh = inp.B, inp.kh, inp.vh
     tens = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     S0 = tens(inp.S)

@@ -44,8 +44,8 @@
 // for its completion in the same way before reading its outputs.
 //
 // Three layouts share that arithmetic:
-//   - gdn_step_c32_kernel: single-token launches with device-resident
-//     inputs.  A CTA of 4 warps takes a 32-column group of a head, warp w
+//   - gdn_step_c32_kernel: single-token launches (with host-memory
+//     inputs, CTAs of two column groups of a head).  A CTA of 4 warps takes a 32-column group of a head, warp w
 //     key rows 32w .. 32w+31 of all 32 columns, so every warp request covers
 //     whole 128-byte row segments; the reductions over the key rows finish
 //     across the 4 warps through shared memory, one barrier per unit.  On
@@ -57,9 +57,10 @@
 //     shared-memory ring filled by bulk copies (see its comment).  On
 //     64 x 48 heads it measured 73 / 79 / 121 us for M = 2 / 4 / 8 without
 //     checkpoints, against 82 / 109 / 170 us for the 8-column layout.
-//   - gdn_steps_kernel (the 8-column layout above): launches whose token
-//     inputs are in host memory, whose warps then share the q and k rows
-//     of a head in L1.
+//   - gdn_steps_kernel (the 8-column layout above): multi-token or
+//     checkpointing launches whose token inputs are in host memory (8 warps
+//     on neighbouring column groups share a head's q and k rows in L1), and
+//     those of fewer heads than SMs.
 //
 // Determinism.  Every product and sum is an explicit round-to-nearest
 // intrinsic and the reduction tree is fixed, so a token gives the same bits
@@ -79,11 +80,12 @@ constexpr int kStages = 3;        // cp.async ring depth per warp
 constexpr int kWarpsPerSm = 16;   // bound by registers and shared memory
 constexpr int kUnitsPerHead = kDim / 8;          // 16 column groups
 constexpr int kUnitFloats = kDim * 8;            // 4 KB
-// Warps per CTA: 4, or 8 for single-token launches whose token inputs are
-// in host memory, so that the 8 warps working on neighbouring column groups
-// of a head share its q and k rows in one SM's L1 (the 64 x 48-head step
-// then takes 70 us instead of 86 us; with device inputs 4-warp CTAs are
-// 0.2 % faster, and 8 measured 2-7 % slower for several tokens).
+// Warps per CTA: 4, or 8 for checkpointing single-token launches whose token
+// inputs are in host memory, so that the 8 warps working on neighbouring
+// column groups of a head share its q and k rows in one SM's L1 (a 64 x
+// 48-head step took 70 us instead of 86 us that way; with device inputs
+// 4-warp CTAs are 0.2 % faster, and 8 measured 2-7 % slower for several
+// tokens).
 template <int kWarps>
 __host__ __device__ constexpr int smem_per_cta() {
   return kWarps * kStages * kUnitFloats * 4;
@@ -493,13 +495,25 @@ __global__ void __launch_bounds__(kWarps * 32, kWarpsPerSm / kWarps)
 // every lane finishes S^T k for its 4 columns over the 4 warps, (W_0 + W_2)
 // + (W_1 + W_3); warp 0's lanes 0-7 also finish S^T q and write o.  The
 // arithmetic is token_update's, term for term.
-constexpr int kC32Warps = 4;
-constexpr int kC32Groups = kDim / 32;                 // units per head
+constexpr int kC32Warps = 4;                          // warps per column group
+// Column groups per CTA when the token inputs are in host memory: 2 (a
+// 64 x 48-head step took 67.9 us end to end, against 78.8 us with 4 groups,
+// whose 16-warp CTAs run one per SM and wait longer at their barrier, and
+// 70.1 us for the 8-column layout with 8-warp CTAs).
+constexpr int kHostGroups = 2;
+constexpr int kC32Groups = kDim / 32;                 // column groups per head
 constexpr int kC32Stage = 32 * 32 * 4;                // one warp's 4 KB
-constexpr int kC32Smem = kC32Warps * kStages * kC32Stage +
-                         (2 * kC32Warps * 64 + 2 * kC32Warps) * 4;
+template <int G>
+__host__ __device__ constexpr int c32_smem() {
+  return G * kC32Warps * kStages * kC32Stage + G * (2 * kC32Warps * 64 + 2 * kC32Warps) * 4;
+}
 
-__global__ void __launch_bounds__(kC32Warps * 32, kWarpsPerSm / kC32Warps)
+// G column groups of a head per CTA (4 G warps): G = 1 for device-resident
+// inputs; G = kHostGroups when the token inputs are in host memory, so that
+// the CTA's column groups share a head's q and k rows in L1 and the rows
+// cross the host link fewer times.
+template <int G>
+__global__ void __launch_bounds__(G * kC32Warps * 32, kWarpsPerSm / (G * kC32Warps))
     gdn_step_c32_kernel(const float *S_in, float *S_out,
                         const float *__restrict__ q,
                         const float *__restrict__ k,
@@ -509,14 +523,17 @@ __global__ void __launch_bounds__(kC32Warps * 32, kWarpsPerSm / kC32Warps)
                         float *__restrict__ o, int vh, int kh, int rep,
                         size_t nheads) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = wid & (kC32Warps - 1), grp = wid / kC32Warps;
   const int rq = lane >> 3, cq = lane & 7;
   const uint32_t ring = (uint32_t)__cvta_generic_to_shared(smem_raw) +
-                        (uint32_t)(warp * kStages * kC32Stage);
-  // exchange: [parity][warp][cq][kv0..3, qs0..3] and [parity][warp] q . k
-  float *xch = reinterpret_cast<float *>(smem_raw + kC32Warps * kStages * kC32Stage);
+                        (uint32_t)(wid * kStages * kC32Stage);
+  // exchange per group: [parity][warp][cq][kv0..3, qs0..3] and
+  // [parity][warp] q . k
+  float *xch = reinterpret_cast<float *>(smem_raw + G * kC32Warps * kStages * kC32Stage) +
+               grp * (2 * kC32Warps * 64 + 2 * kC32Warps);
   float *qkx = xch + 2 * kC32Warps * 64;
-  const size_t nunits = nheads * kC32Groups;
+  const size_t nunits = nheads * (kC32Groups / G);
   const size_t mine =
       blockIdx.x < nunits ? (nunits - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
   const uint64_t pol = l2_keep_priority();
@@ -526,8 +543,8 @@ __global__ void __launch_bounds__(kC32Warps * 32, kWarpsPerSm / kC32Warps)
 
   auto issue = [&](size_t i, int st) {
     const size_t u = blockIdx.x + i * gridDim.x;
-    const size_t head = u / kC32Groups;
-    const int cg = (int)(u % kC32Groups);
+    const size_t head = u / (kC32Groups / G);
+    const int cg = (int)(u % (kC32Groups / G)) * G + grp;
     const float *src = S_in + head * (size_t)(kDim * kDim) + (size_t)r0 * kDim +
                        32 * cg + 4 * cq;
     const uint32_t dst = ring + (uint32_t)(st * kC32Stage) + lane_off;
@@ -549,8 +566,8 @@ __global__ void __launch_bounds__(kC32Warps * 32, kWarpsPerSm / kC32Warps)
       cp_async_commit();
     }
     const size_t u = blockIdx.x + i * gridDim.x;
-    const size_t head = u / kC32Groups;
-    const int cg = (int)(u % kC32Groups);
+    const size_t head = u / (kC32Groups / G);
+    const int cg = (int)(u % (kC32Groups / G)) * G + grp;
     const int b = (int)(head / vh), vi = (int)(head % vh), hh = vi / rep;
     const TokenIn t = load_token(q, k, v, g, beta, ((size_t)b * kh + hh) * kDim + r0,
                                  ((size_t)b * vh + vi) * kDim + 32 * cg + 4 * cq,
@@ -1128,24 +1145,33 @@ cudaError_t launch_steps(const float *S_in, float *S_out, float *ckpt,
   const size_t nheads = (size_t)B * vh;
   const size_t nunits = nheads * kUnitsPerHead;
   if (nunits == 0) return cudaSuccess;
-  if (M == 1 && !ckpt && !host_inputs) {
-    // one token, device-resident inputs: the 32-column layout
-    const size_t units = nheads * kC32Groups;
-    size_t ctas = (size_t)sm_count() * (kWarpsPerSm / kC32Warps);
-    if (ctas > units) ctas = units;
-    const cudaError_t e = cudaFuncSetAttribute(
-        gdn_step_c32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kC32Smem);
-    if (e != cudaSuccess) return e;
-    return launch_maybe_overlapped(gdn_step_c32_kernel, dim3((unsigned)ctas),
-                                   dim3(kC32Warps * 32), kC32Smem, stream,
-                                   overlap, S_in, S_out, q, k, v, g, beta, o,
-                                   vh, kh, vh / kh, nheads);
+  if (M == 1 && !ckpt) {
+    // one token: the 32-column layout, G column groups of a head per CTA
+    auto go32 = [&](auto kernel, int G) {
+      const size_t units = nheads * (kC32Groups / G);
+      size_t ctas = (size_t)sm_count() * (kWarpsPerSm / (G * kC32Warps));
+      if (ctas > units) ctas = units;
+      const int smem = G == 1 ? c32_smem<1>() : G == 2 ? c32_smem<2>() : c32_smem<4>();
+      const cudaError_t e = cudaFuncSetAttribute(
+          kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      return launch_maybe_overlapped(kernel, dim3((unsigned)ctas),
+                                     dim3(G * kC32Warps * 32), smem, stream,
+                                     overlap, S_in, S_out, q, k, v, g, beta, o,
+                                     vh, kh, vh / kh, nheads);
+    };
+    if (!host_inputs) return go32(gdn_step_c32_kernel<1>, 1);
+    return kHostGroups == 4 ? go32(gdn_step_c32_kernel<4>, 4)
+                            : go32(gdn_step_c32_kernel<2>, 2);
   }
-  if (!host_inputs) {
-    // several tokens or checkpoints, device-resident inputs: one CTA per
-    // head (head indices in 32 bits)
+  const size_t sms = (size_t)sm_count();
+  if (!host_inputs && nheads >= sms) {
+    // several tokens or checkpoints, device-resident inputs, at least one
+    // head per SM: one CTA per head (head indices in 32 bits).  Fewer heads
+    // spread better over the SMs in the 8-column layout (one sequence of
+    // 48 heads, 64 tokens: 41 us there against 56 us here).
     if (nheads > 0xffffffffull) return cudaErrorInvalidConfiguration;
-    size_t ctas = (size_t)sm_count() * kHCtasPerSm;
+    size_t ctas = sms * kHCtasPerSm;
     if (ctas > nheads) ctas = nheads;
     auto goh = [&](auto kernel) {
       cudaError_t e = cudaFuncSetAttribute(
@@ -1163,7 +1189,7 @@ cudaError_t launch_steps(const float *S_in, float *S_out, float *ckpt,
   const int wpc = M == 1 && host_inputs ? 8 : 4;
   const int smem = wpc == 8 ? smem_per_cta<8>() : smem_per_cta<4>();
   size_t ctas = (nunits + wpc - 1) / wpc;
-  const size_t cap = (size_t)sm_count() * (kWarpsPerSm / wpc);
+  const size_t cap = sms * (kWarpsPerSm / wpc);
   if (ctas > cap) ctas = cap;
   const dim3 grid((unsigned)ctas), block(wpc * 32);
   auto go = [&](auto kernel, float *ck) {

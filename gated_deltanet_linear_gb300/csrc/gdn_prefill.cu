@@ -532,8 +532,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tm_v,
                      const float *__restrict__ g,
                      const float *__restrict__ beta,
-                     const __grid_constant__ CUtensorMap tm_o, int T, int kh,
-                     int vh, int rep) {
+                     const __grid_constant__ CUtensorMap tm_o,
+                     float *__restrict__ o, int T, int kh, int vh, int rep) {
   // Where the gate warp makes the next chunk's gate vectors, while the
   // chunk still reads its own: warp 7 during the inverse's first step
   // (bf16), or warp 0 while the SIMT warps wait for the correction product
@@ -1006,8 +1006,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 16; ++j) Sh[(size_t)(c0 + j) * kD + myrow] = r[j];
       }
-    } else if (tid == 0) {
-      atomicAdd(&g_prefill_timeouts, 1u);
+    } else {
+      // a wait ran out: the head's state and every o row of the head become
+      // NaN (after the tensor stores already issued have landed), so the
+      // failure shows in the results as well as in the counter
+      if (tid == 0) {
+        atomicAdd(&g_prefill_timeouts, 1u);
+        bulk_wait_all();
+      }
+      simt_sync();
+      const float nan = __int_as_float(0x7fffffff);
+      float *Sh = S + head_off;
+      for (int e = tid; e < kD * kD; e += kSimt) Sh[e] = nan;
+      for (size_t e = tid; e < (size_t)T * kD; e += kSimt) {
+        const size_t t = e / kD;
+        o[(((size_t)b * T + t) * vh + vi) * kD + (e - t * kD)] = nan;
+      }
     }
     if (tid == 0) bulk_wait_all();  // no store of o outlives the CTA
   }
@@ -1084,13 +1098,13 @@ cudaError_t launch_prefill_chunked(float *S, const float *q, const float *k,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
     if (e != cudaSuccess) return e;
     gdn_chunk_kernel<true><<<(unsigned)nheads, kThreads, kSmemAlloc, stream>>>(
-        S, tm_q, tm_k, tm_v, g, beta, tm_o, T, kh, vh, vh / kh);
+        S, tm_q, tm_k, tm_v, g, beta, tm_o, o, T, kh, vh, vh / kh);
   } else {
     e = cudaFuncSetAttribute(gdn_chunk_kernel<false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
     if (e != cudaSuccess) return e;
     gdn_chunk_kernel<false><<<(unsigned)nheads, kThreads, kSmemAlloc, stream>>>(
-        S, tm_q, tm_k, tm_v, g, beta, tm_o, T, kh, vh, vh / kh);
+        S, tm_q, tm_k, tm_v, g, beta, tm_o, o, T, kh, vh, vh / kh);
   }
   return cudaGetLastError();
 }

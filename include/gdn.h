@@ -224,9 +224,9 @@ int gdn_prefill(const gdn_shape *shape, int T, float *S, const float *q,
  * gdn_prefill_timeouts - (an interface addition with no counterpart in the
  * articles) number of chunked-prefill CTAs, since the library
  * was loaded on the current device, that gave up waiting for a tensor-core
- * operation (each wait is bounded) and left their head's state unwritten.
- * Synchronises the current device.  Expected to stay 0; a non-zero count
- * means the results of those launches are invalid.
+ * operation (each wait is bounded).  Such a CTA writes NaN into its head's
+ * whole state and every o row of its head, so the failure shows in the
+ * results too.  Synchronises the current device.  Expected to stay 0.
  */
 int gdn_prefill_timeouts(unsigned int *count);
 

@@ -137,3 +137,10 @@ def test_layer_and_norm_host_refusals(lib):
     assert lib.gdn_layer_hist_rollback(ctypes.byref(ok), 0, 4, *([n] * 5),
                                        n) == gdn.GDN_ERANGE
     assert gdn.gdn_strerror(gdn.GDN_ESCRATCH) != "unknown status"
+
+
+def test_timeout_counters_refuse_a_null_destination(lib):
+    """The wait time-out counters report through an out-parameter; a NULL
+    one is refused on the host (no CUDA call)."""
+    assert lib.gdn_prefill_timeouts(None) == gdn.GDN_EINVAL
+    assert lib.gdn_wait_timeouts(None) == gdn.GDN_EINVAL
