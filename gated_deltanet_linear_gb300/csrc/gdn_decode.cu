@@ -771,6 +771,16 @@ __device__ __forceinline__ void arrive_expect_tx(uint32_t mbar, uint32_t bytes) 
                : "memory");
 }
 
+// Shared-memory fetch-and-add with acquire-release ordering at CTA scope.
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned *p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "r"((uint32_t)__cvta_generic_to_shared(p)), "r"(v)
+               : "memory");
+  return old;
+}
+
 __device__ __forceinline__ float lds32(uint32_t smem) {
   float r;
   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(r) : "r"(smem));
@@ -1001,16 +1011,13 @@ __global__ void __launch_bounds__(kHWarps * 32, kHCtasPerSm)
       // release the slot; the warp that releases it last refills it
       __syncwarp();
       if (lane == 0) {
-        __threadfence_block();
-        const unsigned old = atomicAdd(&cnt[sl], 1u);
-        if ((old & (kHWarps - 1)) == kHWarps - 1) {
+        // release this warp's reads of the slot; the last warp acquires
+        // everyone's before it lets the copy engine overwrite the slot
+        if ((atom_add_acq_rel(cnt + sl, 1u) & (kHWarps - 1)) == kHWarps - 1) {
           unsigned i2 = i;
           int m2 = m;
           ahead(i2, m2);
-          if (i2 < mine) {
-            __threadfence_block();
-            issue_item(i2, m2, sl, use + 1);
-          }
+          if (i2 < mine) issue_item(i2, m2, sl, use + 1);
         }
       }
       if (kCkpt) {
