@@ -334,16 +334,19 @@ def tens_fn(torch, dev):
 
 
 def verify_parts(torch, gdn, tens, stream, hbm_peak, parts, steps,
-                 warmup=5, sm_mhz=2070.0):
+                 warmup=5, sm_mhz=2070.0, case=None):
     """The M-token verify launches, M = 2, 4, 8, without and with per-token
     checkpoints, on 32 sequences x 48 heads (the verify workload) and on
     64 sequences x 48 heads (the batched decode size); each timed over
     max(20, min(200, steps)) launches after `warmup` untimed ones, with
     three state sets in turn (each larger than L2 at B = 64, 100 MB at
     B = 32).  Besides the HBM fraction each entry gives the FP32 issue floor
-    and the fraction of max(HBM floor, FP32 floor)."""
+    and the fraction of max(HBM floor, FP32 floor).  `case` (a part name
+    such as "verify_b64_m8") runs that one configuration only (profiling)."""
     dev = torch.device("cuda", torch.cuda.current_device())
     for wname in ("verify_b32", "verify_b64"):
+        if case is not None and not case.startswith(wname + "_"):
+            continue
         if wname == "verify_b32":
             vin = gdn_inputs.make_workload("verify_b32")
         else:
@@ -357,6 +360,10 @@ def verify_parts(torch, gdn, tens, stream, hbm_peak, parts, steps,
                                             sub.beta)) for _ in range(NSETS)]
             vo = torch.empty(sub.B, M, sub.vh, D, device=dev)
             for use_ck in (False, True):
+                pname = f"{wname}_m{M}{'_ckpt' if use_ck else ''}"
+                if case is not None and case != pname:
+                    continue
+
                 def vstep(i, M=M, use_ck=use_ck):
                     s = Sv[i % NSETS]
                     gdn.gdn_step_m(s, s, ck[:M] if use_ck else None,
@@ -369,7 +376,7 @@ def verify_parts(torch, gdn, tens, stream, hbm_peak, parts, steps,
                 ht = sub.B * sub.vh * M
                 hbm_floor = nb / (hbm_peak * 1e9)
                 fp_floor = fp32_floor_s(ht, sm_mhz)
-                parts[f"{wname}_m{M}{'_ckpt' if use_ck else ''}"] = {
+                parts[pname] = {
                     "ms": vms, "head_steps_per_s": ht / (vms * 1e-3),
                     "gbs": nb / (vms * 1e-3) / 1e9,
                     "frac_of_measured_hbm": nb / (vms * 1e-3) / 1e9 / hbm_peak,
@@ -412,6 +419,23 @@ def small_decode_parts(torch, gdn, tens, stream, parts, steps):
     for i in range(T):
         chain(i)
     ms = time_launches(torch, chain, 10 * T, stream)
+    # the same 64 chained steps captured once in a CUDA graph and replayed
+    # (the per-call host work of the binding and the library is then gone)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for t in range(T):
+            gdn.gdn_step(Sc, *per_tok[t], oc)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for t in range(T):
+            gdn.gdn_step(Sc, *per_tok[t], oc)
+    cur = torch.cuda.current_stream()
+    for _ in range(3):
+        graph.replay()
+    msg = time_launches(torch, lambda i: graph.replay(), 20, cur) / T
     om = torch.empty(1, T, ch.vh, D, device=dev)
     Sm = tens(ch.S)
     multi = lambda i: gdn.gdn_step_m(Sm, Sm, None, q, k, v, g, beta, om,
@@ -422,12 +446,14 @@ def small_decode_parts(torch, gdn, tens, stream, parts, steps):
     parts["decode_b1_t64"] = {
         "us_per_step_chained": ms * 1e3,
         "head_steps_per_s_chained": ch.vh / (ms * 1e-3),
+        "us_per_step_chained_graph": msg * 1e3,
         "us_per_launch_m64": msm * 1e3,
         "us_per_token_m64": msm * 1e3 / T,
         "head_steps_per_s_m64": ch.vh * T / (msm * 1e-3),
-        "note": "64 tokens, B=1 x 48 heads: 64 chained gdn_step calls, and "
+        "note": "64 tokens, B=1 x 48 heads: 64 chained gdn_step calls "
+                "(launched one by one, and replayed from a CUDA graph), and "
                 "one gdn_step_m launch over the same 64 tokens"}
-    del S1, Sc, Sm
+    del S1, Sc, Sm, graph
 
 
 def layer_parts(torch, gdn, tens, stream, hbm_peak, parts, steps,
@@ -543,6 +569,9 @@ def main():
                     help="skip the verify / prefill sub-measurements")
     ap.add_argument("--no-cpu", action="store_true",
                     help="skip the CPU-baseline leg")
+    ap.add_argument("--case", default=None,
+                    help="with --only verify: one configuration, e.g. "
+                         "verify_b64_m8 or verify_b64_m2_ckpt (profiling)")
     ap.add_argument("--only", choices=["prefill", "layer", "verify", "small"],
                     default=None,
                     help="time only the prefill, layer or verify parts (used "
@@ -592,7 +621,8 @@ def main():
             prefill_parts(torch, gdn, tens_fn(torch, dev), stream, peaks, parts)
         elif args.only == "verify":
             verify_parts(torch, gdn, tens_fn(torch, dev), stream, hbm_peak,
-                         parts, args.steps, max(5, args.warmup), sm_max)
+                         parts, args.steps, max(5, args.warmup), sm_max,
+                         args.case)
         elif args.only == "small":
             small_decode_parts(torch, gdn, tens_fn(torch, dev), stream, parts,
                                args.steps)
