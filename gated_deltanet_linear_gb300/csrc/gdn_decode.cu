@@ -51,16 +51,16 @@
 //     across the 4 warps through shared memory, one barrier per unit.  On
 //     the 64 x 48-head step it measured 65.1 us against 69.7 us for the
 //     8-column layout.
-//   - gdn_steps_head_kernel: several tokens, or checkpoints, with
+//   - gdn_steps_head_kernel: several tokens without checkpoints, with
 //     device-resident inputs.  One CTA of 8 warps per head, 16 columns per
 //     warp, two 8-row blocks per lane; the token inputs stream through a
 //     shared-memory ring filled by bulk copies (see its comment).  On
-//     64 x 48 heads it measured 73 / 79 / 121 us for M = 2 / 4 / 8 without
-//     checkpoints, against 82 / 109 / 170 us for the 8-column layout.
-//   - gdn_steps_kernel (the 8-column layout above): multi-token or
-//     checkpointing launches whose token inputs are in host memory (8 warps
-//     on neighbouring column groups share a head's q and k rows in L1), and
-//     those of fewer heads than SMs.
+//     64 x 48 heads it measured 73 / 79 / 121 us for M = 2 / 4 / 8,
+//     against 82 / 109 / 170 us for the 8-column layout.
+//   - gdn_steps_kernel (the 8-column layout above): checkpointing launches
+//     (bound by their stores, faster here), multi-token launches whose
+//     token inputs are in host memory (8 warps on neighbouring column groups
+//     share a head's q and k rows in L1), and those of fewer heads than SMs.
 //
 // Determinism.  Every product and sum is an explicit round-to-nearest
 // intrinsic and the reduction tree is fixed, so a token gives the same bits
@@ -666,7 +666,7 @@ __global__ void __launch_bounds__(G * kC32Warps * 32, kWarpsPerSm / (G * kC32War
   cp_async_wait<0>();
 }
 
-// Multi-token update (M > 1, or checkpoints) with device-resident token
+// Multi-token update (M > 1, no checkpoints) with device-resident token
 // inputs: one CTA of 8 warps per head, warp c on the head's 16-column group
 // c.  Lane = 4 rg + cq holds columns 16 c + 4 cq .. +3 of the two 8-row
 // blocks that the first level of the reduction tree adds: rg = 2 w + j,
@@ -787,10 +787,9 @@ __device__ __forceinline__ float lds32(uint32_t smem) {
   return r;
 }
 
-template <bool kCkpt>
 __global__ void __launch_bounds__(kHWarps * 32, kHCtasPerSm)
     gdn_steps_head_kernel(const float *S_in, float *S_out,
-                          float *__restrict__ ckpt, const float *__restrict__ q,
+                          const float *__restrict__ q,
                           const float *__restrict__ k,
                           const float *__restrict__ v,
                           const float *__restrict__ g,
@@ -813,7 +812,6 @@ __global__ void __launch_bounds__(kHWarps * 32, kHCtasPerSm)
   const unsigned mine =
       blockIdx.x < nheads ? (nheads - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
   const size_t hstride = (size_t)vh * kDim;     // o / v stride per token
-  const size_t ckstride = (size_t)nheads * (kDim * kDim);
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   auto head_of = [&](unsigned i) { return blockIdx.x + i * gridDim.x; };
@@ -921,7 +919,6 @@ __global__ void __launch_bounds__(kHWarps * 32, kHCtasPerSm)
       const unsigned b = head / (unsigned)vh;
       op = o + ((size_t)b * (size_t)M * vh + (head - b * (unsigned)vh)) * kDim + col + w;
     }
-    float *cp = kCkpt ? ckpt + soff : nullptr;
 
     for (m = 0; m < M; ++m) {
       if ((m & 31) == 0) {  // the next 32 tokens' gates, and the chunk after
@@ -1020,12 +1017,6 @@ __global__ void __launch_bounds__(kHWarps * 32, kHCtasPerSm)
           if (i2 < mine) issue_item(i2, m2, sl, use + 1);
         }
       }
-      if (kCkpt) {
-#pragma unroll
-        for (int r = 0; r < 16; ++r)
-          st_stream<false>(cp + (r < 8 ? r : r + 8) * kDim, s[r], 0);
-        cp += ckstride;
-      }
       if (++sl == kHSlots) {
         sl = 0;
         ++use;
@@ -1039,7 +1030,7 @@ __global__ void __launch_bounds__(kHWarps * 32, kHCtasPerSm)
 
   if (!ok) {
     // a wait ran out: every result of this warp not yet written becomes NaN
-    // (the state and checkpoints of unit i on, o of token m of unit i on)
+    // (the state of unit i on, o of token m of unit i on)
     if (lane == 0 && atomicExch(failed, 1) == 0) atomicAdd(&g_steps_timeouts, 1u);
     const float nan = __int_as_float(0x7fffffff);
     const float4 nan4 = make_float4(nan, nan, nan, nan);
@@ -1049,13 +1040,8 @@ __global__ void __launch_bounds__(kHWarps * 32, kHCtasPerSm)
       const unsigned b = head / (unsigned)vh;
       float *op = o + ((size_t)b * (size_t)M * vh + (head - b * (unsigned)vh)) * kDim + col + w;
       for (int r = 0; r < 16; ++r) st_stream<false>(S_out + soff + (r < 8 ? r : r + 8) * kDim, nan4, 0);
-      for (int mm = ii == i ? m : 0; mm < M; ++mm) {
-        if (j) op[(size_t)mm * hstride] = nan;
-        if (kCkpt)
-          for (int r = 0; r < 16; ++r)
-            st_stream<false>(ckpt + (size_t)mm * ckstride + soff + (r < 8 ? r : r + 8) * kDim,
-                             nan4, 0);
-      }
+      if (j)
+        for (int mm = ii == i ? m : 0; mm < M; ++mm) op[(size_t)mm * hstride] = nan;
     }
   }
   cp_async_wait<0>();
@@ -1172,26 +1158,24 @@ cudaError_t launch_steps(const float *S_in, float *S_out, float *ckpt,
                             : go32(gdn_step_c32_kernel<2>, 2);
   }
   const size_t sms = (size_t)sm_count();
-  if (!host_inputs && nheads >= sms) {
-    // several tokens or checkpoints, device-resident inputs, at least one
+  if (!host_inputs && !ckpt && nheads >= sms) {
+    // several tokens, device-resident inputs, no checkpoints, at least one
     // head per SM: one CTA per head (head indices in 32 bits).  Fewer heads
     // spread better over the SMs in the 8-column layout (one sequence of
-    // 48 heads, 64 tokens: 41 us there against 56 us here).
+    // 48 heads, 64 tokens: 41 us there against 56 us here), and
+    // checkpointing launches, bound by their stores, ran faster there too
+    // (64 x 48 heads, M = 2 / 4 / 8: 136 / 194 / 326 us against 139 / 213 /
+    // 355 us here).
     if (nheads > 0xffffffffull) return cudaErrorInvalidConfiguration;
     size_t ctas = sms * kHCtasPerSm;
     if (ctas > nheads) ctas = nheads;
-    auto goh = [&](auto kernel) {
-      cudaError_t e = cudaFuncSetAttribute(
-          kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kHSmem);
-      if (e != cudaSuccess) return e;
-      return launch_maybe_overlapped(kernel, dim3((unsigned)ctas),
-                                     dim3(kHWarps * 32), kHSmem, stream,
-                                     overlap, S_in, S_out, ckpt, q, k, v, g,
-                                     beta, o, vh, kh, vh / kh, M,
-                                     (unsigned)nheads);
-    };
-    return ckpt ? goh(gdn_steps_head_kernel<true>)
-                : goh(gdn_steps_head_kernel<false>);
+    const cudaError_t e = cudaFuncSetAttribute(
+        gdn_steps_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kHSmem);
+    if (e != cudaSuccess) return e;
+    return launch_maybe_overlapped(gdn_steps_head_kernel, dim3((unsigned)ctas),
+                                   dim3(kHWarps * 32), kHSmem, stream, overlap,
+                                   S_in, S_out, q, k, v, g, beta, o, vh, kh,
+                                   vh / kh, M, (unsigned)nheads);
   }
   const int wpc = M == 1 && host_inputs ? 8 : 4;
   const int smem = wpc == 8 ? smem_per_cta<8>() : smem_per_cta<4>();
