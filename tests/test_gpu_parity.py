@@ -246,6 +246,29 @@ def test_verify_b64_bit_exact(oracle_mod, M):
     assert gdn.gdn_wait_timeouts() == 0
 
 
+@pytest.mark.parametrize("B,kh,vh,M", [(4, 16, 48, 3), (4, 16, 48, 7),
+                                       (4, 16, 48, 45), (20, 8, 8, 9),
+                                       (19, 4, 8, 33)])
+def test_multi_token_head_kernel_bit_exact(oracle_mod, B, kh, vh, M):
+    """Multi-token launches of at least one head per SM without checkpoints
+    (the head-per-CTA kernel): token counts that are not multiples of the
+    32-token gate chunk or of the 6-slot input ring, and other key / value
+    head counts (one and two value heads per key head; 152 and 160 heads).
+    o and the final state bit-identical to M single-token launches; within
+    1e-4 of the oracle on two sequences."""
+    inp = gdn_inputs.make_inputs(2000 + 7 * M + vh + B, B=B, T=M, kh=kh, vh=vh)
+    _, S_out, _, o = run_step_m(inp, ckpt=False)
+    S_ss, o_ss, _ = run_single_steps(inp)
+    assert torch.equal(o, o_ss)
+    assert torch.equal(S_out, S_ss)
+    bs = [0, B - 1]
+    S_ref, o_ref = oracle_mod.run_inputs(inp.heads(bs, range(vh)))
+    es = err_state(host(S_out)[bs], S_ref)
+    eo = err_out(host(o)[bs], o_ref)
+    assert es < TOL_MULTI and eo < TOL_MULTI
+    assert gdn.gdn_wait_timeouts() == 0
+
+
 def test_verify_variants_identical():
     """In place vs out of place, with vs without checkpoints: same bits."""
     inp = gdn_inputs.make_workload("verify_b32").tokens(0, 4).heads(
