@@ -256,9 +256,10 @@ def cpu_baseline(inp, seconds=10.0):
 
 
 def cpu_configs(seconds=2.0):
-    """The oracle on the other decode workloads (one sequence, one token;
-    one sequence, 64 chained tokens; 32 sequences x M tokens), each
-    repeated for about `seconds`: head-steps/s per workload."""
+    """The oracle on the other workloads (one sequence, one token; one
+    sequence, 64 chained tokens; 32 sequences x M tokens, each repeated for
+    about `seconds`; the 8 x 4096-token prefill once): head-steps/s per
+    workload."""
     import oracle
     oracle.build()
 
@@ -283,6 +284,14 @@ def cpu_configs(seconds=2.0):
                         sub.B * sub.vh * M)
         out[f"verify_b32_m{M}_ckpt"] = {"value": r,
                                         "sample": f"{c} calls in {el:.1f} s"}
+    # the long-sequence prefill in full (8 x 4096 tokens x 48 heads, one
+    # call: the token-serial definition, which the chunked form regroups)
+    pre = gdn_inputs.make_workload("prefill_b8_t4096")
+    t0 = time.perf_counter()
+    oracle.run_inputs(pre)
+    el = time.perf_counter() - t0
+    out["prefill_b8_t4096"] = {"value": pre.B * pre.T * pre.vh / el,
+                               "sample": f"1 call in {el:.1f} s"}
     return out
 
 
