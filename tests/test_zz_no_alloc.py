@@ -138,6 +138,8 @@ def test_noalloc_matches_workspace_entry_on_two_calls_in_a_row():
 def test_noalloc_refuses_a_valid_request_larger_than_the_scratch():
     """With every buffer valid, B * M beyond the scratch gives GDN_ESCRATCH
     and launches nothing (the outputs keep their contents)."""
+    import __graft_entry__
+    __graft_entry__.build()
     torch.cuda.set_device(0)
     per_token = gdn.gdn_layer_workspace(1, 16, 48, 1)
     M = gdn.GDN_NOALLOC_SCRATCH_BYTES // per_token + 1          # 406 tokens
