@@ -26,10 +26,18 @@ def _pinned(a):
     return torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
 
 
-@pytest.mark.parametrize("host_in,host_out", [(True, True), (False, True),
-                                              (True, False)])
+CASES = [(hi, ho, ck) for hi in (True, False) for ho in (True, False)
+         for ck in (False, True) if hi or ho or ck]
+
+
+@pytest.mark.parametrize("host_in,host_out,ckpt", CASES)
 @pytest.mark.parametrize("M", [1, 3])
-def test_host_token_buffers_same_bits(host_in, host_out, M):
+def test_host_token_buffers_same_bits(host_in, host_out, ckpt, M):
+    """Every combination of token buffers in host or device memory, one or
+    three tokens, with or without checkpoints, against the device-memory
+    launch without checkpoints: the same bits (the launches run different
+    kernels: the 32-column single-token kernel with one or two column groups
+    per CTA, the head-per-CTA kernel, the 8-column kernel)."""
     inp = gdn_inputs.make_inputs(1401 + M, B=5, T=M)
     xs = (inp.q, inp.k, inp.v, inp.g, inp.beta)
     d_in = [dev(x) for x in xs]
@@ -40,13 +48,16 @@ def test_host_token_buffers_same_bits(host_in, host_out, M):
     S = dev(inp.S)
     o = (torch.empty(inp.B, M, inp.vh, inp.vd).pin_memory() if host_out
          else empty(inp.B, M, inp.vh, inp.vd))
-    if M == 1:
+    ck = empty(M, *inp.S.shape) if ckpt else None
+    if M == 1 and not ckpt:
         gdn.gdn_step(S, *ins, o)
     else:
-        gdn.gdn_step_m(S, S, None, *ins, o)
+        gdn.gdn_step_m(S, S, ck, *ins, o)
     torch.cuda.synchronize()
     assert torch.equal(S, S_ref)
     assert torch.equal(o.cpu(), o_ref.cpu())
+    if ckpt:
+        assert torch.equal(ck[M - 1], S_ref)
 
 
 def test_pageable_host_memory_refused():
