@@ -74,7 +74,8 @@ def decode_bytes(B, kh, vh, M=1, ckpt=False):
 # FP32 issue floor of the token-serial update: per head-token and state
 # element, two fused multiply-adds (S^T k and S^T q), one multiply (the
 # decay) and one fused multiply-add (the rank-1 update) -- 4 FP32 lane
-# operations for the 7 flops per element of the definition.  The GB300 has
+# operations for the 7 flops per element of the definition (decay 1, S^T k
+# 2, rank-1 update 2, S^T q 2).  The GB300 has
 # 152 SMs x 128 FP32 lanes; at the measured maximum SM clock that is
 # 152 * 128 * clock lane operations per second.
 FP32_LANE_OPS_PER_ELEM = 4
@@ -390,6 +391,8 @@ def verify_parts(torch, gdn, tens, stream, hbm_peak, parts, steps,
                     "gbs": nb / (vms * 1e-3) / 1e9,
                     "frac_of_measured_hbm": nb / (vms * 1e-3) / 1e9 / hbm_peak,
                     "bytes_per_launch": nb,
+                    "flops_per_launch": ht * 7 * D * D,
+                    "fp32_lane_ops_per_launch": ht * FP32_LANE_OPS_PER_ELEM * D * D,
                     "fp32_floor_us": fp_floor * 1e6,
                     "hbm_floor_us": hbm_floor * 1e6,
                     "frac_of_max_floor": max(hbm_floor, fp_floor) / (vms * 1e-3)}
