@@ -22,6 +22,7 @@ path; only the timing is reduced over ranks).
 from __future__ import annotations
 
 import argparse
+import ctypes
 import datetime
 import hashlib
 import json
@@ -416,9 +417,28 @@ def small_decode_parts(torch, gdn, tens, stream, parts, steps):
         f(i)
     n = max(200, min(2000, steps))
     ms = time_launches(torch, f, n, stream)
+    # the same call through the C ABI with its arguments prepared once: what
+    # a C or C++ caller pays per call (the library's argument checks and the
+    # launch), without the Python binding's tensor checks
+    lib = gdn.load()
+    sh = gdn.Shape(1, one.kh, one.vh, D, D)
+    ptrs = [t.data_ptr() for t in (S1,) + ins + (o1,)]
+    raw_stream = stream.cuda_stream
+    byref_sh = ctypes.byref(sh)
+
+    def raw(i):
+        if lib.gdn_step(byref_sh, *ptrs, raw_stream) != gdn.GDN_OK:
+            raise RuntimeError("gdn_step refused the decode_b1 call")
+    for i in range(20):
+        raw(i)
+    ms_raw = time_launches(torch, raw, n, stream)
     parts["decode_b1"] = {
         "us_per_call": ms * 1e3, "head_steps_per_s": one.vh / (ms * 1e-3),
-        "note": "gdn_step, B=1 x 48 heads, back-to-back launches"}
+        "us_per_call_c_abi": ms_raw * 1e3,
+        "head_steps_per_s_c_abi": one.vh / (ms_raw * 1e-3),
+        "note": "gdn_step, B=1 x 48 heads, back-to-back launches: through "
+                "the Python binding, and through the C ABI with arguments "
+                "prepared once (argument checks and launch every call)"}
 
     ch = gdn_inputs.make_workload("decode_b1_t64")
     T = ch.T

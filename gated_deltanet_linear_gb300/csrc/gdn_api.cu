@@ -30,42 +30,44 @@ bool overlaps(const Buf &a, const Buf &b) {
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
-// Device (or managed) memory of the current device.
-int check_device_ptr(const void *p) {
-  cudaPointerAttributes attr;
-  memset(&attr, 0, sizeof(attr));
-  cudaError_t e = cudaPointerGetAttributes(&attr, p);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return GDN_EPTR;
-  }
-  if (attr.type == cudaMemoryTypeManaged) return GDN_OK;
-  if (attr.type != cudaMemoryTypeDevice) return GDN_EPTR;
+// The caller's current device, or -1 (the CUDA error is cleared).
+int current_device() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
-    return GDN_ECUDA;
+    return -1;
   }
-  return attr.device == dev ? GDN_OK : GDN_EPTR;
+  return dev;
 }
 
-// Token inputs and outputs may also live in page-locked host memory that is
-// mapped into the device's address space at the same address (any
-// cudaHostAlloc / cudaMallocHost block under unified addressing): kernels
-// then read and write it over the host link.  Pageable memory is refused.
-// *host (if given) is set when p is host memory.
-int check_io_ptr(const void *p, bool *host = nullptr) {
+// One attribute query per pointer.  Device memory of `dev` and managed
+// memory pass.  Token inputs and outputs (allow_host) may also live in
+// page-locked host memory that is mapped into the device's address space at
+// the same address (any cudaHostAlloc / cudaMallocHost block under unified
+// addressing): kernels then read and write it over the host link, and *host
+// is set.  Pageable memory is refused.
+int classify_ptr(const void *p, int dev, bool allow_host, bool *host) {
   cudaPointerAttributes attr;
   memset(&attr, 0, sizeof(attr));
   if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
     cudaGetLastError();
     return GDN_EPTR;
   }
+  if (attr.type == cudaMemoryTypeManaged) return GDN_OK;
   if (attr.type == cudaMemoryTypeHost) {
+    if (!allow_host || attr.devicePointer != p) return GDN_EPTR;
     if (host) *host = true;
-    return attr.devicePointer == p ? GDN_OK : GDN_EPTR;
+    return GDN_OK;
   }
-  return check_device_ptr(p);
+  if (attr.type != cudaMemoryTypeDevice) return GDN_EPTR;
+  return attr.device == dev ? GDN_OK : GDN_EPTR;
+}
+
+// Device (or managed) memory of the current device.
+int check_device_ptr(const void *p) {
+  const int dev = current_device();
+  if (dev < 0) return GDN_ECUDA;
+  return classify_ptr(p, dev, false, nullptr);
 }
 
 int check_shape(const gdn_shape *s) {
@@ -76,31 +78,31 @@ int check_shape(const gdn_shape *s) {
   return GDN_OK;
 }
 
-// Every buffer: non-null, 16-byte aligned, device memory.
-int check_bufs(const Buf *b, int n) {
+// Every buffer: non-null, 16-byte aligned, device memory (or, for token
+// inputs and outputs, allow_host: mapped page-locked host memory; *any_host
+// is then set if one is).  A pointer already checked in the same list is
+// not queried again.
+int check_list(const Buf *b, int n, bool allow_host, bool *any_host) {
   for (int i = 0; i < n; ++i) {
     if (!b[i].p) return GDN_EINVAL;
     if (!aligned16(b[i].p)) return GDN_EALIGN;
   }
+  const int dev = current_device();
+  if (dev < 0) return GDN_ECUDA;
   for (int i = 0; i < n; ++i) {
-    const int r = check_device_ptr(b[i].p);
+    bool seen = false;
+    for (int j = 0; j < i && !seen; ++j) seen = b[j].p == b[i].p;
+    if (seen) continue;
+    const int r = classify_ptr(b[i].p, dev, allow_host, any_host);
     if (r != GDN_OK) return r;
   }
   return GDN_OK;
 }
 
-// check_bufs for token inputs and outputs (device, managed or mapped
-// page-locked host memory).
+int check_bufs(const Buf *b, int n) { return check_list(b, n, false, nullptr); }
+
 int check_io_bufs(const Buf *b, int n, bool *any_host = nullptr) {
-  for (int i = 0; i < n; ++i) {
-    if (!b[i].p) return GDN_EINVAL;
-    if (!aligned16(b[i].p)) return GDN_EALIGN;
-  }
-  for (int i = 0; i < n; ++i) {
-    const int r = check_io_ptr(b[i].p, any_host);
-    if (r != GDN_OK) return r;
-  }
-  return GDN_OK;
+  return check_list(b, n, true, any_host);
 }
 
 int status_of(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ECUDA; }
