@@ -1,0 +1,115 @@
+"""Launches whose token buffers hold more than 2^31 elements.
+
+Every kernel addresses its buffers with 64-bit offsets; these cases put
+the last tokens of a launch past element 2^31 of q, k, v and o, so an
+offset kept in 32 bits anywhere would read or write the wrong rows.  The
+bulk of each sequence is drawn on the GPU (seeded; unit-norm q and k,
+gates of the workload recipe).  The last two tokens come from
+gdn_inputs, with a reset gate at the first of them (g = -200: exp(g) is 0
+in fp32, so the state after it no longer depends on what came before).
+Their outputs and the final state must then be those of the same two
+tokens launched alone from any state:
+- bit for bit on the token-serial kernels, whose result for a token
+  depends only on the state and that token's inputs (a reset state is
+  k tmp^T whatever the earlier state was);
+- to the precision's tolerance against the oracle on the chunked path.
+
+Sizes: 48 value heads (16 key heads); one sequence of 350,000 tokens for
+the 8-column kernel (48 heads, fewer than SMs), four of 90,000 for the
+head-per-CTA kernel (192 heads), two of 350,000 for the chunked prefill
+(whose limit is T * vh < 2^31 per sequence).  Up to about 46 GB on the
+device.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import gated_deltanet_linear_gb300 as gdn
+import gdn_inputs
+from oracle.ref64 import max_rel
+from gpu_util import dev, empty, host
+
+pytestmark = pytest.mark.gpu
+
+KH, VH, D = 16, 48, 128
+RESET_G = -200.0
+TOL_MULTI = 1e-4
+TOL_CHUNK = {gdn.GDN_PREC_BF16X3: 1e-4, gdn.GDN_PREC_BF16: 8 * 2.0 ** -9}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    yield
+    torch.cuda.empty_cache()
+
+
+def _long_inputs(seed, B, T):
+    """q, k, v, g, beta of B sequences x T tokens on the device; tokens
+    T-2 and T-1 are those of `tail` (returned), with the reset at T-2."""
+    gen = torch.Generator(device="cuda").manual_seed(seed)
+
+    def unit(x):
+        return x / x.norm(dim=-1, keepdim=True)
+
+    q = unit(torch.randn(B, T, KH, D, device="cuda", generator=gen))
+    k = unit(torch.randn(B, T, KH, D, device="cuda", generator=gen))
+    v = torch.randn(B, T, VH, D, device="cuda", generator=gen)
+    g = -torch.nn.functional.softplus(
+        torch.randn(B, T, VH, device="cuda", generator=gen))
+    beta = torch.sigmoid(torch.randn(B, T, VH, device="cuda", generator=gen))
+    tail = gdn_inputs.make_inputs(seed, B=B, T=2)
+    tail.g[:, 0] = RESET_G
+    for big, small in ((q, tail.q), (k, tail.k), (v, tail.v), (g, tail.g),
+                       (beta, tail.beta)):
+        big[:, T - 2:] = dev(small)
+    assert B * T * VH * D > 2 ** 31
+    return (q, k, v, g, beta), tail
+
+
+def _tail_launch(tail):
+    S = dev(tail.S)
+    o = empty(tail.B, 2, VH, D)
+    gdn.gdn_step_m(S, S, None, *(dev(x) for x in (tail.q, tail.k, tail.v,
+                                                  tail.g, tail.beta)), o)
+    return S, o
+
+
+@pytest.mark.parametrize("B,T", [(1, 350_000), (4, 90_000)])
+def test_token_serial_beyond_2_31_elements(oracle_mod, B, T):
+    ins, tail = _long_inputs(7100 + B, B, T)
+    S = dev(gdn_inputs.make_inputs(7200 + B, B=B, T=1).S)
+    o = torch.empty(B, T, VH, D, device="cuda")
+    gdn.gdn_step_m(S, S, None, *ins, o)
+    o_tail = o[:, T - 2:].contiguous()
+    assert torch.isfinite(o_tail).all()
+    del ins, o
+    torch.cuda.empty_cache()
+    S2, o2 = _tail_launch(tail)
+    assert torch.equal(S, S2)
+    assert torch.equal(o_tail, o2)
+    S_ref, o_ref = oracle_mod.run_inputs(tail)
+    assert max_rel(host(S), S_ref, axes=(-2, -1)) < TOL_MULTI
+    assert max_rel(host(o_tail), o_ref, axes=(-2, -1)) < TOL_MULTI
+    assert gdn.gdn_wait_timeouts() == 0
+
+
+@pytest.mark.parametrize("precision", [gdn.GDN_PREC_BF16X3, gdn.GDN_PREC_BF16])
+def test_chunked_beyond_2_31_elements(oracle_mod, precision):
+    B, T = 2, 350_000                      # last chunk: 48 tokens (ragged)
+    ins, tail = _long_inputs(7300 + precision, B, T)
+    S = torch.zeros(B, VH, D, D, device="cuda")
+    o = torch.empty(B, T, VH, D, device="cuda")
+    gdn.gdn_prefill(S, *ins, o, precision=precision)
+    o_tail = o[:, T - 2:].contiguous()
+    del ins, o
+    torch.cuda.empty_cache()
+    assert gdn.gdn_prefill_timeouts() == 0
+    S_ref, o_ref = oracle_mod.run_inputs(tail)
+    es = max_rel(host(S), S_ref, axes=(-2, -1))
+    eo = max_rel(host(o_tail), o_ref, axes=(-2, -1))
+    print(f"chunked {precision}, {B} x {T} tokens: state {es:.3e} o {eo:.3e}")
+    assert es < TOL_CHUNK[precision] and eo < TOL_CHUNK[precision]
