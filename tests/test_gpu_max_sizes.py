@@ -1,8 +1,10 @@
-"""Launches whose token buffers hold more than 2^31 elements.
+"""Launches whose buffers hold more than 2^31 elements.
 
 Every kernel addresses its buffers with 64-bit offsets; these cases put
-the last tokens of a launch past element 2^31 of q, k, v and o, so an
-offset kept in 32 bits anywhere would read or write the wrong rows.  The
+the last rows of a launch past element 2^31 of its buffers, so an offset
+kept in 32 bits anywhere would read or write the wrong rows.
+
+Long sequences (token buffers beyond 2^31 elements).  The
 bulk of each sequence is drawn on the GPU (seeded; unit-norm q and k,
 gates of the workload recipe).  The last two tokens come from
 gdn_inputs, with a reset gate at the first of them (g = -200: exp(g) is 0
@@ -17,8 +19,14 @@ tokens launched alone from any state:
 Sizes: 48 value heads (16 key heads); one sequence of 350,000 tokens for
 the 8-column kernel (48 heads, fewer than SMs), four of 90,000 for the
 head-per-CTA kernel (192 heads), two of 350,000 for the chunked prefill
-(whose limit is T * vh < 2^31 per sequence).  Up to about 46 GB on the
-device.
+(whose limit is T * vh < 2^31 per sequence).
+
+Many sequences (state or checkpoint buffers beyond 2^31 elements): the
+last sequence gets the same state and tokens as the first, so its results
+must be the first's bit for bit, and the first's are checked against the
+oracle.
+
+Up to about 46 GB on the device.
 """
 
 import numpy as np
@@ -113,3 +121,73 @@ def test_chunked_beyond_2_31_elements(oracle_mod, precision):
     eo = max_rel(host(o_tail), o_ref, axes=(-2, -1))
     print(f"chunked {precision}, {B} x {T} tokens: state {es:.3e} o {eo:.3e}")
     assert es < TOL_CHUNK[precision] and eo < TOL_CHUNK[precision]
+
+
+def _wide_inputs(seed, B, M):
+    """B sequences x M tokens on the device, sequences 0 and B-1 both
+    holding the state and tokens of `one` (returned, B = 1)."""
+    gen = torch.Generator(device="cuda").manual_seed(seed)
+
+    def unit(x):
+        return x / x.norm(dim=-1, keepdim=True)
+
+    S = torch.randn(B, VH, D, D, device="cuda", generator=gen).mul_(0.02)
+    q = unit(torch.randn(B, M, KH, D, device="cuda", generator=gen))
+    k = unit(torch.randn(B, M, KH, D, device="cuda", generator=gen))
+    v = torch.randn(B, M, VH, D, device="cuda", generator=gen)
+    g = -torch.nn.functional.softplus(
+        torch.randn(B, M, VH, device="cuda", generator=gen))
+    beta = torch.sigmoid(torch.randn(B, M, VH, device="cuda", generator=gen))
+    one = gdn_inputs.make_inputs(seed, B=1, T=M)
+    for big, small in ((S, one.S), (q, one.q), (k, one.k), (v, one.v),
+                       (g, one.g), (beta, one.beta)):
+        big[0] = dev(small)[0]
+        big[B - 1] = dev(small)[0]
+    return S, (q, k, v, g, beta), one
+
+
+# (sequences, tokens, checkpoints): a state of 2,800 x 48 heads is 8.8 GB
+# (more than 2^31 elements), for one token (32-column kernel) and two
+# (head-per-CTA kernel); 400 x 48 heads x 8 tokens of checkpoints are 10 GB
+# (8-column kernel)
+WIDE = [(2800, 1, False), (2800, 2, False), (400, 8, True)]
+
+
+@pytest.mark.parametrize("B,M,ckpt", WIDE)
+def test_state_beyond_2_31_elements(oracle_mod, B, M, ckpt):
+    S, ins, one = _wide_inputs(7400 + M, B, M)
+    assert S.numel() * (M if ckpt else 1) > 2 ** 31
+    o = torch.empty(B, M, VH, D, device="cuda")
+    ck = torch.empty(M, B, VH, D, D, device="cuda") if ckpt else None
+    if M == 1:
+        gdn.gdn_step(S, *ins, o)
+    else:
+        gdn.gdn_step_m(S, S, ck, *ins, o)
+    torch.cuda.synchronize()
+    assert torch.equal(S[B - 1], S[0]) and torch.equal(o[B - 1], o[0])
+    if ckpt:
+        assert torch.equal(ck[:, B - 1], ck[:, 0])
+    S_ref, o_ref = oracle_mod.run_inputs(one)
+    tol = 1e-5 if M == 1 else TOL_MULTI
+    assert max_rel(host(S[:1]), S_ref, axes=(-2, -1)) < tol
+    assert max_rel(host(o[:1]), o_ref, axes=(-2, -1)) < tol
+    assert gdn.gdn_wait_timeouts() == 0
+    del S, ins, o, ck
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("precision", [gdn.GDN_PREC_BF16X3, gdn.GDN_PREC_BF16])
+def test_chunked_state_beyond_2_31_elements(oracle_mod, precision):
+    B, T = 2800, 70                        # two chunks, the second ragged
+    S, ins, one = _wide_inputs(7500 + precision, B, T)
+    o = torch.empty(B, T, VH, D, device="cuda")
+    gdn.gdn_prefill(S, *ins, o, precision=precision)
+    torch.cuda.synchronize()
+    assert gdn.gdn_prefill_timeouts() == 0
+    assert torch.equal(S[B - 1], S[0]) and torch.equal(o[B - 1], o[0])
+    S_ref, o_ref = oracle_mod.run_inputs(one)
+    es = max_rel(host(S[:1]), S_ref, axes=(-2, -1))
+    eo = max_rel(host(o[:1]), o_ref, axes=(-2, -1))
+    assert es < TOL_CHUNK[precision] and eo < TOL_CHUNK[precision]
+    del S, ins, o
+    torch.cuda.empty_cache()
