@@ -191,3 +191,56 @@ def test_chunked_state_beyond_2_31_elements(oracle_mod, precision):
     assert es < TOL_CHUNK[precision] and eo < TOL_CHUNK[precision]
     del S, ins, o
     torch.cuda.empty_cache()
+
+
+def test_layer_step_beyond_2_31_elements(oracle_mod):
+    """The layer step (convolution with history, normalisation, gates, then
+    the update) over one sequence of 210,000 tokens, whose raw projections
+    x hold more than 2^31 elements.  The last five rows of x, a and b come
+    from gdn_inputs; a = 1e4 at token T-2 makes g about -1e4 there, a reset.
+    The last two tokens then depend only on those five rows (three of
+    convolution history and two tokens): a launch of the two tokens with
+    the three rows as its history must give the same state, history and
+    outputs bit for bit, and the oracle agrees with them."""
+    T = 210_000
+    L = gdn_inputs.make_layer_inputs(7600, B=1, T=5)
+    conv_dim = L.x.shape[-1]
+    assert T * conv_dim > 2 ** 31
+    a_tail = L.a.copy()
+    a_tail[:, 3] = 1e4
+    gen = torch.Generator(device="cuda").manual_seed(7601)
+    x = torch.randn(1, T, conv_dim, device="cuda", generator=gen)
+    a = torch.randn(1, T, VH, device="cuda", generator=gen)
+    b = torch.randn(1, T, VH, device="cuda", generator=gen)
+    x[:, T - 5:] = dev(L.x)
+    a[:, T - 5:] = dev(a_tail)
+    b[:, T - 5:] = dev(L.b)
+    w = [dev(t) for t in (L.conv_w, L.A_log, L.dt_bias)]
+
+    def launch(S_in, hist_in, x_, a_, b_):
+        M = x_.shape[1]
+        S_out = torch.empty_like(S_in)
+        hist_out = torch.empty_like(hist_in)
+        o = torch.empty(1, M, VH, D, device="cuda")
+        ws = torch.empty(gdn.gdn_layer_workspace(1, L.kh, VH, M),
+                         dtype=torch.uint8, device="cuda")
+        gdn.gdn_layer_step_m(S_in, S_out, None, hist_in, hist_out, x_, w[0],
+                             a_, b_, w[1], w[2], o, L.kh, ws)
+        torch.cuda.synchronize()
+        return S_out, hist_out, o
+
+    S_big, h_big, o_big = launch(dev(L.S), dev(L.hist), x, a, b)
+    o_big = o_big[:, T - 2:].contiguous()
+    del x, a, b
+    torch.cuda.empty_cache()
+    x5, a5, b5 = dev(L.x), dev(a_tail), dev(L.b)
+    S2, h2, o2 = launch(dev(L.S), x5[:, :3].contiguous(), x5[:, 3:].contiguous(),
+                        a5[:, 3:].contiguous(), b5[:, 3:].contiguous())
+    assert torch.equal(S_big, S2) and torch.equal(h_big, h2)
+    assert torch.equal(o_big, o2)
+    S_ref, h_ref, o_ref = oracle_mod.run_layer(
+        L.S, L.x[:, :3], L.x[:, 3:], L.conv_w, a_tail[:, 3:], L.b[:, 3:],
+        L.A_log, L.dt_bias, L.kh)
+    assert np.array_equal(host(h2), h_ref)
+    assert max_rel(host(S2), S_ref, axes=(-2, -1)) < TOL_MULTI
+    assert max_rel(host(o2), o_ref, axes=(-2, -1)) < TOL_MULTI
