@@ -161,9 +161,12 @@ int steps_common(const gdn_shape *s, int M, const float *S_in, float *S_out,
                                    &host_inputs);
   if (r || s->B == 0) return r;
   cudaGetLastError();  // start from a clean per-thread error state
+  // a programmatic dependent of the previous kernel, reading nothing
+  // before it ends (launch_steps keeps the ordinary launch for grids that
+  // do not fill the GPU)
   return status_of(gdn::launch_steps(S_in, S_out, ckpt, q, k, v, g, beta, o,
-                                     s->B, s->kh, s->vh, M, stream, false,
-                                     host_inputs));
+                                     s->B, s->kh, s->vh, M, stream,
+                                     gdn::kOverlapAny, host_inputs));
 }
 
 }  // namespace
@@ -459,7 +462,7 @@ int gdn_layer_step_m(const gdn_shape *s, int M, int ck, float eps,
   // prologue never writes, before it waits for q, k, v, g, beta
   return status_of(gdn::launch_steps(S_in, S_out, ckpt, q, k, v, g, beta, o,
                                      s->B, s->kh, s->vh, M,
-                                     (cudaStream_t)stream, true));
+                                     (cudaStream_t)stream, gdn::kOverlapPrologue));
 }
 
 int gdn_layer_hist_rollback(const gdn_shape *s, int M, int ck,

@@ -39,9 +39,13 @@
 // programmatic dependent: it may start while the prologue still runs, puts
 // its first state units in flight (the prologue never writes the state),
 // and waits for the prologue's results (griddepcontrol.wait) before its
-// first read of the token inputs.  In an ordinary launch the wait returns at
-// once.  The kernel also lets its own dependents launch early; they wait
-// for its completion in the same way before reading its outputs.
+// first read of the token inputs.  A single-token launch that fills every
+// CTA slot is a programmatic dependent of whatever kernel came before (the
+// previous decode step, which writes the state): its CTAs are launched as
+// the previous kernel's CTAs leave, and wait for that kernel's end before
+// they read anything.  In an ordinary launch the wait returns at once.  The
+// kernels also let their own dependents launch early; those wait for the
+// completion in the same way before reading the outputs.
 //
 // Three layouts share that arithmetic:
 //   - gdn_step_c32_kernel: single-token launches (with host-memory
@@ -318,7 +322,8 @@ __global__ void __launch_bounds__(kWarps * 32, kWarpsPerSm / kWarps)
                      const float *__restrict__ k, const float *__restrict__ v,
                      const float *__restrict__ g,
                      const float *__restrict__ beta, float *__restrict__ o,
-                     int vh, int kh, int rep, int M, size_t nheads) {
+                     int vh, int kh, int rep, int M, size_t nheads,
+                     int wait_first) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -334,6 +339,8 @@ __global__ void __launch_bounds__(kWarps * 32, kWarpsPerSm / kWarps)
   const size_t mine = gw < nunits ? (nunits - gw + nw - 1) / nw : 0;
   const uint64_t pol = kOne ? l2_keep_priority() : 0;
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // behind a kernel that may write the state, nothing is read before it ends
+  if (wait_first) asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // Prologue: the first kStages - 1 units in flight (empty groups keep the
   // group count uniform).
@@ -512,7 +519,7 @@ __host__ __device__ constexpr int c32_smem() {
 // inputs; G = kHostGroups when the token inputs are in host memory, so that
 // the CTA's column groups share a head's q and k rows in L1 and the rows
 // cross the host link fewer times.
-template <int G>
+template <int G, bool kWaitFirst>
 __global__ void __launch_bounds__(G * kC32Warps * 32, kWarpsPerSm / (G * kC32Warps))
     gdn_step_c32_kernel(const float *S_in, float *S_out,
                         const float *__restrict__ q,
@@ -540,6 +547,8 @@ __global__ void __launch_bounds__(G * kC32Warps * 32, kWarpsPerSm / (G * kC32War
   const int r0 = 32 * warp + 8 * rq;
   const uint32_t lane_off = (uint32_t)(8 * rq * 128 + cq * 16);
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // behind a kernel that may write the state, nothing is read before it ends
+  if constexpr (kWaitFirst) asm volatile("griddepcontrol.wait;" ::: "memory");
 
   auto issue = [&](size_t i, int st) {
     const size_t u = blockIdx.x + i * gridDim.x;
@@ -557,7 +566,7 @@ __global__ void __launch_bounds__(G * kC32Warps * 32, kWarpsPerSm / (G * kC32War
     cp_async_commit();
   }
   // the token inputs may come from the kernel this one overlaps with
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if constexpr (!kWaitFirst) asm volatile("griddepcontrol.wait;" ::: "memory");
 
   for (size_t i = 0; i < mine; ++i) {
     {
@@ -795,7 +804,7 @@ __global__ void __launch_bounds__(kHWarps * 32, kHCtasPerSm)
                           const float *__restrict__ g,
                           const float *__restrict__ beta,
                           float *__restrict__ o, int vh, int kh, int rep, int M,
-                          unsigned nheads) {
+                          unsigned nheads, int wait_first) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rg = lane >> 2, cq = lane & 3;
@@ -813,6 +822,8 @@ __global__ void __launch_bounds__(kHWarps * 32, kHCtasPerSm)
       blockIdx.x < nheads ? (nheads - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
   const size_t hstride = (size_t)vh * kDim;     // o / v stride per token
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // behind a kernel that may write the state, nothing is read before it ends
+  if (wait_first) asm volatile("griddepcontrol.wait;" ::: "memory");
 
   auto head_of = [&](unsigned i) { return blockIdx.x + i * gridDim.x; };
   // offset of this lane's first state element (row rowA, column col) in
@@ -1130,14 +1141,24 @@ cudaError_t launch_maybe_overlapped(void (*kernel)(Params...), dim3 grid,
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+constexpr int kOverlapMaxTokens = 16;
+
 cudaError_t launch_steps(const float *S_in, float *S_out, float *ckpt,
                          const float *q, const float *k, const float *v,
                          const float *g, const float *beta, float *o, int B,
                          int kh, int vh, int M, cudaStream_t stream,
-                         bool overlap, bool host_inputs) {
+                         int overlap, bool host_inputs) {
   const size_t nheads = (size_t)B * vh;
   const size_t nunits = nheads * kUnitsPerHead;
   if (nunits == 0) return cudaSuccess;
+  // Behind any kernel only for short launches without checkpoints.  A long
+  // launch gains nothing from an earlier start, and its CTAs would wait on
+  // SM slots beside the previous launch's last CTAs (8 x 48 heads, 4096
+  // tokens: 7.37 ms against 6.75 ms).  Checkpointing launches, bound by
+  // their stores, measured mixed (64 x 48 heads, M = 4: 195.2 against
+  // 192.6 us; 32 x 48 heads, M = 2: 65.9 against 67.5 us).
+  if (overlap == kOverlapAny && (M > kOverlapMaxTokens || ckpt))
+    overlap = kOverlapNone;
   if (M == 1 && !ckpt) {
     // one token: the 32-column layout, G column groups of a head per CTA
     auto go32 = [&](auto kernel, int G) {
@@ -1153,9 +1174,21 @@ cudaError_t launch_steps(const float *S_in, float *S_out, float *ckpt,
                                      overlap, S_in, S_out, q, k, v, g, beta, o,
                                      vh, kh, vh / kh, nheads);
     };
-    if (!host_inputs) return go32(gdn_step_c32_kernel<1>, 1);
-    return kHostGroups == 4 ? go32(gdn_step_c32_kernel<4>, 4)
-                            : go32(gdn_step_c32_kernel<2>, 2);
+    static_assert(kHostGroups == 2, "host-input launches use two groups");
+    const int G = host_inputs ? kHostGroups : 1;
+    // Behind any kernel only when the grid fills every CTA slot.  There
+    // the launch and the start of the CTAs overlap the previous kernel's
+    // end: 64 x 48 heads, 62.8 us against 65.0 us.  A smaller launch (one
+    // sequence of 48 heads, state in L2) loses more by loading its state
+    // only after the wait: 2.83 us against 2.65 us a step from a graph.
+    const bool full = nheads * (kC32Groups / G) >=
+                      (size_t)sm_count() * (kWarpsPerSm / (G * kC32Warps));
+    if (overlap == kOverlapAny && !full) overlap = kOverlapNone;
+    if (overlap == kOverlapAny)
+      return host_inputs ? go32(gdn_step_c32_kernel<kHostGroups, true>, kHostGroups)
+                         : go32(gdn_step_c32_kernel<1, true>, 1);
+    return host_inputs ? go32(gdn_step_c32_kernel<kHostGroups, false>, kHostGroups)
+                       : go32(gdn_step_c32_kernel<1, false>, 1);
   }
   const size_t sms = (size_t)sm_count();
   if (!host_inputs && !ckpt && nheads >= sms) {
@@ -1169,19 +1202,25 @@ cudaError_t launch_steps(const float *S_in, float *S_out, float *ckpt,
     if (nheads > 0xffffffffull) return cudaErrorInvalidConfiguration;
     size_t ctas = sms * kHCtasPerSm;
     if (ctas > nheads) ctas = nheads;
+    // behind any kernel only when the grid fills every CTA slot (as for
+    // one token)
+    if (overlap == kOverlapAny && ctas < sms * kHCtasPerSm) overlap = kOverlapNone;
     const cudaError_t e = cudaFuncSetAttribute(
         gdn_steps_head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kHSmem);
     if (e != cudaSuccess) return e;
     return launch_maybe_overlapped(gdn_steps_head_kernel, dim3((unsigned)ctas),
                                    dim3(kHWarps * 32), kHSmem, stream, overlap,
                                    S_in, S_out, q, k, v, g, beta, o, vh, kh,
-                                   vh / kh, M, (unsigned)nheads);
+                                   vh / kh, M, (unsigned)nheads,
+                                   (int)(overlap == kOverlapAny));
   }
   const int wpc = M == 1 && host_inputs ? 8 : 4;
   const int smem = wpc == 8 ? smem_per_cta<8>() : smem_per_cta<4>();
   size_t ctas = (nunits + wpc - 1) / wpc;
   const size_t cap = sms * (kWarpsPerSm / wpc);
   if (ctas > cap) ctas = cap;
+  if (overlap == kOverlapAny && ctas < cap) overlap = kOverlapNone;
+  const int wait_first = overlap == kOverlapAny;
   const dim3 grid((unsigned)ctas), block(wpc * 32);
   auto go = [&](auto kernel, float *ck) {
     cudaError_t e = cudaFuncSetAttribute(
@@ -1189,7 +1228,7 @@ cudaError_t launch_steps(const float *S_in, float *S_out, float *ckpt,
     if (e != cudaSuccess) return e;
     return launch_maybe_overlapped(kernel, grid, block, smem, stream,
                                    overlap, S_in, S_out, ck, q, k, v, g, beta,
-                                   o, vh, kh, vh / kh, M, nheads);
+                                   o, vh, kh, vh / kh, M, nheads, wait_first);
   };
   cudaError_t e;
   if (ckpt)

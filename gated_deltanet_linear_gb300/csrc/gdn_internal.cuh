@@ -9,18 +9,27 @@ namespace gdn {
 
 constexpr int kDim = 128;  // kd == vd: the only head size the kernels serve
 
+// Launch modes of launch_steps.
+//   kOverlapNone: an ordinary launch.
+//   kOverlapPrologue: a programmatic dependent of the previous kernel on the
+//     stream, which must not write S_in (the kernel starts loading the
+//     state before it waits for that kernel): the layer prologue.
+//   kOverlapAny: a programmatic dependent of whatever kernel came before;
+//     the kernel reads nothing before that kernel has ended, so it only
+//     takes over the launch and the start of its CTAs.  Applied to grids
+//     that fill every CTA slot; smaller grids launch ordinarily.
+constexpr int kOverlapNone = 0, kOverlapPrologue = 1, kOverlapAny = 2;
+
 // Token-serial update of every head over M tokens (gdn_step, gdn_step_m and
 // the fp32 prefill path).  Pointers and layouts as in gdn.h; S_out may equal
-// S_in.  ckpt may be nullptr.  overlap: launch as a programmatic dependent of
-// the previous kernel on the stream, which then must not write S_in (the
-// kernel starts loading the state before it waits for that kernel).
+// S_in.  ckpt may be nullptr.  overlap: one of the modes above.
 // host_inputs: some token input is in mapped host memory (single-token
 // launches then use larger CTAs, whose warps share the inputs in L1).
 cudaError_t launch_steps(const float *S_in, float *S_out, float *ckpt,
                          const float *q, const float *k, const float *v,
                          const float *g, const float *beta, float *o, int B,
                          int kh, int vh, int M, cudaStream_t stream,
-                         bool overlap = false, bool host_inputs = false);
+                         int overlap = kOverlapNone, bool host_inputs = false);
 
 // Layer prologue (conv1d + SiLU with a width-4 history, q/k normalisation,
 // gates) writing the token inputs q, k, v, g, beta of M tokens.  hist_in and
