@@ -410,7 +410,8 @@ int gdn_layer_prologue_m(const gdn_shape *s, int M, int ck, float eps,
   cudaGetLastError();
   return status_of(gdn::launch_layer_prologue(
       hist_in, hist_out, x, conv_w, a, b, A_log, dt_bias, eps, q, k, v, g,
-      beta, s->B, s->kh, s->vh, M, (cudaStream_t)stream));
+      beta, s->B, s->kh, s->vh, M, (cudaStream_t)stream,
+      M <= gdn::kOverlapMaxTokens));
 }
 
 size_t gdn_layer_workspace(const gdn_shape *s, int M) {
@@ -454,9 +455,12 @@ int gdn_layer_step_m(const gdn_shape *s, int M, int ck, float eps,
   r = steps_common_check(sh, M, S_in, S_out, ckpt, q, k, v, g, beta, o);
   if (r) return r;
   cudaGetLastError();
+  // the prologue starts behind the kernel before it (short launches) and
+  // touches nothing before that kernel has ended
   cudaError_t e = gdn::launch_layer_prologue(
       hist_in, hist_out, x, conv_w, a, b, A_log, dt_bias, eps, q, k, v, g,
-      beta, s->B, s->kh, s->vh, M, (cudaStream_t)stream);
+      beta, s->B, s->kh, s->vh, M, (cudaStream_t)stream,
+      M <= gdn::kOverlapMaxTokens);
   if (e != cudaSuccess) return GDN_ECUDA;
   // the update overlaps the prologue's tail: it loads the state, which the
   // prologue never writes, before it waits for q, k, v, g, beta

@@ -44,8 +44,12 @@
 // previous decode step, which writes the state): its CTAs are launched as
 // the previous kernel's CTAs leave, and wait for that kernel's end before
 // they read anything.  In an ordinary launch the wait returns at once.  The
-// kernels also let their own dependents launch early; those wait for the
-// completion in the same way before reading the outputs.
+// kernels let their own dependents be scheduled once every CTA (or warp)
+// has reached its last unit; those wait for the completion in the same way
+// before reading the outputs.  Signalled at the start instead, a following
+// layer prologue's small CTAs waited beside the running update for its
+// whole length and slowed it (64 x 48-head layer step: 90.0 us against
+// 67.9 us).
 //
 // Three layouts share that arithmetic:
 //   - gdn_step_c32_kernel: single-token launches (with host-memory
@@ -338,7 +342,6 @@ __global__ void __launch_bounds__(kWarps * 32, kWarpsPerSm / kWarps)
   const size_t nw = (size_t)gridDim.x * kWarps;
   const size_t mine = gw < nunits ? (nunits - gw + nw - 1) / nw : 0;
   const uint64_t pol = kOne ? l2_keep_priority() : 0;
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // behind a kernel that may write the state, nothing is read before it ends
   if (wait_first) asm volatile("griddepcontrol.wait;" ::: "memory");
 
@@ -410,6 +413,8 @@ __global__ void __launch_bounds__(kWarps * 32, kWarpsPerSm / kWarps)
     }
   }
   for (size_t i = 0; i < mine; ++i) {
+    // dependents may be scheduled once every warp is on its last unit
+    if (i + 1 == mine) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     {
       const size_t ahead = i + kStages - 1;
       if (ahead < mine)
@@ -546,7 +551,6 @@ __global__ void __launch_bounds__(G * kC32Warps * 32, kWarpsPerSm / (G * kC32War
   const uint64_t pol = l2_keep_priority();
   const int r0 = 32 * warp + 8 * rq;
   const uint32_t lane_off = (uint32_t)(8 * rq * 128 + cq * 16);
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // behind a kernel that may write the state, nothing is read before it ends
   if constexpr (kWaitFirst) asm volatile("griddepcontrol.wait;" ::: "memory");
 
@@ -569,6 +573,10 @@ __global__ void __launch_bounds__(G * kC32Warps * 32, kWarpsPerSm / (G * kC32War
   if constexpr (!kWaitFirst) asm volatile("griddepcontrol.wait;" ::: "memory");
 
   for (size_t i = 0; i < mine; ++i) {
+    // dependents may be scheduled once every CTA is on its last unit: a
+    // following step's CTAs then take the slots as these CTAs leave, and
+    // small CTAs of another kernel do not wait beside this one's for long
+    if (i + 1 == mine) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     {
       const size_t ahead = i + kStages - 1;
       if (ahead < mine) issue(ahead, (int)(ahead % kStages));
@@ -821,7 +829,6 @@ __global__ void __launch_bounds__(kHWarps * 32, kHCtasPerSm)
   const unsigned mine =
       blockIdx.x < nheads ? (nheads - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
   const size_t hstride = (size_t)vh * kDim;     // o / v stride per token
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // behind a kernel that may write the state, nothing is read before it ends
   if (wait_first) asm volatile("griddepcontrol.wait;" ::: "memory");
 
@@ -918,6 +925,8 @@ __global__ void __launch_bounds__(kHWarps * 32, kHCtasPerSm)
   unsigned i = 0;
   int m = 0, sl = 0, use = 0;
   for (; i < mine; ++i) {
+    // dependents may be scheduled once every CTA is on its last unit
+    if (i + 1 == mine) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     cp_async_wait<0>();  // unit i has landed (this lane's bytes)
 #pragma unroll
     for (int r = 0; r < 16; ++r) s[r] = lds128(stage + r * 512);
@@ -1140,8 +1149,6 @@ cudaError_t launch_maybe_overlapped(void (*kernel)(Params...), dim3 grid,
   cfg.numAttrs = overlap ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
-
-constexpr int kOverlapMaxTokens = 16;
 
 cudaError_t launch_steps(const float *S_in, float *S_out, float *ckpt,
                          const float *q, const float *k, const float *v,

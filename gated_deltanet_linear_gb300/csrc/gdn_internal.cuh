@@ -19,6 +19,10 @@ constexpr int kDim = 128;  // kd == vd: the only head size the kernels serve
 //     takes over the launch and the start of its CTAs.  Applied to grids
 //     that fill every CTA slot; smaller grids launch ordinarily.
 constexpr int kOverlapNone = 0, kOverlapPrologue = 1, kOverlapAny = 2;
+// Launches of more tokens than this start ordinarily: a long launch gains
+// nothing from an earlier start, and its CTAs would wait on SM slots beside
+// the previous launch's last CTAs.
+constexpr int kOverlapMaxTokens = 16;
 
 // Token-serial update of every head over M tokens (gdn_step, gdn_step_m and
 // the fp32 prefill path).  Pointers and layouts as in gdn.h; S_out may equal
@@ -33,14 +37,17 @@ cudaError_t launch_steps(const float *S_in, float *S_out, float *ckpt,
 
 // Layer prologue (conv1d + SiLU with a width-4 history, q/k normalisation,
 // gates) writing the token inputs q, k, v, g, beta of M tokens.  hist_in and
-// hist_out must not overlap.
+// hist_out must not overlap.  overlap: launch as a programmatic dependent of
+// the kernel before it; the prologue reads and writes nothing before that
+// kernel has ended, and only then lets its own dependents start.
 cudaError_t launch_layer_prologue(const float *hist_in, float *hist_out,
                                   const float *x, const float *conv_w,
                                   const float *a, const float *b,
                                   const float *A_log, const float *dt_bias,
                                   float eps, float *q, float *k, float *v,
                                   float *g, float *beta, int B, int kh, int vh,
-                                  int M, cudaStream_t stream);
+                                  int M, cudaStream_t stream,
+                                  bool overlap = false);
 
 // Gated RMSNorm of `rows` rows of 128 channels (see gdn_gated_rmsnorm_m);
 // y may equal o.

@@ -59,8 +59,12 @@ __device__ __forceinline__ float silu(float x) {
 // of every value head.  Lane l owns channels 4l .. 4l+3 of its row.
 __global__ void __launch_bounds__(128)
     layer_prologue_kernel(const PrologueArgs P) {
+  // behind the kernel before it (which may write x, the history or the
+  // state): nothing is read or written before that kernel has ended
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // the state kernel that follows may start now: it loads the state (which
-  // this kernel never writes) and waits for these results before reading them
+  // this kernel never writes, and whose last writer has ended) and waits for
+  // these results before reading them
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const size_t gw = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -199,7 +203,7 @@ cudaError_t launch_layer_prologue(const float *hist_in, float *hist_out,
                                   const float *A_log, const float *dt_bias,
                                   float eps, float *q, float *k, float *v,
                                   float *g, float *beta, int B, int kh, int vh,
-                                  int M, cudaStream_t stream) {
+                                  int M, cudaStream_t stream, bool overlap) {
   PrologueArgs P;
   P.x = x;
   P.conv_w = conv_w;
@@ -224,8 +228,16 @@ cudaError_t launch_layer_prologue(const float *hist_in, float *hist_out,
   if (warps == 0) return cudaSuccess;
   const size_t blocks = (warps + 3) / 4;
   if (blocks > 0x7fffffffull) return cudaErrorInvalidConfiguration;
-  layer_prologue_kernel<<<(unsigned)blocks, 128, 0, stream>>>(P);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(128);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, layer_prologue_kernel, P);
 }
 
 cudaError_t launch_gate_norm(const float *o, const float *z, const float *w,
