@@ -138,6 +138,13 @@ int gdn_step(const gdn_shape *shape, float *S, const float *q, const float *k,
  * 1 <= M <= GDN_MAX_TOKENS (GDN_ERANGE otherwise).  Output m is
  * bit-identical to the m-th of M successive gdn_step calls on the same
  * inputs, and ckpt[m] to the state after it.
+ * Stream order: a launch of at most 16 tokens without checkpoints whose
+ * grid fills the GPU starts as a programmatic dependent of the kernel
+ * before it on the stream.  Its CTAs may become resident before that
+ * kernel ends, but they read and write no memory until it has completed,
+ * so the call sees every earlier write on the stream, as an ordinary launch
+ * would.  The same holds for gdn_step, gdn_layer_step_m and
+ * gdn_layer_prologue_m.
  */
 int gdn_step_m(const gdn_shape *shape, int M, const float *S_in, float *S_out,
                float *ckpt, const float *q, const float *k, const float *v,
