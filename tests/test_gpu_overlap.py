@@ -107,3 +107,34 @@ def test_layer_steps_back_to_back():
     assert torch.equal(S[T % 2], S_m) and torch.equal(hist[T % 2], hist_m)
     for m in range(T):
         assert torch.equal(outs[m][:, 0], o_m[:, m]), m
+
+
+def test_two_streams_back_to_back():
+    """Two batches decoded on two streams at once, each a run of
+    back-to-back steps: every step on a stream starts behind the one
+    before it on the same stream while the other stream's kernels run
+    beside it.  Results equal the same steps run on one stream."""
+    T = 6
+    inps = [gdn_inputs.make_inputs(8400 + i, B=B, T=T) for i in range(2)]
+    per_tok, states, outs = [], [], []
+    for inp in inps:
+        q, k, v, g, beta = _tokens(inp)
+        per_tok.append([tuple(x[:, t:t + 1].contiguous()
+                              for x in (q, k, v, g, beta)) for t in range(T)])
+        states.append(dev(inp.S))
+        outs.append([empty(B, 1, VH, D) for _ in range(T)])
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    for t in range(T):
+        for i in range(2):
+            gdn.gdn_step(states[i], *per_tok[i][t], outs[i][t],
+                         stream=streams[i])
+    torch.cuda.synchronize()
+    for i, inp in enumerate(inps):
+        S = dev(inp.S)
+        for t in range(T):
+            o = empty(B, 1, VH, D)
+            gdn.gdn_step(S, *per_tok[i][t], o)
+            assert torch.equal(o, outs[i][t]), (i, t)
+        torch.cuda.synchronize()
+        assert torch.equal(S, states[i]), i
