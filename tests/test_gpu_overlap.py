@@ -138,3 +138,40 @@ def test_two_streams_back_to_back():
             assert torch.equal(o, outs[i][t]), (i, t)
         torch.cuda.synchronize()
         assert torch.equal(S, states[i]), i
+
+
+def test_decode_steps_back_to_back_in_a_graph():
+    """Eight back-to-back full-grid steps captured in one CUDA graph (the
+    programmatic dependencies between them become graph edges) and
+    replayed: the same bits as the steps made eagerly."""
+    T = 8
+    inp = gdn_inputs.make_inputs(8500, B=B, T=T)
+    q, k, v, g, beta = _tokens(inp)
+    per_tok = [tuple(x[:, t:t + 1].contiguous() for x in (q, k, v, g, beta))
+               for t in range(T)]
+    outs = [empty(B, 1, VH, D) for _ in range(T)]
+    S0 = dev(inp.S)
+    S = S0.clone()
+
+    def steps():
+        for t in range(T):
+            gdn.gdn_step(S, *per_tok[t], outs[t])
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        steps()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        steps()
+    S.copy_(S0)
+    graph.replay()
+    torch.cuda.synchronize()
+    S_ref = S0.clone()
+    for t in range(T):
+        o = empty(B, 1, VH, D)
+        gdn.gdn_step(S_ref, *per_tok[t], o)
+        assert torch.equal(o, outs[t]), t
+    assert torch.equal(S, S_ref)
