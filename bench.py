@@ -561,6 +561,12 @@ def prefill_parts(torch, gdn, tens, stream, peaks, parts):
     tc_flops = (2 * 128 * 64 * 128 + 2 * 128 * 128 * 128 +
                 2 * 128 * 64 * 64 + 2 * 128 * 64 * 64 +
                 2 * 128 * 128 * 64) * (pin_.T // 64) * pin_.B * pin_.vh
+    # algorithmic HBM bytes: q, k, v, g, beta read and o written once, the
+    # state read and written once
+    hbm_bytes = (4 * pin_.B * pin_.T * (2 * pin_.kh * D + 2 * pin_.vh * D +
+                                        2 * pin_.vh) +
+                 2 * 4 * pin_.B * pin_.vh * D * D)
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
     for prec, name, reps in ((gdn.GDN_PREC_FP32, "fp32", 3),
                              (gdn.GDN_PREC_BF16X3, "bf16x3", 10),
                              (gdn.GDN_PREC_BF16, "bf16", 10)):
@@ -574,17 +580,29 @@ def prefill_parts(torch, gdn, tens, stream, peaks, parts):
             "ms": pms, "tokens_per_s": toks / (pms * 1e-3),
             "head_steps_per_s": toks * pin_.vh / (pms * 1e-3),
             "tflops_fp32_equiv": flops / (pms * 1e-3) / 1e12}
+        hbm_floor = hbm_bytes / (hbm_peak * 1e9)
+        entry.update({"bytes_per_launch": hbm_bytes,
+                      "hbm_floor_us": hbm_floor * 1e6})
         if prec == gdn.GDN_PREC_FP32:
-            entry["note"] = "token-serial fp32 path"
+            fp_floor = fp32_floor_s(toks * pin_.vh, 2070.0)
+            entry.update({"fp32_floor_us": fp_floor * 1e6,
+                          "frac_of_max_floor": max(hbm_floor, fp_floor) / (pms * 1e-3),
+                          "note": "token-serial fp32 path"})
         else:
             mult = 3 if prec == gdn.GDN_PREC_BF16X3 else 1
             ach = tc_flops * mult / (pms * 1e-3) / 1e12
             peak = float(peaks.get("bf16_tflops_sustained",
                                    peaks.get("bf16_tflops", 1900.0)))
+            tensor_floor = tc_flops * mult / (peak * 1e12)
             entry.update({"tensor_tflops": ach, "tensor_peak_tflops": peak,
                           "tensor_frac": ach / peak,
+                          "tensor_floor_us": tensor_floor * 1e6,
+                          "frac_of_max_floor":
+                              max(hbm_floor, tensor_floor) / (pms * 1e-3),
                           "note": "chunk-parallel form on tcgen05; "
-                                  "executed MMA flops (x3 for split-bf16)"})
+                                  "executed MMA flops (x3 for split-bf16); "
+                                  "frac_of_max_floor against the larger of "
+                                  "the HBM and tensor floors"})
         parts[f"prefill_b8_t4096_{name}"] = entry
     del pq, pk, pv, pg, pb, Sp, po
 
