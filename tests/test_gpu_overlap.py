@@ -175,3 +175,28 @@ def test_decode_steps_back_to_back_in_a_graph():
         gdn.gdn_step(S_ref, *per_tok[t], o)
         assert torch.equal(o, outs[t]), t
     assert torch.equal(S, S_ref)
+
+
+def test_host_input_launches_back_to_back():
+    """Two-token launches whose token inputs and outputs are page-locked
+    host memory (the 8-column kernel, a full grid at 64 sequences, started
+    behind the launch before it), back to back in place: the same bits as
+    one launch over all tokens with device-resident inputs."""
+    M, n = 2, 3
+    inp = gdn_inputs.make_inputs(8600, B=B, T=n * M)
+    host = [torch.from_numpy(x.copy()) for x in
+            (inp.q, inp.k, inp.v, inp.g, inp.beta)]
+    chunks = [tuple(x[:, i * M:(i + 1) * M].contiguous().pin_memory()
+                    for x in host) for i in range(n)]
+    outs = [torch.empty(B, M, VH, D).pin_memory() for _ in range(n)]
+    S = dev(inp.S)
+    torch.cuda.synchronize()
+    for i in range(n):
+        gdn.gdn_step_m(S, S, None, *chunks[i], outs[i])
+    S_m = dev(inp.S)
+    o_m = empty(B, n * M, VH, D)
+    gdn.gdn_step_m(S_m, S_m, None, *_tokens(inp), o_m)
+    torch.cuda.synchronize()
+    assert torch.equal(S, S_m)
+    for i in range(n):
+        assert torch.equal(outs[i], o_m[:, i * M:(i + 1) * M].cpu()), i
