@@ -397,6 +397,31 @@ def verify_parts(torch, gdn, tens, stream, hbm_peak, parts, steps,
                     "fp32_floor_us": fp_floor * 1e6,
                     "hbm_floor_us": hbm_floor * 1e6,
                     "frac_of_max_floor": max(hbm_floor, fp_floor) / (vms * 1e-3)}
+        rname = f"{wname}_rollback_m8"
+        if case is None or case == rname:
+            # per-sequence rollback after an 8-token verify: sequence b keeps
+            # m[b] of the 8 tokens (seeded, 0..8), i.e. S[b] = snap[b] or
+            # ckpt[m[b] - 1][b]; one state read and one written per launch
+            snap = tens(vin.S)
+            rng = np.random.default_rng(gdn_inputs.SEED_BASE + 6)
+            m_dev = torch.from_numpy(
+                rng.integers(0, 9, size=vin.B).astype(np.int32)).to(dev)
+
+            def rstep(i):
+                gdn.gdn_rollback_seq(Sv[i % NSETS], 8, m_dev, snap, ck, vin.kh,
+                                     stream=stream)
+            for i in range(warmup):
+                rstep(i)
+            rms = time_launches(torch, rstep, max(20, min(200, steps)), stream)
+            rbytes = 2 * Sv[0].numel() * 4
+            parts[rname] = {
+                "ms": rms, "gbs": rbytes / (rms * 1e-3) / 1e9,
+                "frac_of_measured_hbm": rbytes / (rms * 1e-3) / 1e9 / hbm_peak,
+                "bytes_per_launch": rbytes,
+                "note": "gdn_rollback_seq after an 8-token verify: each "
+                        "sequence's state restored from the snapshot or one "
+                        "of its 8 checkpoints (accepted counts 0..8, seeded)"}
+            del snap
         del Sv, ck
         torch.cuda.empty_cache()
 
